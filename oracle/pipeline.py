@@ -1,0 +1,45 @@
+"""The five stages composed (oracle; test infrastructure only).
+
+Stage order follows [P-V41] ("DeepSeek-V4.1 模型结构（5）：记忆，Engram")
+§"哈希函数" -> §"一层只有一张表" -> §"196B 参数怎么存、怎么取" -> §"门控", and the
+summary of [P-LMNT] ("Engram条件记忆：DeepSeek-V4.1-Flash中196B稀疏参数N-gram哈希查表的实现原理")
+§小结: compress tokens -> rolling XOR hash of 2/3/4-grams -> prime buckets in
+an FP8 table -> gate decides how much is injected.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+from . import dequant, gate, hashing
+from .layout import Layout
+
+
+@dataclasses.dataclass
+class LayerResult:
+    rows: np.ndarray       # int64 [T][n_cols]
+    mask: np.ndarray       # bool [T]
+    hist: np.ndarray       # int64 [S][max_ngram-1]
+    e: np.ndarray          # float64 [T][n_cols*256] (bf16 values)
+    gate: np.ndarray       # float64 [T][hc]
+    v: np.ndarray          # float64 [T][H] (unrounded)
+    h_out: np.ndarray      # float64 [T][hc][H] (bf16 values)
+
+
+def layer_forward(layout: Layout, layer: int, raw_ids, cu_seqlens, token_map, table_rows,
+                  wkv, h, q_w, k_w, hist: Optional[np.ndarray] = None, eps: float = 1e-6,
+                  clamp: float = 1e-6, score_scale=None) -> LayerResult:
+    """Prefill of one Engram layer on packed sequences.
+
+    wkv: float64 [n_cols*256][(hc+1)H]; h: float64 [T][hc][H].
+    """
+    rows, mask, new_hist = hashing.hash_prefill(raw_ids, cu_seqlens, token_map, layout, layer, hist)
+    e = dequant.gather_dequant(rows, table_rows)
+    hc, H = h.shape[1], h.shape[2]
+    kv = gate.project(e, wkv)
+    k, v = gate.split_kv(kv, H, hc)
+    g = gate.gate(h, k, q_w, k_w, mask, eps, clamp, score_scale)
+    h_out = gate.residual(h, g, v, mask)
+    return LayerResult(rows, mask, new_hist, e, g, v, h_out)
