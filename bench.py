@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Throughput of the Engram layer prefill (hash -> gather -> project -> gate/add).
+
+Default workload: 4 x 4096 Zipf(1.1) tokens with 5% image (DEAD) spans,
+compressed vocabulary 99092, a 48,004,402-row table (12.67 GB of E4M3+E8M0
+rows) from base 2,000,000, hidden 5120, 4 residual streams, wkv [6144, 25600].
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line is printed by rank 0.  A "step" is one pass of the whole layer
+over one batch of 16384 tokens.  Timing: CUDA events on the launching stream
+around every step; the L2 cache is flushed (a 512 MB write) before every
+step, outside the events.  Under torchrun every rank runs its own batch (no
+collective on the data path, weak scaling) and the slowest rank's time is
+used.  ``--impl reference`` times the CPU oracle on a bounded sample of the
+same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Engram layer tokens/s (hash+gather+gate) at T=16k; gather HBM GB/s vs peak"
+GATHER_BYTES_PER_TOKEN = 4 + 24 * 264 + 24 * 256 * 2   # raw id + 24 rows + bf16 e = 18,628 B
+KERNEL_FILES = ["project.cu", "gather.cu", "hash.cu", "gate.cu", "engram_internal.h"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="prefill")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--cpu-sample", type=int, default=2048, help="tokens of the oracle CPU baseline sample")
+    p.add_argument("--ref-sample", type=int, default=128, help="tokens per reference-arm step")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def workload_desc(w):
+    return (f"{w.name}: {w.n_seqs} x {w.seq_len} Zipf(1.1) tokens, {int(w.dead_frac * 100)}% DEAD spans, "
+            f"V_raw {w.v_raw} -> V {w.v}, 24 primes above {w.base_rows}, hidden {w.hidden}, hc {w.hc}, "
+            f"wkv [6144, {(w.hc + 1) * w.hidden}]")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_FILES:
+        with open(os.path.join(ROOT, "hashed_gram_conditional_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches the kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return {}
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash():
+        return {}
+    return d.get("per_launch_bytes", {})
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", self.gpu_id], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------- inputs
+
+
+def make_inputs(w, seed, dev):
+    import torch
+    import hashed_gram_conditional_gb300 as eg
+    from workloads import layer_weights, prefill_batch, residual_bits, token_map
+
+    tm = token_map(w.v_raw, w.v, w.seed)
+    lay = eg.build_layout(w.v, w.base_rows, [w.layer_id], pad_id=int(tm[0]), expected_vocab=w.v)
+    total = lay.total_rows(0)
+    table = torch.empty(total * eg.ROW_BYTES, dtype=torch.uint8, device=dev)
+    eg.engram_fill_synthetic_table(table, total, w.seed)
+    lw = layer_weights(w)
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    wkv = bf16(lw.wkv_bits)
+    layer = eg.EngramLayer(lay, 0, table, torch.from_numpy(tm).to(dev), eg.engram_pack_wkv(wkv),
+                           torch.from_numpy(lw.q_w).to(dev), torch.from_numpy(lw.k_w).to(dev))
+    del wkv
+    b = prefill_batch(w, seed=seed)
+    h_bits = residual_bits(len(b.raw_ids), w.hc, w.hidden, seed)
+    return dict(tm=tm, lay=lay, layer=layer, lw=lw, batch=b, h_bits=h_bits, bf16=bf16)
+
+
+# ------------------------------------------------------------------------- our arm
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+    import hashed_gram_conditional_gb300 as eg
+    from workloads import WORKLOADS
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, w.seed + rank, dev)
+    layer, b = inp["layer"], inp["batch"]
+    T = len(b.raw_ids)
+    raw = torch.from_numpy(b.raw_ids).to(dev)
+    cu = torch.from_numpy(b.cu_seqlens).to(dev)
+    h = inp["bf16"](inp["h_bits"])
+    h0 = h.clone()
+    hist = torch.full((w.n_seqs, 3), inp["lay"].pad_id, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    b_ = layer._buffers(T, dev)
+
+    def step(ev=None):
+        # one pass of the whole layer; events between the stage launches when timing
+        if ev is not None:
+            ev[0].record(stream)
+        eg.engram_hash(layer.layout, 0, raw, cu, layer.token_map, hist, b_["rows"], b_["mask"], status)
+        if ev is not None:
+            ev[1].record(stream)
+        eg.engram_gather_dequant(layer.table, layer.total_rows, b_["rows"], b_["e"], status)
+        if ev is not None:
+            ev[2].record(stream)
+        eg.engram_project(b_["e"], layer.wkv_packed, h, layer.q_w, layer.k_w, b_["partials"], b_["v"], status)
+        if ev is not None:
+            ev[3].record(stream)
+        eg.engram_gate_add(b_["partials"], b_["v"], h, b_["mask"], layer.eps, layer.clamp, layer.score_scale)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) is not None else str(local)
+    sampler = ClockSampler(gpu_id)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler's first reading land
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        step(events[k])
+    torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    st = int(status.item())
+
+    def ms(k, i, j):
+        return events[k][i].elapsed_time(events[k][j])
+
+    step_ms = [ms(k, 0, 4) for k in range(args.steps)]
+    stage = {name: [ms(k, i, i + 1) for k in range(args.steps)]
+             for i, name in enumerate(["hash", "gather", "project", "gate_add"])}
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+
+    # ---- end to end: host buffers through the public layer API
+    e2e = None
+    if args.e2e_steps > 0:
+        raw_h = torch.from_numpy(b.raw_ids).pin_memory()
+        cu_h = torch.from_numpy(b.cu_seqlens).pin_memory()
+        h_host = h0.cpu().pin_memory()
+        out_host = torch.empty_like(h_host).pin_memory()
+        raw_d, cu_d, h_d = torch.empty_like(raw), torch.empty_like(cu), torch.empty_like(h)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            raw_d.copy_(raw_h, non_blocking=True)
+            cu_d.copy_(cu_h, non_blocking=True)
+            h_d.copy_(h_host, non_blocking=True)
+            layer.prefill(raw_d, cu_d, h_d, hist, status)
+            out_host.copy_(h_d, non_blocking=True)
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(args.e2e_steps):
+            flush.zero_()
+            e0.record(stream)
+            raw_d.copy_(raw_h, non_blocking=True)
+            cu_d.copy_(cu_h, non_blocking=True)
+            h_d.copy_(h_host, non_blocking=True)
+            layer.prefill(raw_d, cu_d, h_d, hist, status)
+            out_host.copy_(h_d, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1) / 1e3
+        if world > 1:
+            t = torch.tensor([tot], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            tot = float(t.item())
+        h2d = raw_h.numel() * 4 + cu_h.numel() * 8 + h_host.numel() * 2
+        e2e = {"value": world * T * args.e2e_steps / tot, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(out_host.numel() * 2), "steps": args.e2e_steps,
+               "api": "EngramLayer.prefill with pinned host inputs/outputs"}
+
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    sustained = total_s >= 2.0
+    tf_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    flops = 2.0 * T * 6144 * (w.hc + 1) * w.hidden
+    proj_s = statistics.mean(stage["project"]) / 1e3
+    gat_s = statistics.mean(stage["gather"]) / 1e3
+    traffic = profiled_traffic()
+    roof = {"bound": "tensor", "kernel": "project_kernel (tcgen05 wkv GEMM + fused gate partials)",
+            "achieved": flops / proj_s / 1e12, "peak": tf_peak, "unit": "TFLOP/s",
+            "frac": flops / proj_s / 1e12 / tf_peak, "traffic": traffic.get("project_kernel"),
+            "algorithmic_per_launch": f"{flops:.4g} FLOP (2*T*6144*{(w.hc + 1) * w.hidden}, T={T})",
+            "peak_source": f"{peak_src} bf16_tflops{'_sustained' if sustained else ''}"}
+    gbytes = GATHER_BYTES_PER_TOKEN * T
+    roof_g = {"bound": "hbm", "kernel": "gather_dequant_kernel", "achieved": gbytes / gat_s / 1e9,
+              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbytes / gat_s / 1e9 / peaks["hbm_gbs"],
+              "traffic": traffic.get("gather_dequant_kernel"),
+              "algorithmic_per_launch": f"{gbytes} B ({GATHER_BYTES_PER_TOKEN} B/token, T={T})",
+              "peak_source": f"{peak_src} hbm_gbs"}
+    out = {
+        "metric": METRIC,
+        "value": world * T * args.steps / total_s,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_s / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded Zipf tokens, SplitMix64 table, N(0,0.02) wkv, N(0,1) residual)",
+        "config": {"workload": workload_desc(w), "tokens_per_step": T, "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every step (512 MB write, outside the timed events)"},
+        "stages_ms": {k: statistics.mean(v) for k, v in stage.items()},
+        "roofline": roof,
+        "roofline_gather": roof_g,
+        "gpu_launches": args.steps * 5,
+        "clocks": clocks,
+        "e2e": e2e,
+        "wall_s_timed": wall1 - wall0,
+        "device_status": st,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_sample)
+    return out
+
+
+# ------------------------------------------------------------------------- oracle timing
+
+
+def oracle_sample(w, inp, n_tokens):
+    """Prepare a bounded oracle run over the first n_tokens positions of sequence 0."""
+    from oracle import hashing as OH
+    from oracle import layout as OL
+    from oracle import pipeline as OP
+    from workloads import bf16_bits_to_f64, table_rows
+
+    b = inp["batch"]
+    n = min(n_tokens, int(b.cu_seqlens[1]))
+    raw = b.raw_ids[:n]
+    cu = np.array([0, n], dtype=np.int64)
+    tm = inp["tm"]
+    lay_o = OL.build_layout(w.v, w.base_rows, [w.layer_id], pad_id=int(tm[0]))
+    rows, _, _ = OH.hash_prefill(raw, cu, tm, lay_o, 0)
+    uniq = np.unique(rows)
+    cache = dict(zip(uniq.tolist(), table_rows(w.seed, uniq)))   # table bytes, read by the oracle below
+
+    def table(r):
+        return np.stack([cache[int(x)] for x in r])
+
+    W = bf16_bits_to_f64(inp["lw"].wkv_bits)
+    h = bf16_bits_to_f64(inp["h_bits"][:n])
+
+    def run():
+        return OP.layer_forward(lay_o, 0, raw, cu, tm, table, W, h, inp["lw"].q_w, inp["lw"].k_w)
+    return n, run
+
+
+def cpu_baseline(w, inp, n_tokens):
+    n, run = oracle_sample(w, inp, n_tokens)
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {n} positions of sequence 0 of the same batch, one full layer pass "
+                      f"(numpy fp64, BLAS threads = all cores); {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    # inputs are generated on the host; no GPU work on this arm
+    from workloads import layer_weights, prefill_batch, residual_bits, token_map
+    tm = token_map(w.v_raw, w.v, w.seed)
+    b = prefill_batch(w, seed=w.seed)
+    inp = dict(tm=tm, lw=layer_weights(w), batch=b, h_bits=residual_bits(len(b.raw_ids), w.hc, w.hidden, w.seed))
+    n, run = oracle_sample(w, inp, args.ref_sample)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = n * args.steps / tot
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": tot / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": workload_desc(w), "tokens_per_step": n,
+                   "note": "each step is the CPU oracle on a bounded sample of the workload"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"first {n} positions of sequence 0 per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        import torch
+        if world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+        out = run_ours(args, rank, world, local)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,458 @@
+"""Engram lookup layer for one GB300 GPU: Python binding of libengram.
+
+Every function here only marshals arguments into the C ABI declared in
+``include/engram.h`` (device pointers, sizes, the current CUDA stream) and
+allocates output tensors with PyTorch; all computation runs in the CUDA
+kernels of ``libengram.so``.  If the library has not been built the first
+call raises ``EngramError``; there is no fallback path.
+
+Build: ``python -m hashed_gram_conditional_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+__all__ = [
+    "EngramError", "Layout", "build_layout", "engram_hash", "engram_hash_step", "engram_gather_dequant",
+    "engram_pack_wkv", "engram_project", "engram_gate_add", "engram_fill_synthetic_table",
+    "engram_selftest_mod", "partials_shape", "EngramLayer", "library_path", "ST_BAD_TOKEN", "ST_BAD_ROW",
+    "ST_BAD_SLOT", "ST_TIMEOUT", "DEAD", "ROW_BYTES",
+]
+
+MAX_LAYERS = 8
+MAX_NGRAM = 4
+MAX_COLS = 32
+DEAD = -1
+ROW_BYTES = 264
+HEAD_DIM = 256
+ST_BAD_TOKEN, ST_BAD_ROW, ST_BAD_SLOT, ST_TIMEOUT = 1, 2, 4, 8
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libengram.so")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+class EngramError(RuntimeError):
+    pass
+
+
+class _LayoutParams(ctypes.Structure):
+    _fields_ = [
+        ("vocab_compressed", ctypes.c_int64),
+        ("expected_vocab", ctypes.c_int64),
+        ("base_rows", ctypes.c_int64),
+        ("n_layers", ctypes.c_int32),
+        ("layer_ids", ctypes.c_int32 * MAX_LAYERS),
+        ("max_ngram", ctypes.c_int32),
+        ("n_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("pad_id", ctypes.c_int32),
+        ("use_multiplier_override", ctypes.c_int32),
+        ("multiplier_override", (ctypes.c_int64 * MAX_NGRAM) * MAX_LAYERS),
+    ]
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [
+        ("vocab_compressed", ctypes.c_int64),
+        ("base_rows", ctypes.c_int64),
+        ("n_layers", ctypes.c_int32),
+        ("max_ngram", ctypes.c_int32),
+        ("n_heads", ctypes.c_int32),
+        ("n_cols", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("pad_id", ctypes.c_int32),
+        ("layer_ids", ctypes.c_int32 * MAX_LAYERS),
+        ("total_rows", ctypes.c_int64 * MAX_LAYERS),
+        ("primes", (ctypes.c_int64 * MAX_COLS) * MAX_LAYERS),
+        ("offsets", (ctypes.c_int64 * MAX_COLS) * MAX_LAYERS),
+        ("reciprocal", (ctypes.c_uint64 * MAX_COLS) * MAX_LAYERS),
+        ("multipliers", (ctypes.c_int64 * MAX_NGRAM) * MAX_LAYERS),
+    ]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_F32 = ctypes.c_float
+
+_SIGS = {
+    "engram_build_layout": [ctypes.POINTER(_LayoutParams), ctypes.POINTER(_Layout)],
+    "engram_hash": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _P, _P, _P],
+    "engram_hash_step": [ctypes.POINTER(_Layout), _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _P],
+    "engram_gather_dequant": [_P, _I64, _I64, _P, _I64, _I32, _P, _P, _P],
+    "engram_pack_wkv": [_P, _I64, _I64, _P, _P],
+    "engram_project": [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P],
+    "engram_gate_add": [_P, _P, _P, _P, _I64, _I32, _I32, _F32, _F32, _F32, _P, _P],
+    "engram_fill_synthetic_table": [_P, _I64, ctypes.c_uint64, _P],
+    "engram_selftest_mod": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _P],
+}
+
+
+def _load():
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise EngramError(
+                f"CUDA library {_LIB_PATH} is not built; run `python -m hashed_gram_conditional_gb300.build`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, args in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.engram_last_error.restype = ctypes.c_char_p
+        lib.engram_status_string.restype = ctypes.c_char_p
+        lib.engram_status_string.argtypes = [ctypes.c_int]
+        lib.engram_project_partials_bytes.restype = ctypes.c_size_t
+        lib.engram_project_partials_bytes.argtypes = [_I64, _I32, _I32]
+        lib.engram_layout_size.restype = ctypes.c_size_t
+        lib.engram_layout_params_size.restype = ctypes.c_size_t
+        if lib.engram_layout_size() != ctypes.sizeof(_Layout) or \
+                lib.engram_layout_params_size() != ctypes.sizeof(_LayoutParams):
+            raise EngramError("libengram struct layout does not match the binding")
+        _lib = lib
+        return lib
+
+
+def lib():
+    """The loaded ctypes library (raises EngramError when it is not built)."""
+    return _load()
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        L = _load()
+        raise EngramError(f"{name}: {L.engram_status_string(rc).decode()}: {L.engram_last_error().decode()}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, device=None, numel=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, has {t.numel()}")
+
+
+# --------------------------------------------------------------------------- layout
+
+
+class Layout:
+    """Immutable table layout (wraps the C struct engram_layout)."""
+
+    def __init__(self, raw: _Layout):
+        self._raw = raw
+
+    @property
+    def ref(self):
+        return ctypes.byref(self._raw)
+
+    @property
+    def n_layers(self) -> int:
+        return self._raw.n_layers
+
+    @property
+    def n_cols(self) -> int:
+        return self._raw.n_cols
+
+    @property
+    def max_ngram(self) -> int:
+        return self._raw.max_ngram
+
+    @property
+    def n_heads(self) -> int:
+        return self._raw.n_heads
+
+    @property
+    def pad_id(self) -> int:
+        return self._raw.pad_id
+
+    @property
+    def vocab(self) -> int:
+        return self._raw.vocab_compressed
+
+    def layer_id(self, layer: int) -> int:
+        return self._raw.layer_ids[layer]
+
+    def primes(self, layer: int):
+        return [self._raw.primes[layer][j] for j in range(self.n_cols)]
+
+    def offsets(self, layer: int):
+        return [self._raw.offsets[layer][j] for j in range(self.n_cols)]
+
+    def total_rows(self, layer: int) -> int:
+        return self._raw.total_rows[layer]
+
+    def multipliers(self, layer: int):
+        return [self._raw.multipliers[layer][i] for i in range(self.max_ngram)]
+
+
+def build_layout(vocab: int, base_rows: int, layer_ids: Sequence[int], max_ngram: int = 4, n_heads: int = 8,
+                 head_dim: int = 256, pad_id: int = 0, expected_vocab: int = 0,
+                 multipliers: Optional[Sequence[Sequence[int]]] = None) -> Layout:
+    L = _load()
+    p = _LayoutParams()
+    p.vocab_compressed = vocab
+    p.expected_vocab = expected_vocab
+    p.base_rows = base_rows
+    if not (1 <= len(layer_ids) <= MAX_LAYERS):
+        raise ValueError("1..8 layers")
+    p.n_layers = len(layer_ids)
+    for i, lid in enumerate(layer_ids):
+        p.layer_ids[i] = lid
+    p.max_ngram = max_ngram
+    p.n_heads = n_heads
+    p.head_dim = head_dim
+    p.pad_id = pad_id
+    if multipliers is not None:
+        p.use_multiplier_override = 1
+        for i, row in enumerate(multipliers):
+            for j, m in enumerate(row):
+                p.multiplier_override[i][j] = int(m)
+    out = _Layout()
+    _check(L.engram_build_layout(ctypes.byref(p), ctypes.byref(out)), "engram_build_layout")
+    return Layout(out)
+
+
+# --------------------------------------------------------------------------- stages
+
+
+def new_status(device) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def engram_hash(layout: Layout, layer: int, raw_ids: torch.Tensor, cu_seqlens: torch.Tensor,
+                token_map: torch.Tensor, hist: Optional[torch.Tensor] = None,
+                row_ids: Optional[torch.Tensor] = None, mask: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None):
+    """Prefill hash; returns (row_ids int32 [T][n_cols], mask uint8 [T]). hist is updated in place."""
+    L = _load()
+    dev = raw_ids.device
+    T = raw_ids.numel()
+    n_seqs = cu_seqlens.numel() - 1
+    _need(raw_ids, "raw_ids", torch.int32)
+    _need(cu_seqlens, "cu_seqlens", torch.int64, dev)
+    _need(token_map, "token_map", torch.int32, dev)
+    if hist is not None:
+        _need(hist, "hist", torch.int32, dev, n_seqs * (layout.max_ngram - 1))
+    if row_ids is None:
+        row_ids = torch.empty((T, layout.n_cols), dtype=torch.int32, device=dev)
+    if mask is None:
+        mask = torch.empty(T, dtype=torch.uint8, device=dev)
+    _need(row_ids, "row_ids", torch.int32, dev, T * layout.n_cols)
+    _need(mask, "mask", torch.uint8, dev, T)
+    _check(L.engram_hash(layout.ref, layer, _ptr(raw_ids), T, _ptr(cu_seqlens), n_seqs, _ptr(token_map),
+                         token_map.numel(), _ptr(hist), _ptr(row_ids), _ptr(mask), _ptr(status), _stream(dev)),
+           "engram_hash")
+    return row_ids, mask
+
+
+def engram_hash_step(layout: Layout, layer: int, raw_ids: torch.Tensor, slots: torch.Tensor,
+                     token_map: torch.Tensor, hist: torch.Tensor, row_ids: Optional[torch.Tensor] = None,
+                     mask: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """One decode step; returns (row_ids [B][n_cols], mask [B]); hist [S][max_ngram-1] updated in place."""
+    L = _load()
+    dev = raw_ids.device
+    B = raw_ids.numel()
+    _need(raw_ids, "raw_ids", torch.int32)
+    _need(slots, "slots", torch.int32, dev, B)
+    _need(token_map, "token_map", torch.int32, dev)
+    _need(hist, "hist", torch.int32, dev)
+    depth = layout.max_ngram - 1
+    if hist.numel() % depth:
+        raise ValueError("hist must be [n_slots][max_ngram-1]")
+    if row_ids is None:
+        row_ids = torch.empty((B, layout.n_cols), dtype=torch.int32, device=dev)
+    if mask is None:
+        mask = torch.empty(B, dtype=torch.uint8, device=dev)
+    _need(row_ids, "row_ids", torch.int32, dev, B * layout.n_cols)
+    _need(mask, "mask", torch.uint8, dev, B)
+    _check(L.engram_hash_step(layout.ref, layer, _ptr(raw_ids), _ptr(slots), B, _ptr(token_map),
+                              token_map.numel(), _ptr(hist), hist.numel() // depth, _ptr(row_ids), _ptr(mask),
+                              _ptr(status), _stream(dev)), "engram_hash_step")
+    return row_ids, mask
+
+
+def engram_gather_dequant(table: torch.Tensor, total_rows: int, row_ids: torch.Tensor,
+                          e: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Gather and dequantise: returns e bf16 [T][n_cols*256]."""
+    L = _load()
+    dev = row_ids.device
+    _need(table, "table", torch.uint8, dev)
+    _need(row_ids, "row_ids", torch.int32)
+    T, C = row_ids.shape
+    if e is None:
+        e = torch.empty((T, C * HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    _need(e, "e", torch.bfloat16, dev, T * C * HEAD_DIM)
+    _check(L.engram_gather_dequant(_ptr(table), total_rows, table.numel(), _ptr(row_ids), T, C, _ptr(e),
+                                   _ptr(status), _stream(dev)), "engram_gather_dequant")
+    return e
+
+
+def engram_pack_wkv(wkv: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """[K][N] bf16 -> K-major [N][K] bf16 operand layout."""
+    L = _load()
+    _need(wkv, "wkv", torch.bfloat16)
+    K, N = wkv.shape
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.bfloat16, device=wkv.device)
+    _need(out, "out", torch.bfloat16, wkv.device, N * K)
+    _check(L.engram_pack_wkv(_ptr(wkv), K, N, _ptr(out), _stream(wkv.device)), "engram_pack_wkv")
+    return out
+
+
+def partials_shape(n_tokens: int, hidden: int, hc: int):
+    return (n_tokens, hc, hidden // 256, 4)
+
+
+def engram_project(e: torch.Tensor, wkv_packed: torch.Tensor, h: torch.Tensor, q_w: torch.Tensor,
+                   k_w: torch.Tensor, partials: Optional[torch.Tensor] = None, v: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None):
+    """Tensor-core projection; returns (partials f32 [T][hc][H/256][4], v bf16 [T][H])."""
+    L = _load()
+    dev = e.device
+    _need(e, "e", torch.bfloat16)
+    T, K = e.shape
+    _need(h, "h", torch.bfloat16, dev)
+    if h.dim() != 3 or h.shape[0] != T:
+        raise ValueError("h must be [T][hc][H]")
+    hc, H = h.shape[1], h.shape[2]
+    _need(wkv_packed, "wkv_packed", torch.bfloat16, dev, (hc + 1) * H * K)
+    _need(q_w, "q_w", torch.float32, dev, H * hc)
+    _need(k_w, "k_w", torch.float32, dev, H * hc)
+    if partials is None:
+        partials = torch.empty(partials_shape(T, H, hc), dtype=torch.float32, device=dev)
+    if v is None:
+        v = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    _need(partials, "partials", torch.float32, dev, T * hc * (H // 256) * 4)
+    _need(v, "v", torch.bfloat16, dev, T * H)
+    _check(L.engram_project(_ptr(e), T, K, _ptr(wkv_packed), H, hc, _ptr(h), _ptr(q_w), _ptr(k_w),
+                            _ptr(partials), _ptr(v), _ptr(status), _stream(dev)), "engram_project")
+    return partials, v
+
+
+def engram_gate_add(partials: torch.Tensor, v: torch.Tensor, h: torch.Tensor, mask: Optional[torch.Tensor],
+                    eps: float = 1e-6, clamp: float = 1e-6, score_scale: Optional[float] = None,
+                    gate_out: Optional[torch.Tensor] = None) -> Optional[torch.Tensor]:
+    """h <- bf16(h + gate * v) in place; returns gate_out (f32 [T][hc]) when given."""
+    L = _load()
+    dev = h.device
+    _need(h, "h", torch.bfloat16)
+    T, hc, H = h.shape
+    _need(partials, "partials", torch.float32, dev, T * hc * (H // 256) * 4)
+    _need(v, "v", torch.bfloat16, dev, T * H)
+    if mask is not None:
+        _need(mask, "mask", torch.uint8, dev, T)
+    if gate_out is not None:
+        _need(gate_out, "gate_out", torch.float32, dev, T * hc)
+    if score_scale is None:
+        score_scale = H ** -0.5
+    _check(L.engram_gate_add(_ptr(partials), _ptr(v), _ptr(h), _ptr(mask), T, H, hc, eps, clamp, score_scale,
+                             _ptr(gate_out), _stream(dev)), "engram_gate_add")
+    return gate_out
+
+
+def engram_fill_synthetic_table(table: torch.Tensor, n_rows: int, seed: int) -> torch.Tensor:
+    L = _load()
+    _need(table, "table", torch.uint8)
+    if table.numel() < n_rows * ROW_BYTES:
+        raise ValueError("table too small")
+    _check(L.engram_fill_synthetic_table(_ptr(table), n_rows, seed, _stream(table.device)),
+           "engram_fill_synthetic_table")
+    return table
+
+
+def engram_selftest_mod(layout: Layout, layer: int, x: torch.Tensor) -> torch.Tensor:
+    """x: uint64 values stored in an int64 tensor; returns int64 [n][n_cols]."""
+    L = _load()
+    _need(x, "x", torch.int64)
+    out = torch.empty((x.numel(), layout.n_cols), dtype=torch.int64, device=x.device)
+    _check(L.engram_selftest_mod(layout.ref, layer, _ptr(x), x.numel(), _ptr(out), _stream(x.device)),
+           "engram_selftest_mod")
+    return out
+
+
+# --------------------------------------------------------------------------- layer
+
+
+class EngramLayer:
+    """One Engram layer with resident weights: table, token map, packed wkv, q_w, k_w.
+
+    ``prefill`` runs hash -> gather -> project -> gate_add on the current
+    stream and updates the residual ``h`` in place.
+    """
+
+    def __init__(self, layout: Layout, layer: int, table: torch.Tensor, token_map: torch.Tensor,
+                 wkv_packed: torch.Tensor, q_w: torch.Tensor, k_w: torch.Tensor, eps: float = 1e-6,
+                 clamp: float = 1e-6, score_scale: Optional[float] = None):
+        self.layout, self.layer = layout, layer
+        self.table, self.token_map = table, token_map
+        self.wkv_packed, self.q_w, self.k_w = wkv_packed, q_w, k_w
+        self.hidden, self.hc = q_w.shape[0], q_w.shape[1]
+        self.eps, self.clamp = eps, clamp
+        self.score_scale = self.hidden ** -0.5 if score_scale is None else score_scale
+        self.total_rows = layout.total_rows(layer)
+        self._ws = {}
+
+    def _buffers(self, T: int, device):
+        key = (T, str(device))
+        if key not in self._ws:
+            self._ws = {key: dict(
+                rows=torch.empty((T, self.layout.n_cols), dtype=torch.int32, device=device),
+                mask=torch.empty(T, dtype=torch.uint8, device=device),
+                e=torch.empty((T, self.layout.n_cols * HEAD_DIM), dtype=torch.bfloat16, device=device),
+                partials=torch.empty(partials_shape(T, self.hidden, self.hc), dtype=torch.float32, device=device),
+                v=torch.empty((T, self.hidden), dtype=torch.bfloat16, device=device),
+            )}
+        return self._ws[key]
+
+    def prefill(self, raw_ids: torch.Tensor, cu_seqlens: torch.Tensor, h: torch.Tensor,
+                hist: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                gate_out: Optional[torch.Tensor] = None):
+        T = raw_ids.numel()
+        b = self._buffers(T, raw_ids.device)
+        engram_hash(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, hist, b["rows"], b["mask"],
+                    status)
+        engram_gather_dequant(self.table, self.total_rows, b["rows"], b["e"], status)
+        engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
+        engram_gate_add(b["partials"], b["v"], h, b["mask"], self.eps, self.clamp, self.score_scale, gate_out)
+        return b
+
+    def decode(self, raw_ids: torch.Tensor, slots: torch.Tensor, hist: torch.Tensor, h: torch.Tensor,
+               status: Optional[torch.Tensor] = None, gate_out: Optional[torch.Tensor] = None):
+        B = raw_ids.numel()
+        b = self._buffers(B, raw_ids.device)
+        engram_hash_step(self.layout, self.layer, raw_ids, slots, self.token_map, hist, b["rows"], b["mask"],
+                         status)
+        engram_gather_dequant(self.table, self.total_rows, b["rows"], b["e"], status)
+        engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
+        engram_gate_add(b["partials"], b["v"], h, b["mask"], self.eps, self.clamp, self.score_scale, gate_out)
+        return b

@@ -1,0 +1,269 @@
+// Stage 4 of the Engram lookup: gather 24 rows of 264 bytes per position and
+// dequantise them (E4M3 x E8M0 per 32 elements) to bf16.
+//
+// Pages cited by title:
+//   [P-V41] "DeepSeek-V4.1 模型结构（5）：记忆，Engram" §"196B 参数怎么存、怎么取"
+//   [P-DS4] "ds4.c 学习笔记" -- glossary entry "Engram", §布局与哈希探测 and
+//           §永不常驻的 I/O 设计 (the e4m3_e8m0_32_row264 row format)
+//   [P-O1]  "条件记忆：DeepSeek V4.1 Engram 如何用 O(1) 查表换掉一层计算" §2.3
+//
+// Design (GB300): the rows are scattered at random over a table of up to
+// ~100 GB, so the kernel is bound by HBM latency and bandwidth.  Row r starts
+// at byte 264 r, which is 16-byte aligned for even r and 8 bytes past a
+// 16-byte boundary for odd r; the 16-byte-aligned 272-byte window that
+// starts at or 8 bytes before the row covers it in both cases.  Each warp
+// runs its own pipeline of `stages` positions: lanes 0..n_cols-1 each issue
+// one 272-byte bulk copy (cp.async.bulk, completion counted on the stage's
+// mbarrier) into shared memory, so ~100 rows per SM are in flight.  When a
+// stage lands, each lane dequantises 8 consecutive elements of every row in
+// registers and the warp writes each 512-byte bf16 row segment with one
+// coalesced 16-byte store per lane.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "engram_internal.h"
+
+namespace engram {
+namespace {
+
+constexpr int kRowBytes = ENGRAM_ROW_BYTES;  // 264
+constexpr int kSlot = 272;                   // 16-byte aligned window of a row
+constexpr int kWarps = 8;                    // warps per CTA (each an independent pipeline)
+
+struct GatherArgs {
+  const uint8_t* table;
+  int64_t total_rows;
+  int64_t table_bytes;
+  const int32_t* rows;
+  int64_t n_tokens;
+  int32_t n_cols;
+  int32_t stages;
+  uint16_t* e;
+  int32_t* status;
+};
+
+// Two E4M3 codes (low byte = first element) -> two bf16 values scaled by
+// 2^(s-127).  E4M3 -> f16 is exact, f16 -> f32 is exact, the product by a
+// power of two is exact in fp32 for every code and scale (an E4M3 value has
+// 4 significant bits and the smallest product, 2^-136, is above fp32's
+// subnormal resolution), so the single rounding is the final RNE to bf16.
+__device__ __forceinline__ uint32_t dq2(uint32_t two, float scale) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two)));
+  __half2 hv = *reinterpret_cast<__half2*>(&h2);
+  float2 f = __half22float2(hv);
+  __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// E8M0 scale 2^(s-127) as fp32: s = 0 is the subnormal 2^-127, s = 255 is NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+  if (s == 0) return __uint_as_float(0x00400000u);
+  if (s == 255) return __uint_as_float(0x7fc00000u);
+  return __uint_as_float(s << 23);
+}
+
+__device__ __forceinline__ uint4 dequant8(uint2 w, uint32_t sbyte) {
+  const float sc = e8m0_to_f32(sbyte);
+  uint4 o;
+  o.x = dq2(w.x & 0xffffu, sc);
+  o.y = dq2(w.x >> 16, sc);
+  o.z = dq2(w.y & 0xffffu, sc);
+  o.w = dq2(w.y >> 16, sc);
+  return o;
+}
+
+__global__ void __launch_bounds__(kWarps * 32, 1) gather_dequant_kernel(GatherArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int w = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t stage_bytes = static_cast<uint32_t>(a.n_cols) * kSlot;
+  const int S = a.stages;
+  uint8_t* wbuf = smem + static_cast<size_t>(w) * S * stage_bytes;
+  uint8_t* meta = smem + static_cast<size_t>(kWarps) * S * stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(meta) + w * S;
+  uint32_t* masks = reinterpret_cast<uint32_t*>(meta + kWarps * S * 8) + w * S * 2;
+
+  if (lane == 0)
+    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
+  fence_mbar_init();
+  __syncwarp();
+
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + w;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int n_cols = a.n_cols;
+
+  // Issue the bulk copies of position t into stage s.
+  auto issue = [&](int64_t t, int s) {
+    int32_t r = -1;
+    bool valid = false;
+    if (lane < static_cast<uint32_t>(n_cols)) {
+      r = __ldg(a.rows + t * n_cols + lane);
+      valid = r >= 0 && static_cast<int64_t>(r) < a.total_rows;
+      if (!valid && a.status) atomicOr(a.status, static_cast<int>(ENGRAM_ST_BAD_ROW));
+    }
+    // An even row's window extends 8 bytes past the row; for the table's last
+    // row that may pass the end of the allocation, so such a row copies its
+    // 256 weight bytes in bulk and its 8 scale bytes with a plain load.
+    const bool tail = valid && !(r & 1) && static_cast<int64_t>(r) * kRowBytes + kSlot > a.table_bytes;
+    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+    const uint32_t odd = __ballot_sync(0xffffffffu, valid && (r & 1));
+    const uint32_t tmask = __ballot_sync(0xffffffffu, tail);
+    const uint32_t bytes = __popc(vmask & ~tmask) * kSlot + __popc(tmask) * 256u;
+    const uint32_t bar = smem_u32(&bars[s]);
+    uint8_t* dst = wbuf + static_cast<size_t>(s) * stage_bytes + lane * kSlot;
+    if (lane == 0) {
+      masks[2 * s] = odd;
+      masks[2 * s + 1] = vmask;
+      mbar_arrive_expect_tx(bar, bytes);
+    }
+    __syncwarp();
+    if (valid) {
+      const int64_t off = static_cast<int64_t>(r) * kRowBytes;
+      const uint8_t* src = a.table + (off & ~int64_t(15));
+      if (!tail) {
+        bulk_g2s(smem_u32(dst), src, kSlot, bar);
+      } else {
+        bulk_g2s(smem_u32(dst), src, 256, bar);
+        *reinterpret_cast<uint2*>(dst + 256) = __ldg(reinterpret_cast<const uint2*>(a.table + off + 256));
+      }
+    }
+  };
+
+  // prologue: fill every stage
+  for (int s = 0; s < S; ++s) {
+    const int64_t t = gw + s * nw;
+    if (t < a.n_tokens) issue(t, s);
+  }
+
+  int64_t k = 0;
+  bool timed_out = false;
+  for (;; ++k) {
+    const int64_t t = gw + k * nw;
+    if (t >= a.n_tokens) break;
+    const int s = static_cast<int>(k % S);
+    const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
+    if (!mbar_wait_bounded(smem_u32(&bars[s]), parity, nullptr)) {
+      timed_out = true;
+      break;
+    }
+    const uint32_t odd = masks[2 * s];
+    const uint32_t vm = masks[2 * s + 1];
+    const uint8_t* sb = wbuf + static_cast<size_t>(s) * stage_bytes;
+    uint16_t* out = a.e + t * static_cast<int64_t>(n_cols) * ENGRAM_HEAD_DIM;
+#pragma unroll 4
+    for (int j = 0; j < n_cols; ++j) {
+      const uint8_t* row = sb + j * kSlot + (((odd >> j) & 1u) ? 8 : 0);
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if ((vm >> j) & 1u) {
+        const uint2 wv = *reinterpret_cast<const uint2*>(row + lane * 8);
+        const uint32_t sbyte = row[256 + (lane >> 2)];
+        o = dequant8(wv, sbyte);
+      }
+      *reinterpret_cast<uint4*>(out + j * ENGRAM_HEAD_DIM + lane * 8) = o;
+    }
+    __syncwarp();
+    const int64_t t2 = t + static_cast<int64_t>(S) * nw;
+    if (t2 < a.n_tokens) {
+      fence_proxy_async_smem();  // order this warp's shared reads before the async refill
+      issue(t2, s);
+    }
+  }
+  if (timed_out) {
+    if (lane == 0 && a.status) atomicOr(a.status, static_cast<int>(ENGRAM_ST_TIMEOUT));
+    // Let every copy already issued land before the CTA's shared memory is
+    // released: wait (bounded) on each outstanding stage.
+    for (int64_t kk = k; kk < k + S; ++kk) {
+      const int64_t t = gw + kk * nw;
+      if (t >= a.n_tokens) break;
+      const int s = static_cast<int>(kk % S);
+      mbar_wait_bounded(smem_u32(&bars[s]), static_cast<uint32_t>((kk / S) & 1), nullptr);
+    }
+  }
+}
+
+// SplitMix64 output number n+1 of a stream starting at `seed` (Steele, Lea &
+// Flood 2014): finaliser applied to seed + (n+1) * golden gamma.
+__device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t n) {
+  uint64_t z = seed + (n + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+__global__ void fill_table_kernel(uint8_t* table, int64_t n_words, uint64_t seed) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t wi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; wi < n_words;
+       wi += stride) {
+    uint64_t v = splitmix64_at(seed, static_cast<uint64_t>(wi));
+    if (wi % (kRowBytes / 8) < 32) {
+      // weight bytes: an E4M3 NaN code (low 7 bits all ones) becomes byte ^ 1;
+      // adding 1 to each byte's low 7 bits sets its bit 7 exactly for 0x7F.
+      const uint64_t low7 = v & 0x7F7F7F7F7F7F7F7Full;
+      const uint64_t hit = ((low7 + 0x0101010101010101ull) & 0x8080808080808080ull) >> 7;
+      v ^= hit;
+    } else {
+      uint64_t o = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const uint64_t byte = (v >> (8 * b)) & 0xFF;
+        o |= (120 + byte % 11) << (8 * b);
+      }
+      v = o;
+    }
+    reinterpret_cast<uint64_t*>(table)[wi] = v;
+  }
+}
+
+}  // namespace
+}  // namespace engram
+
+using namespace engram;
+
+extern "C" int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows,
+                                     int64_t table_bytes, const int32_t* row_ids_d,
+                                     int64_t n_tokens, int32_t n_cols, uint16_t* e_d,
+                                     int32_t* status_d, void* stream) {
+  if (n_tokens < 0 || total_rows < 0) return fail(ENGRAM_E_INVALID, "negative size");
+  if (n_cols < 1 || n_cols > ENGRAM_MAX_COLS) return fail(ENGRAM_E_SHAPE, "n_cols %d", n_cols);
+  if (table_bytes < total_rows * kRowBytes)
+    return fail(ENGRAM_E_SHAPE, "table_bytes %lld < total_rows * 264", (long long)table_bytes);
+  if (n_tokens == 0) return ENGRAM_OK;
+  if (!table_d || !row_ids_d || !e_d) return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (!aligned(table_d, 16) || !aligned(e_d, 16))
+    return fail(ENGRAM_E_ALIGN, "table and e must be 16-byte aligned");
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  const int smem_max = 227 * 1024;
+  const int per_stage = n_cols * kSlot + 16;  // slots + mbarrier + two masks
+  int stages = smem_max / (kWarps * per_stage);
+  if (stages > 4) stages = 4;
+  if (stages < 1) return fail(ENGRAM_E_SHAPE, "n_cols %d does not fit shared memory", n_cols);
+  const size_t smem = static_cast<size_t>(kWarps) * stages * per_stage;
+  cudaError_t err = cudaFuncSetAttribute(gather_dequant_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+  if (err != cudaSuccess)
+    return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(gather): %s", cudaGetErrorString(err));
+  GatherArgs a{table_d, total_rows, table_bytes, row_ids_d, n_tokens, n_cols, stages, e_d, status_d};
+  const int64_t want = (n_tokens + kWarps - 1) / kWarps;
+  const int blocks = static_cast<int>(want < sms ? want : sms);
+  gather_dequant_kernel<<<blocks, kWarps * 32, smem, as_stream(stream)>>>(a);
+  return check_launch("gather_dequant_kernel");
+}
+
+extern "C" int engram_fill_synthetic_table(uint8_t* table_d, int64_t n_rows, uint64_t seed,
+                                           void* stream) {
+  if (n_rows < 0) return fail(ENGRAM_E_INVALID, "n_rows < 0");
+  if (n_rows == 0) return ENGRAM_OK;
+  if (!table_d) return fail(ENGRAM_E_INVALID, "null table");
+  if (!aligned(table_d, 8)) return fail(ENGRAM_E_ALIGN, "table must be 8-byte aligned");
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  const int64_t n_words = n_rows * (kRowBytes / 8);
+  fill_table_kernel<<<sms * 8, 256, 0, as_stream(stream)>>>(table_d, n_words, seed);
+  return check_launch("fill_table_kernel");
+}

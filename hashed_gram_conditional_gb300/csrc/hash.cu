@@ -1,0 +1,314 @@
+// Stages 1-3 of the Engram lookup: token map, suffix window with pad/DEAD,
+// multiplicative-XOR mix and per-column prime modulo plus segment offset.
+//
+// Pages cited by title:
+//   [P-V41]    "DeepSeek-V4.1 模型结构（5）：记忆，Engram"
+//   [P-LMNT]   "Engram条件记忆：DeepSeek-V4.1-Flash中196B稀疏参数N-gram哈希查表的实现原理"
+//   [P-O1]     "条件记忆：DeepSeek V4.1 Engram 如何用 O(1) 查表换掉一层计算"
+//   [P-DS4]    "ds4.c 学习笔记" -- glossary entry "Engram"
+//   [P-DETAIL] "DeepSeek Engram 详解：把静态知识从计算里拆出来"
+//
+// Work mapping: one warp per position.  Lanes 0..max_ngram-1 fetch the window
+// slots, the slots are broadcast with shuffles, and lane j < n_cols computes
+// column j, so the 24 row ids of a position leave as one 96-byte store.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "engram_internal.h"
+
+namespace engram {
+namespace {
+
+constexpr int kDead = ENGRAM_DEAD;
+
+struct HashConsts {
+  uint64_t mult[ENGRAM_MAX_NGRAM];
+  uint64_t recip[ENGRAM_MAX_COLS];
+  uint32_t prime[ENGRAM_MAX_COLS];
+  uint32_t offset[ENGRAM_MAX_COLS];
+  int32_t n_cols;
+  int32_t n_heads;
+  int32_t max_ngram;
+  int32_t pad_id;
+  int64_t vocab;      // V (compressed)
+  int64_t vocab_raw;  // V_raw
+};
+
+int make_consts(const engram_layout* L, int layer, int64_t vocab_raw, HashConsts* c) {
+  if (L == nullptr) return fail(ENGRAM_E_INVALID, "null layout");
+  if (layer < 0 || layer >= L->n_layers)
+    return fail(ENGRAM_E_INVALID, "layer %d not in [0, %d)", layer, L->n_layers);
+  if (L->n_cols < 1 || L->n_cols > ENGRAM_MAX_COLS || L->max_ngram < 2 ||
+      L->max_ngram > ENGRAM_MAX_NGRAM || L->n_cols != (L->max_ngram - 1) * L->n_heads)
+    return fail(ENGRAM_E_SHAPE, "layout has inconsistent column counts");
+  if (vocab_raw < 1 || vocab_raw > INT32_MAX) return fail(ENGRAM_E_INVALID, "bad vocab_raw");
+  for (int j = 0; j < L->n_cols; ++j) {
+    int64_t p = L->primes[layer][j];
+    int64_t o = L->offsets[layer][j];
+    if (p < 2 || p >= (int64_t(1) << 31) || o < 0 || o + p > (int64_t(1) << 31))
+      return fail(ENGRAM_E_RANGE, "column %d prime/offset out of the int32 row range", j);
+    c->prime[j] = static_cast<uint32_t>(p);
+    c->offset[j] = static_cast<uint32_t>(o);
+    c->recip[j] = ~0ull / static_cast<uint64_t>(p);  // recomputed: never trust a stale field
+  }
+  for (int i = 0; i < L->max_ngram; ++i) c->mult[i] = static_cast<uint64_t>(L->multipliers[layer][i]);
+  c->n_cols = L->n_cols;
+  c->n_heads = L->n_heads;
+  c->max_ngram = L->max_ngram;
+  c->pad_id = L->pad_id;
+  c->vocab = L->vocab_compressed;
+  c->vocab_raw = vocab_raw;
+  return ENGRAM_OK;
+}
+
+// x mod p for any 64-bit x, with r = floor((2^64-1)/p) precomputed (Barrett
+// reduction, Barrett 1986).  q = floor(x r / 2^64) is floor(x/p) or one less,
+// so a single conditional subtraction finishes.
+__device__ __forceinline__ uint32_t mod_prime(uint64_t x, uint32_t p, uint64_t r) {
+  uint64_t q = __umul64hi(x, r);
+  uint64_t rem = x - q * static_cast<uint64_t>(p);
+  if (rem >= p) rem -= p;
+  return static_cast<uint32_t>(rem);
+}
+
+// Compressed id of one raw id, DEAD for an image position; an invalid raw id
+// or map value reports ENGRAM_ST_BAD_TOKEN and becomes DEAD (masked).
+__device__ __forceinline__ int32_t compress_id(int32_t raw, const int32_t* __restrict__ tmap,
+                                               const HashConsts& c, int32_t* status) {
+  if (raw == kDead) return kDead;
+  if (raw < 0 || static_cast<int64_t>(raw) >= c.vocab_raw) {
+    if (status) atomicOr(status, static_cast<int>(ENGRAM_ST_BAD_TOKEN));
+    return kDead;
+  }
+  int32_t x = __ldg(tmap + raw);
+  if (x < 0 || static_cast<int64_t>(x) >= c.vocab) {
+    if (status) atomicOr(status, static_cast<int>(ENGRAM_ST_BAD_TOKEN));
+    return kDead;
+  }
+  return x;
+}
+
+// A history entry must be DEAD or a compressed id.
+__device__ __forceinline__ int32_t check_hist(int32_t x, const HashConsts& c, int32_t* status) {
+  if (x == kDead) return kDead;
+  if (x < 0 || static_cast<int64_t>(x) >= c.vocab) {
+    if (status) atomicOr(status, static_cast<int>(ENGRAM_ST_BAD_TOKEN));
+    return kDead;
+  }
+  return x;
+}
+
+// Given the window slot held by lane i < max_ngram (slot i = x'_{t-i}),
+// applies the DEAD cascade, forms the mixes and writes the row ids of one
+// position.  All 32 lanes call it.
+__device__ __forceinline__ void hash_window(int32_t my_slot, const HashConsts& c,
+                                            int32_t* __restrict__ rows_out, uint8_t* mask_out,
+                                            bool force_mask) {
+  const uint32_t lane = lane_id();
+  // [P-V41] image tokens / [P-LMNT] §多模态细节: looking back, the first DEAD
+  // slot and every slot farther back count as pad.
+  uint64_t g[ENGRAM_MAX_NGRAM];
+  bool dead_seen = false;
+  bool self_dead = false;
+#pragma unroll
+  for (int i = 0; i < ENGRAM_MAX_NGRAM; ++i) {
+    int32_t v = __shfl_sync(0xffffffffu, my_slot, i);
+    if (i < c.max_ngram) {
+      if (v == kDead) {
+        dead_seen = true;
+        if (i == 0) self_dead = true;
+      }
+      g[i] = static_cast<uint64_t>(dead_seen ? c.pad_id : v);
+    } else {
+      g[i] = 0;
+    }
+  }
+  if (lane < static_cast<uint32_t>(c.n_cols)) {
+    // [P-V41] eq. (H): mix_n = XOR_{i<n} x'_{t-i} * m_i; column j is order
+    // n = 2 + j / n_heads ([P-DS4] step 3: row = mix mod p + offset).
+    const int n = 2 + static_cast<int>(lane) / c.n_heads;
+    uint64_t mix = 0;
+#pragma unroll
+    for (int i = 0; i < ENGRAM_MAX_NGRAM; ++i)
+      if (i < n) mix ^= g[i] * c.mult[i];
+    const uint32_t z = mod_prime(mix, c.prime[lane], c.recip[lane]);
+    rows_out[lane] = static_cast<int32_t>(z + c.offset[lane]);
+  }
+  if (lane == 0) *mask_out = (self_dead || force_mask) ? 1 : 0;
+}
+
+__global__ void __launch_bounds__(256) hash_prefill_kernel(
+    HashConsts c, const int32_t* __restrict__ raw, int64_t n_tokens,
+    const int64_t* __restrict__ cu, int32_t n_seqs, const int32_t* __restrict__ tmap,
+    const int32_t* __restrict__ hist, int32_t* __restrict__ rows, uint8_t* __restrict__ mask,
+    int32_t* status) {
+  const uint32_t lane = lane_id();
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  const int depth = c.max_ngram - 1;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+       t < n_tokens; t += warps) {
+    // sequence of position t: largest s with cu[s] <= t
+    int lo = 0, hi = n_seqs - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    const int64_t start = __ldg(cu + lo);
+    int32_t slot = c.pad_id;
+    if (lane < static_cast<uint32_t>(c.max_ngram)) {
+      const int64_t src = t - static_cast<int64_t>(lane);
+      if (src >= start) {
+        slot = compress_id(__ldg(raw + src), tmap, c, status);
+      } else if (hist != nullptr) {
+        // before the chunk start: carried history, most recent first
+        const int64_t hidx = static_cast<int64_t>(lane) - 1 - (t - start);
+        slot = check_hist(__ldg(hist + static_cast<int64_t>(lo) * depth + hidx), c, status);
+      }
+    }
+    hash_window(slot, c, rows + t * c.n_cols, mask + t, false);
+  }
+}
+
+// History after a chunk: the last `depth` compressed ids of each sequence,
+// most recent first, falling back to the previous history for short chunks.
+// One thread per sequence reads all it needs before writing its own row.
+__global__ void hash_commit_kernel(HashConsts c, const int32_t* __restrict__ raw,
+                                   const int64_t* __restrict__ cu, int32_t n_seqs,
+                                   const int32_t* __restrict__ tmap, int32_t* hist,
+                                   int32_t* status) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= n_seqs) return;
+  const int depth = c.max_ngram - 1;
+  const int64_t start = cu[s], end = cu[s + 1];
+  const int64_t len = end - start;
+  int32_t nh[ENGRAM_MAX_NGRAM - 1];
+#pragma unroll
+  for (int i = 0; i < ENGRAM_MAX_NGRAM - 1; ++i) {
+    if (i >= depth) break;
+    const int64_t pos = end - 1 - i;
+    if (pos >= start) {
+      nh[i] = compress_id(raw[pos], tmap, c, nullptr);  // errors already reported by the hash
+    } else {
+      nh[i] = hist[static_cast<int64_t>(s) * depth + (i - len)];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < ENGRAM_MAX_NGRAM - 1; ++i) {
+    if (i >= depth) break;
+    hist[static_cast<int64_t>(s) * depth + i] = nh[i];
+  }
+}
+
+// Decode step: warp per batch entry; the entry's history row is read by the
+// first lanes, hashed, and rolled forward by lane 0 ([P-O1] §4.4: hash and
+// history commit in one launch; padding entries commit nothing).
+__global__ void __launch_bounds__(256) hash_step_kernel(
+    HashConsts c, const int32_t* __restrict__ raw, const int32_t* __restrict__ slots, int32_t batch,
+    const int32_t* __restrict__ tmap, int32_t* hist, int64_t n_slots, int32_t* __restrict__ rows,
+    uint8_t* __restrict__ mask, int32_t* status) {
+  const uint32_t lane = lane_id();
+  const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (b >= batch) return;
+  const int depth = c.max_ngram - 1;
+  int32_t sl = slots[b];
+  bool pad_row = sl < 0;
+  if (sl >= 0 && static_cast<int64_t>(sl) >= n_slots) {
+    if (lane == 0 && status) atomicOr(status, static_cast<int>(ENGRAM_ST_BAD_SLOT));
+    pad_row = true;
+  }
+  int32_t slot = c.pad_id;
+  int32_t xnew = kDead;
+  if (lane == 0) {
+    xnew = compress_id(raw[b], tmap, c, status);
+    slot = xnew;
+  } else if (lane < static_cast<uint32_t>(c.max_ngram) && !pad_row) {
+    slot = check_hist(hist[static_cast<int64_t>(sl) * depth + (lane - 1)], c, status);
+  }
+  // Every lane's history read has been consumed by the shuffles inside
+  // hash_window before any lane writes the row below.
+  hash_window(slot, c, rows + static_cast<int64_t>(b) * c.n_cols, mask + b, pad_row);
+  __syncwarp();
+  // Roll (h0, h1, ...) <- (x', h0, ...): lane i holds window slot g_i =
+  // x'_{t-i}, which is exactly the new history entry i (most recent first).
+  if (!pad_row && lane < static_cast<uint32_t>(depth)) {
+    hist[static_cast<int64_t>(sl) * depth + lane] = (lane == 0) ? xnew : slot;
+  }
+}
+
+__global__ void selftest_mod_kernel(HashConsts c, const uint64_t* __restrict__ x, int64_t n,
+                                    int64_t* __restrict__ out) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint64_t v = x[i];
+  for (int j = 0; j < c.n_cols; ++j)
+    out[i * c.n_cols + j] = static_cast<int64_t>(mod_prime(v, c.prime[j], c.recip[j])) + c.offset[j];
+}
+
+}  // namespace
+}  // namespace engram
+
+using namespace engram;
+
+extern "C" int engram_hash(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
+                           int64_t n_tokens, const int64_t* cu_seqlens_d, int32_t n_seqs,
+                           const int32_t* token_map_d, int64_t vocab_raw, int32_t* hist_d,
+                           int32_t* row_ids_d, uint8_t* mask_d, int32_t* status_d, void* stream) {
+  HashConsts c;
+  int rc = make_consts(layout, layer, vocab_raw, &c);
+  if (rc) return rc;
+  if (n_tokens < 0 || n_seqs < 1) return fail(ENGRAM_E_INVALID, "n_tokens < 0 or n_seqs < 1");
+  if (n_tokens == 0 && hist_d == nullptr) return ENGRAM_OK;
+  if (!cu_seqlens_d || !token_map_d || (n_tokens > 0 && (!raw_ids_d || !row_ids_d || !mask_d)))
+    return fail(ENGRAM_E_INVALID, "null device pointer");
+  int sms = 0;
+  if ((rc = check_device(&sms))) return rc;
+  cudaStream_t st = as_stream(stream);
+  if (n_tokens > 0) {
+    const int threads = 256;
+    const int64_t want = (n_tokens + 7) / 8;
+    const int blocks = static_cast<int>(want < int64_t(sms) * 16 ? want : int64_t(sms) * 16);
+    hash_prefill_kernel<<<blocks, threads, 0, st>>>(c, raw_ids_d, n_tokens, cu_seqlens_d, n_seqs,
+                                                    token_map_d, hist_d, row_ids_d, mask_d,
+                                                    status_d);
+    if ((rc = check_launch("hash_prefill_kernel"))) return rc;
+  }
+  if (hist_d != nullptr) {
+    hash_commit_kernel<<<(n_seqs + 127) / 128, 128, 0, st>>>(c, raw_ids_d, cu_seqlens_d, n_seqs,
+                                                            token_map_d, hist_d, status_d);
+    if ((rc = check_launch("hash_commit_kernel"))) return rc;
+  }
+  return ENGRAM_OK;
+}
+
+extern "C" int engram_hash_step(const engram_layout* layout, int32_t layer,
+                                const int32_t* raw_ids_d, const int32_t* slots_d, int32_t batch,
+                                const int32_t* token_map_d, int64_t vocab_raw, int32_t* hist_d,
+                                int64_t n_slots, int32_t* row_ids_d, uint8_t* mask_d,
+                                int32_t* status_d, void* stream) {
+  HashConsts c;
+  int rc = make_consts(layout, layer, vocab_raw, &c);
+  if (rc) return rc;
+  if (batch < 0 || n_slots < 0) return fail(ENGRAM_E_INVALID, "negative batch or n_slots");
+  if (batch == 0) return ENGRAM_OK;
+  if (!raw_ids_d || !slots_d || !token_map_d || !row_ids_d || !mask_d || (n_slots > 0 && !hist_d))
+    return fail(ENGRAM_E_INVALID, "null device pointer");
+  if ((rc = check_device(nullptr))) return rc;
+  const int wpb = 8;
+  hash_step_kernel<<<(batch + wpb - 1) / wpb, wpb * 32, 0, as_stream(stream)>>>(
+      c, raw_ids_d, slots_d, batch, token_map_d, hist_d, n_slots, row_ids_d, mask_d, status_d);
+  return check_launch("hash_step_kernel");
+}
+
+extern "C" int engram_selftest_mod(const engram_layout* layout, int32_t layer, const uint64_t* x_d,
+                                   int64_t n, int64_t* out_d, void* stream) {
+  HashConsts c;
+  int rc = make_consts(layout, layer, 1, &c);
+  if (rc) return rc;
+  if (n < 0) return fail(ENGRAM_E_INVALID, "n < 0");
+  if (n == 0) return ENGRAM_OK;
+  if (!x_d || !out_d) return fail(ENGRAM_E_INVALID, "null device pointer");
+  if ((rc = check_device(nullptr))) return rc;
+  selftest_mod_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, as_stream(stream)>>>(c, x_d, n,
+                                                                                            out_d);
+  return check_launch("selftest_mod_kernel");
+}

@@ -1,0 +1,480 @@
+// Stage 5a/5b of the Engram lookup: kv = e @ wkv on the 5th-generation
+// tensor cores (tcgen05, accumulators in TMEM, operands staged by TMA), with
+// the context gate's reductions fused into the epilogue.
+//
+// Pages cited by title:
+//   [P-V41] "DeepSeek-V4.1 模型结构（5）：记忆，Engram" §门控 (one linear map from
+//           the 6144-dim lookup vector to 4 keys and 1 value of 5120 each) and
+//           §"每条流一个 key 的设计沿用自原版" (one [6144, 25600] matrix wkv)
+//   [P-DS4] "ds4.c 学习笔记" -- glossary entry "Engram", §消费：学习投影 + 余弦门控
+//           (dot = sum_i h_i (q_w_i k_w_i) k_i and the two mean squares)
+//
+// Kernel structure (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: 128x64 tile of e and 256x64 tile of the packed
+//               wkv per k-block into a 4-stage ring (48 KB per stage, 128-byte
+//               swizzle), completion on the stage's "full" mbarrier.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//               issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) from one
+//               thread; tcgen05.commit frees each stage and, per tile, signals
+//               the accumulator to the epilogue.
+//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time; thread r owns row r
+//               (one position) of the tile.  For a key tile it accumulates, over
+//               its 256 columns, sum h q_w k_w k, sum k^2 and sum h^2 into one
+//               float4 partial per (position, stream, tile); keys never reach
+//               memory.  For a value tile it rounds v to bf16 and stores it.
+//   Two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// Every wait is bounded; a wait that runs out records ENGRAM_ST_TIMEOUT, the
+// roles unwind, in-flight copies and MMAs are drained and TMEM is freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "engram_internal.h"
+
+namespace engram {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int kThreads = 192;
+constexpr int kGroupM = 32;  // M-blocks per raster group (L2 reuse of wkv)
+constexpr int kMaxHc = 8;
+
+struct ProjArgs {
+  int64_t M;
+  int32_t K;
+  int32_t H;
+  int32_t hc;
+  int32_t mt;
+  int32_t nt;
+  int32_t num_tiles;
+  const uint16_t* h;
+  const float* q_w;
+  const float* k_w;
+  float4* partials;
+  uint16_t* v;
+  int32_t* status;
+};
+
+struct __align__(8) SmemCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort;
+  float qk[4][BN];  // q_w * k_w of the current key tile, one copy per epilogue warp
+};
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
+// tile: start address, leading byte offset (unused for this layout, 16 B),
+// stride byte offset 1024 B between 8-row groups, descriptor version 1,
+// swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16,
+// both K-major, N = BN, M = BM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tile_coords(int tile, int mt, int nt, int& mb, int& nb) {
+  const int per_group = kGroupM * nt;
+  const int g = tile / per_group;
+  const int first_m = g * kGroupM;
+  const int gm = min(kGroupM, mt - first_m);
+  const int local = tile - g * per_group;
+  mb = first_m + local % gm;
+  nb = local / gm;
+}
+
+__device__ __forceinline__ void raise_abort(SmemCtl* ctl, int32_t* status) {
+  ctl->abort = 1;
+  if (status) atomicOr(status, static_cast<int>(ENGRAM_ST_TIMEOUT));
+}
+
+__device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    project_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   ProjArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + STAGES * A_BYTES;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const int nkb = a.K / BK;
+  volatile int* abort_flag = &ctl->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctl->tfull[i]), 1);
+      mbar_init(smem_u32(&ctl->tempty[i]), 4);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, a.mt, a.nt, mb, nb);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag)) {
+            if (!*abort_flag) raise_abort(ctl, a.status);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          tma_load_2d(smem_u32(smA + s * A_BYTES), &tmA, kb * BK, mb * BM, fb);
+          tma_load_2d(smem_u32(smB + s * B_BYTES), &tmB, kb * BK, nb * BN, fb);
+        }
+      }
+      // Drain: the last STAGES loads issued must have landed before the CTA
+      // exits (already true after a normal run, where the MMA consumed them).
+      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+        mbar_wait_bounded(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1, nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1, abort_flag)) {
+          if (!*abort_flag) raise_abort(ctl, a.status);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag)) {
+            if (!*abort_flag) raise_abort(ctl, a.status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smA + s * A_BYTES);
+          const uint32_t b0 = smem_u32(smB + s * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            tc_mma(d, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&ctl->empty[s]));
+        }
+        if (ok) tc_commit(smem_u32(&ctl->tfull[acc]));
+      }
+      // every MMA issued so far completes before TMEM is released
+      tc_commit(smem_u32(&ctl->drain));
+      mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + static_cast<int>(lane);
+    const int ntile = a.H / BN;
+    const int key_cols = a.hc * a.H;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++local) {
+      int mb, nb;
+      tile_coords(tile, a.mt, a.nt, mb, nb);
+      const int acc = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      const int n0 = nb * BN;
+      const bool key_tile = n0 < key_cols;
+      const int m = key_tile ? n0 / a.H : 0;
+      const int c0 = key_tile ? n0 - m * a.H : n0 - key_cols;
+      float* qk = ctl->qk[q];
+      if (key_tile) {
+        // q_w * k_w of the tile's 256 columns, staged per warp (no cross-warp barrier)
+        __syncwarp();
+        for (int c = static_cast<int>(lane); c < BN; c += 32) {
+          const int64_t idx = static_cast<int64_t>(c0 + c) * a.hc + m;
+          qk[c] = __ldg(a.q_w + idx) * __ldg(a.k_w + idx);
+        }
+        __syncwarp();
+      }
+      const bool ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag);
+      if (!ok) {
+        if (lane == 0 && !*abort_flag) raise_abort(ctl, a.status);
+        break;
+      }
+      tc_fence_after();
+      const int64_t t = static_cast<int64_t>(mb) * BM + row;
+      const bool live = t < a.M;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if (key_tile) {
+        const uint4* hrow = reinterpret_cast<const uint4*>(a.h + (t * a.hc + m) * a.H + c0);
+        float dot = 0.f, kk = 0.f, hh = 0.f;
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint4 hv[4];
+          if (live) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) hv[i] = __ldg(hrow + ch * 4 + i);
+          }
+          uint32_t r[32];
+          __syncwarp();
+          tc_ld32(taddr + ch * 32, r);
+          if (live) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t w4[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int col = ch * 32 + i * 8 + j * 2;
+                const float h0 = bf16f(w4[j] & 0xffffu), h1 = bf16f(w4[j] >> 16);
+                const float k0 = __uint_as_float(r[i * 8 + j * 2]);
+                const float k1 = __uint_as_float(r[i * 8 + j * 2 + 1]);
+                dot += h0 * qk[col] * k0 + h1 * qk[col + 1] * k1;
+                kk += k0 * k0 + k1 * k1;
+                hh += h0 * h0 + h1 * h1;
+              }
+            }
+          }
+        }
+        if (live) a.partials[(t * a.hc + m) * ntile + c0 / BN] = make_float4(dot, kk, hh, 0.f);
+      } else {
+        uint4* vrow = reinterpret_cast<uint4*>(a.v + t * a.H + c0);
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          __syncwarp();
+          tc_ld32(taddr + ch * 32, r);
+          if (live) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[i * 8 + j * 2]),
+                                                         __uint_as_float(r[i * 8 + j * 2 + 1]));
+                pk[j] = *reinterpret_cast<uint32_t*>(&b);
+              }
+              vrow[ch * 4 + i] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+__global__ void pack_wkv_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
+                                uint16_t* __restrict__ wt) {
+  __shared__ uint16_t tile[32][33];
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int64_t k0 = static_cast<int64_t>(blockIdx.y) * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t k = k0 + i, n = n0 + threadIdx.x;
+    if (k < K && n < N) tile[i][threadIdx.x] = w[k * N + n];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t n = n0 + i, k = k0 + threadIdx.x;
+    if (k < K && n < N) wt[n * K + k] = tile[threadIdx.x][i];
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int get_encode_fn(EncodeTiledFn* out) {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                       cudaEnableDefault, &q);
+    if (err != cudaSuccess || q != cudaDriverEntryPointSuccess || p == nullptr)
+      return fail(ENGRAM_E_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  *out = fn;
+  return ENGRAM_OK;
+}
+
+// 2-D bf16 tensor [rows][cols] (cols contiguous), box = box_rows x 64 columns,
+// 128-byte swizzle, zero fill outside the tensor.
+int make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc;
+  int rc = get_encode_fn(&enc);
+  if (rc) return rc;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ENGRAM_E_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return ENGRAM_OK;
+}
+
+size_t project_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + sizeof(SmemCtl); }
+
+}  // namespace
+}  // namespace engram
+
+using namespace engram;
+
+extern "C" int engram_pack_wkv(const uint16_t* wkv_d, int64_t K, int64_t N, uint16_t* wkv_packed_d,
+                               void* stream) {
+  if (K < 1 || N < 1) return fail(ENGRAM_E_INVALID, "K and N must be positive");
+  if (!wkv_d || !wkv_packed_d) return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (wkv_d == wkv_packed_d) return fail(ENGRAM_E_INVALID, "in-place repack is not supported");
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  const int64_t gx = (N + 31) / 32, gy = (K + 31) / 32;
+  if (gy > 65535) return fail(ENGRAM_E_SHAPE, "K too large");
+  pack_wkv_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), dim3(32, 8), 0,
+                    as_stream(stream)>>>(wkv_d, K, N, wkv_packed_d);
+  return check_launch("pack_wkv_kernel");
+}
+
+extern "C" size_t engram_project_partials_bytes(int64_t n_tokens, int32_t hidden, int32_t hc) {
+  if (n_tokens < 0 || hidden < 256 || hc < 1) return 0;
+  return static_cast<size_t>(n_tokens) * hc * (hidden / 256) * 4 * sizeof(float);
+}
+
+extern "C" int engram_project(const uint16_t* e_d, int64_t n_tokens, int64_t K,
+                              const uint16_t* wkv_packed_d, int32_t hidden, int32_t hc,
+                              const uint16_t* h_d, const float* q_w_d, const float* k_w_d,
+                              float* partials_d, uint16_t* v_d, int32_t* status_d, void* stream) {
+  if (n_tokens < 0) return fail(ENGRAM_E_INVALID, "n_tokens < 0");
+  if (K < BK || K % BK != 0 || K > (int64_t(1) << 20)) return fail(ENGRAM_E_SHAPE, "K %lld must be a positive multiple of 64", (long long)K);
+  if (hidden < BN || hidden % BN != 0) return fail(ENGRAM_E_SHAPE, "hidden %d must be a multiple of 256", hidden);
+  if (hc < 1 || hc > kMaxHc) return fail(ENGRAM_E_SHAPE, "hc %d not in [1, %d]", hc, kMaxHc);
+  if (n_tokens == 0) return ENGRAM_OK;
+  if (n_tokens > (int64_t(1) << 31) - BM) return fail(ENGRAM_E_SHAPE, "too many tokens");
+  if (!e_d || !wkv_packed_d || !h_d || !q_w_d || !k_w_d || !partials_d || !v_d)
+    return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (!aligned(e_d, 16) || !aligned(wkv_packed_d, 16) || !aligned(h_d, 16) || !aligned(partials_d, 16) ||
+      !aligned(v_d, 16))
+    return fail(ENGRAM_E_ALIGN, "e, wkv, h, partials and v must be 16-byte aligned");
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  const int64_t N = static_cast<int64_t>(hc + 1) * hidden;
+  CUtensorMap tmA, tmB;
+  if ((rc = make_tmap(&tmA, e_d, static_cast<uint64_t>(n_tokens), static_cast<uint64_t>(K), BM))) return rc;
+  if ((rc = make_tmap(&tmB, wkv_packed_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN))) return rc;
+  ProjArgs a;
+  a.M = n_tokens;
+  a.K = static_cast<int32_t>(K);
+  a.H = hidden;
+  a.hc = hc;
+  a.mt = static_cast<int32_t>((n_tokens + BM - 1) / BM);
+  a.nt = static_cast<int32_t>(N / BN);
+  const int64_t tiles = static_cast<int64_t>(a.mt) * a.nt;
+  if (tiles > INT32_MAX) return fail(ENGRAM_E_SHAPE, "too many tiles");
+  a.num_tiles = static_cast<int32_t>(tiles);
+  a.h = h_d;
+  a.q_w = q_w_d;
+  a.k_w = k_w_d;
+  a.partials = reinterpret_cast<float4*>(partials_d);
+  a.v = v_d;
+  a.status = status_d;
+  const size_t smem = project_smem_bytes();
+  cudaError_t err = cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(project): %s", cudaGetErrorString(err));
+  const int grid = static_cast<int>(a.num_tiles < sms ? a.num_tiles : sms);
+  project_kernel<<<grid, kThreads, smem, as_stream(stream)>>>(tmA, tmB, a);
+  return check_launch("project_kernel");
+}

@@ -1,0 +1,303 @@
+/*
+ * engram.h -- C ABI of the Engram lookup layer (hashed n-gram conditional
+ * memory) for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Pages cited by title:
+ *   [P-V41]    "DeepSeek-V4.1 模型结构（5）：记忆，Engram"
+ *   [P-LMNT]   "Engram条件记忆：DeepSeek-V4.1-Flash中196B稀疏参数N-gram哈希查表的实现原理"
+ *   [P-O1]     "条件记忆：DeepSeek V4.1 Engram 如何用 O(1) 查表换掉一层计算"
+ *   [P-DS4]    "ds4.c 学习笔记" -- glossary entry "Engram"
+ *   [P-DETAIL] "DeepSeek Engram 详解：把静态知识从计算里拆出来"
+ *
+ * Conventions shared by every entry point
+ *   - Every function returns 0 (ENGRAM_OK) or a negative ENGRAM_E_* code and
+ *     never throws.  engram_last_error() returns a thread-local message for
+ *     the last failure on the calling thread.
+ *   - Pointers named *_d are device pointers; the caller allocates and owns
+ *     them.  The library allocates no device memory.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream).  Results are visible after
+ *     the caller synchronises that stream.
+ *   - Problems found on the device (bad token id, row out of range, bad
+ *     history slot, a bounded wait that ran out) are OR-ed into the caller's
+ *     device word `status_d` (ENGRAM_ST_* bits) when it is non-NULL; the
+ *     kernel then writes a defined fallback (masked position / zero row) and
+ *     completes.  No kernel traps.
+ *   - bf16 tensors are passed as uint16_t* holding bf16 bit patterns.
+ *   - Every kernel is compiled for sm_103a only; entry points that launch
+ *     work return ENGRAM_E_DEVICE on any other GPU.
+ */
+#ifndef ENGRAM_H
+#define ENGRAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ENGRAM_ABI_VERSION 1
+
+#define ENGRAM_MAX_LAYERS 8
+#define ENGRAM_MAX_NGRAM 4   /* n-gram orders 2..max_ngram; history depth max_ngram-1 */
+#define ENGRAM_MAX_COLS 32   /* (max_ngram-1) * n_heads */
+#define ENGRAM_DEAD (-1)     /* raw / compressed id of an image position */
+#define ENGRAM_ROW_BYTES 264 /* 256 E4M3 weights + 8 E8M0 scales */
+#define ENGRAM_HEAD_DIM 256
+
+/* Return codes. */
+enum {
+  ENGRAM_OK = 0,
+  ENGRAM_E_INVALID = -1,  /* null pointer, bad count, bad layer index */
+  ENGRAM_E_VOCAB = -2,    /* compressed vocabulary differs from the expected one */
+  ENGRAM_E_SHAPE = -3,    /* unsupported or inconsistent sizes */
+  ENGRAM_E_ALIGN = -4,    /* a pointer is not aligned as the entry point requires */
+  ENGRAM_E_RANGE = -5,    /* a value does not fit (row count >= 2^31, multiplier bound) */
+  ENGRAM_E_CUDA = -6,     /* a CUDA runtime call or launch failed */
+  ENGRAM_E_DEVICE = -7    /* the current device is not an sm_103 GPU */
+};
+
+/* Bits OR-ed into the device status word. */
+#define ENGRAM_ST_BAD_TOKEN 0x1u /* raw id not in [0, V_raw) and not DEAD, or map value not in [0, V) */
+#define ENGRAM_ST_BAD_ROW 0x2u   /* row id not in [0, total_rows) */
+#define ENGRAM_ST_BAD_SLOT 0x4u  /* decode history slot >= n_slots */
+#define ENGRAM_ST_TIMEOUT 0x8u   /* a bounded on-chip wait ran out; outputs are undefined */
+
+/* ------------------------------------------------------------------------ */
+/* Layout                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Inputs of engram_build_layout.  The names follow the checkpoint config
+ * keys listed on [P-LMNT] (整体架构 table): engram_vocab_size (base_rows),
+ * engram_layer_ids, engram_max_ngram_size, engram_n_heads, engram_head_dim,
+ * engram_compressed_vocab_size (vocab_compressed). */
+typedef struct engram_layout_params {
+  int64_t vocab_compressed;  /* V: compressed vocabulary size */
+  int64_t expected_vocab;    /* 0: no check; otherwise must equal V (ENGRAM_E_VOCAB) */
+  int64_t base_rows;         /* primes are taken strictly above this value */
+  int32_t n_layers;          /* 1..ENGRAM_MAX_LAYERS */
+  int32_t layer_ids[ENGRAM_MAX_LAYERS];
+  int32_t max_ngram;         /* 2..ENGRAM_MAX_NGRAM (4 in DeepSeek-V4.1) */
+  int32_t n_heads;           /* heads per order (8); (max_ngram-1)*n_heads <= ENGRAM_MAX_COLS */
+  int32_t head_dim;          /* 256 (the only row format supported) */
+  int32_t pad_id;            /* compressed id used for padding, 0 <= pad_id < V */
+  int32_t use_multiplier_override; /* nonzero: take multipliers from the array below */
+  int64_t multiplier_override[ENGRAM_MAX_LAYERS][ENGRAM_MAX_NGRAM];
+} engram_layout_params;
+
+/* Immutable description of every layer's table.  Column j (0 <= j < n_cols)
+ * is order n = 2 + j / n_heads, head k = j % n_heads. */
+typedef struct engram_layout {
+  int64_t vocab_compressed;
+  int64_t base_rows;
+  int32_t n_layers;
+  int32_t max_ngram;
+  int32_t n_heads;
+  int32_t n_cols;
+  int32_t head_dim;
+  int32_t pad_id;
+  int32_t layer_ids[ENGRAM_MAX_LAYERS];
+  int64_t total_rows[ENGRAM_MAX_LAYERS];               /* sum of the layer's primes */
+  int64_t primes[ENGRAM_MAX_LAYERS][ENGRAM_MAX_COLS];
+  int64_t offsets[ENGRAM_MAX_LAYERS][ENGRAM_MAX_COLS]; /* exclusive cumulative sum */
+  uint64_t reciprocal[ENGRAM_MAX_LAYERS][ENGRAM_MAX_COLS]; /* floor((2^64-1)/p), for the modulo */
+  int64_t multipliers[ENGRAM_MAX_LAYERS][ENGRAM_MAX_NGRAM];
+} engram_layout;
+
+/* Build the table layout on the host (no device work).
+ *
+ * Primes: [P-V41] §"一层只有一张表" (search upward from engram_vocab_size,
+ * one prime per head, never reused; the printed per-layer min/max/sum for
+ * layers 1 and 14) and [P-O1] §2.2 (one ascending sequence consumed in
+ * (layer, order, head) order; primality by deterministic Miller-Rabin).
+ * This build takes the primes strictly greater than base_rows.
+ * Offsets: [P-O1] §2.2 / [P-DS4] §布局与哈希探测 step 3 (cumulative sum).
+ * Multipliers: [P-V41] §"哈希函数" under eq. (H) and [P-O1] §4.3 -- per
+ * layer, odd, drawn from a generator seeded with 10007 * layer_id and bounded
+ * by int64max // V // 2.  This library draws them from SplitMix64 (Steele,
+ * Lea & Flood 2014): r_i = i-th output mod half, m_i = 2 r_i + 1, with
+ * half = ((2^63-1) // V) // 2.  Checkpoint multipliers from another generator
+ * are passed through use_multiplier_override (each must be odd and keep
+ * (V-1) * m within int64).
+ *
+ * Errors: ENGRAM_E_INVALID (null pointer, counts out of range, pad id not a
+ * compressed id), ENGRAM_E_VOCAB (expected_vocab != V, the guard of
+ * [P-V41] under eq. (H) and [P-O1] §2.1), ENGRAM_E_SHAPE (head_dim != 256,
+ * too many columns), ENGRAM_E_RANGE (a layer's row count would reach 2^31, or
+ * an override multiplier breaks the bound). */
+int engram_build_layout(const engram_layout_params* params, engram_layout* out);
+
+/* sizeof(engram_layout_params) and sizeof(engram_layout), for bindings. */
+size_t engram_layout_params_size(void);
+size_t engram_layout_size(void);
+
+/* ------------------------------------------------------------------------ */
+/* Hash (stages 1-3): token map, suffix window, multiplicative-XOR mix,      */
+/* per-head prime modulo plus segment offset.                                */
+/* ------------------------------------------------------------------------ */
+
+/* Prefill hash over packed sequences.
+ *
+ * For every position t of sequence s (positions cu_seqlens_d[s] ..
+ * cu_seqlens_d[s+1]-1):
+ *   x'_t = token_map_d[raw_ids_d[t]]                 ([P-V41] §tokenizer 压缩)
+ *   g_i  = x'_{t-i} for i < max_ngram; before the sequence start the slot comes
+ *          from hist_d[s][i-1-(t-start)] (most recent first) or, with
+ *          hist_d == NULL, is pad_id                  ([P-DETAIL] §3.2)
+ *   from the first DEAD slot on every slot is pad_id ([P-V41] image tokens,
+ *          [P-LMNT] §多模态细节)
+ *   mix_n = XOR_{i<n} g_i * m_i, n = 2..max_ngram   ([P-V41] eq. (H))
+ *   row_ids_d[t][j] = mix_{n(j)} mod p_j + offset_j  ([P-DS4] step 3)
+ *   mask_d[t] = 1 if the position itself is DEAD, else 0.
+ * After the hash, hist_d (if non-NULL) is advanced to the last max_ngram-1
+ * compressed ids of each sequence (DEAD kept as -1), so a later call on the
+ * next chunk continues the same n-grams ([P-LMNT] §第二步: prefill and decode
+ * share one history).
+ *
+ * Arguments
+ *   layout, layer     layout from engram_build_layout; 0 <= layer < n_layers
+ *   raw_ids_d         int32 [n_tokens]; values in [0, vocab_raw) or DEAD
+ *   cu_seqlens_d      int64 [n_seqs+1], nondecreasing, [0] = 0, [n_seqs] = n_tokens
+ *   token_map_d       int32 [vocab_raw]; values in [0, V)
+ *   hist_d            int32 [n_seqs][max_ngram-1] in/out, or NULL (all pad, not written)
+ *   row_ids_d         int32 [n_tokens][n_cols] out
+ *   mask_d            uint8 [n_tokens] out
+ *   status_d          int32 device word (OR-ed ENGRAM_ST_*), or NULL
+ * A bad raw id or map value sets ENGRAM_ST_BAD_TOKEN and the position is
+ * treated as DEAD.  n_tokens == 0 is a no-op. */
+int engram_hash(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
+                int64_t n_tokens, const int64_t* cu_seqlens_d, int32_t n_seqs,
+                const int32_t* token_map_d, int64_t vocab_raw, int32_t* hist_d,
+                int32_t* row_ids_d, uint8_t* mask_d, int32_t* status_d, void* stream);
+
+/* One decode step: one new raw id per batch entry, hashed against the
+ * sequence's rolling history and committed in the same launch ([P-O1] §4.4;
+ * [P-DS4] §布局与哈希探测: the hash state is the last 3 ids and a copy of it is
+ * a snapshot).
+ *
+ *   raw_ids_d  int32 [batch]
+ *   slots_d    int32 [batch]: history row of each entry, or -1 for a padding
+ *              entry (hashed with an all-pad history, masked, commits nothing;
+ *              [P-O1] §4.4: padding rows must not pollute the history).
+ *              Two entries of one call must not name the same slot.
+ *   hist_d     int32 [n_slots][max_ngram-1] in/out; a used slot becomes
+ *              (x', h0, h1, ...) after the step.
+ *   row_ids_d  int32 [batch][n_cols]; mask_d uint8 [batch] (1 = DEAD or padding)
+ * A slot >= n_slots sets ENGRAM_ST_BAD_SLOT and the entry is treated as padding. */
+int engram_hash_step(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
+                     const int32_t* slots_d, int32_t batch, const int32_t* token_map_d,
+                     int64_t vocab_raw, int32_t* hist_d, int64_t n_slots, int32_t* row_ids_d,
+                     uint8_t* mask_d, int32_t* status_d, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Gather + dequantise (stage 4)                                             */
+/* ------------------------------------------------------------------------ */
+
+/* e_d[t][256*j + c] = bf16_rne(E4M3(b[c]) * 2^(s[c/32] - 127)) where b, s are
+ * the 256 weight bytes and 8 scale bytes of row row_ids_d[t][j]
+ * ([P-V41] §"196B 参数怎么存、怎么取"; [P-DS4] §布局与哈希探测 and the
+ * e4m3_e8m0_32_row264 encoding of §永不常驻的 I/O 设计; [P-O1] §2.3).
+ * E4M3 is OCP FP8 E4M3 (no infinities, 0x7F/0xFF NaN), E8M0 is the OCP scale
+ * (0xFF NaN).  The result is the exact product rounded once to bf16.
+ *
+ *   table_d      uint8 [total_rows][264], 16-byte aligned (ENGRAM_E_ALIGN)
+ *   table_bytes  size of the table allocation in bytes, >= total_rows * 264
+ *   row_ids_d    int32 [n_tokens][n_cols]
+ *   e_d          bf16 [n_tokens][n_cols*256] out, 16-byte aligned
+ * A row id outside [0, total_rows) sets ENGRAM_ST_BAD_ROW and its 256 outputs
+ * are +0. */
+int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows, int64_t table_bytes,
+                          const int32_t* row_ids_d, int64_t n_tokens, int32_t n_cols,
+                          uint16_t* e_d, int32_t* status_d, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* wkv projection with the gate reduction fused (stage 5a/5b)                */
+/* ------------------------------------------------------------------------ */
+
+/* Repack wkv from [K][N] (kv = e @ wkv, [P-V41] §"每条流一个 key 的设计":
+ * one [6144, 25600] matrix) to the K-major [N][K] operand layout of the
+ * tensor-core projection.  One-time, for static weights.  Both bf16. */
+int engram_pack_wkv(const uint16_t* wkv_d, int64_t K, int64_t N, uint16_t* wkv_packed_d,
+                    void* stream);
+
+/* Bytes of the partial-sum buffer of engram_project:
+ * float32 [n_tokens][hc][hidden/256][4]. */
+size_t engram_project_partials_bytes(int64_t n_tokens, int32_t hidden, int32_t hc);
+
+/* kv = e @ wkv on the tensor cores (bf16 x bf16 -> fp32), with the gate's
+ * reductions in the epilogue ([P-V41] §门控; [P-DS4] §消费):
+ *   columns [m*H, (m+1)*H) are key k^(m+1), m < hc; columns [hc*H, (hc+1)*H)
+ *   are the value v.
+ *   For every token t, stream m and 256-column tile q of key m the epilogue
+ *   writes partials_d[t][m][q] = { sum_i h_{m,i} q_w[i][m] k_w[i][m] k_{m,i},
+ *   sum_i k_{m,i}^2, sum_i h_{m,i}^2, 0 } over the tile's 256 columns i;
+ *   keys are not stored.  The value is stored as v_d[t][i] = bf16_rne(v_i).
+ *
+ *   e_d          bf16 [n_tokens][K], K = n_cols*256, 16-byte aligned
+ *   wkv_packed_d bf16 [(hc+1)*hidden][K] from engram_pack_wkv, 16-byte aligned
+ *   h_d          bf16 [n_tokens][hc][hidden] residual streams (read only here)
+ *   q_w_d, k_w_d float32 [hidden][hc]
+ *   partials_d   float32, engram_project_partials_bytes(...) bytes
+ *   v_d          bf16 [n_tokens][hidden] out
+ * Requires hidden % 256 == 0, K % 64 == 0, 1 <= hc <= 8.  A bounded
+ * on-chip wait that runs out sets ENGRAM_ST_TIMEOUT. */
+int engram_project(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint16_t* wkv_packed_d,
+                   int32_t hidden, int32_t hc, const uint16_t* h_d, const float* q_w_d,
+                   const float* k_w_d, float* partials_d, uint16_t* v_d, int32_t* status_d,
+                   void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Gate + residual add (stage 5b/5c)                                          */
+/* ------------------------------------------------------------------------ */
+
+/* For every token t and stream m (sums over the partials' tiles in a fixed
+ * order):
+ *   s = dot * rsqrt(hh/H + eps) * rsqrt(kk/H + eps) * score_scale
+ *   g = sigmoid(copysign(sqrt(max(|s|, clamp)), s))
+ *   h_d[t][m][i] <- bf16_rne(h + g * bf16(v_d[t][i]))   in fp32
+ * ([P-V41] §门控 and §"sigmoid 之前多一步带符号的平方根"; [P-DS4] §消费).
+ * Masked positions (mask_d[t] != 0) leave h_d untouched and get g = 0
+ * ([P-V41] image tokens; [P-DS4] step 4: the masked branch returns).
+ * score_scale is H^-0.5 in this build's reading of the pages ([P-V41]
+ * derives s = sqrt(d) cos(theta); [P-DS4] prints a sqrt(width) factor).
+ *
+ *   partials_d   from engram_project
+ *   v_d          bf16 [n_tokens][hidden]
+ *   h_d          bf16 [n_tokens][hc][hidden], updated in place, 16-byte aligned
+ *   mask_d       uint8 [n_tokens], or NULL (no masked positions)
+ *   gate_out_d   float32 [n_tokens][hc] out, or NULL */
+int engram_gate_add(const float* partials_d, const uint16_t* v_d, uint16_t* h_d,
+                    const uint8_t* mask_d, int64_t n_tokens, int32_t hidden, int32_t hc, float eps,
+                    float clamp, float score_scale, float* gate_out_d, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Test-data and diagnostics                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Fill a table with synthetic rows: row r holds the little-endian bytes of
+ * SplitMix64 outputs number 33*r + j + 1 (j = 0..32) of a stream whose state
+ * starts at `seed`; weight bytes equal to an E4M3 NaN code (0x7F, 0xFF) are
+ * replaced by byte ^ 1 and each scale byte b becomes 120 + (b mod 11).  This
+ * is input generation for tests and benchmarks, not part of the method.
+ *   table_d  uint8 [n_rows][264], 8-byte aligned */
+int engram_fill_synthetic_table(uint8_t* table_d, int64_t n_rows, uint64_t seed, void* stream);
+
+/* Diagnostic of the on-device modulo: out_d[i][j] = x_d[i] mod p_j + offset_j
+ * for the layer's n_cols columns, computed by the same device routine as
+ * engram_hash.  x_d: uint64 [n] (any 64-bit value); out_d: int64 [n][n_cols]. */
+int engram_selftest_mod(const engram_layout* layout, int32_t layer, const uint64_t* x_d, int64_t n,
+                        int64_t* out_d, void* stream);
+
+/* Thread-local message of the last failure (empty string if none). */
+const char* engram_last_error(void);
+/* Name of an ENGRAM_* return code. */
+const char* engram_status_string(int code);
+/* ENGRAM_ABI_VERSION of the loaded library. */
+int engram_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENGRAM_H */

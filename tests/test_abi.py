@@ -1,0 +1,108 @@
+"""The C-ABI library loads, exports every declared symbol, and its host-side
+layout builder and argument checks agree with the oracle (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import hashed_gram_conditional_gb300 as eg
+from conftest import ROOT
+from oracle import layout as OL
+
+HEADER = os.path.join(ROOT, "include", "engram.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(eg.library_path()):
+        from hashed_gram_conditional_gb300 import build
+        build.build()
+    return eg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(engram_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for required in ["engram_build_layout", "engram_hash", "engram_hash_step", "engram_gather_dequant",
+                     "engram_project", "engram_gate_add"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_struct_sizes_match(lib):
+    assert lib.engram_layout_size() == ctypes.sizeof(eg._Layout)
+    assert lib.engram_layout_params_size() == ctypes.sizeof(eg._LayoutParams)
+    assert lib.engram_abi_version() == 1
+
+
+@pytest.mark.parametrize("vocab,base,layers", [(1000, 4099, [1]), (99092, 2_000_000, [1]),
+                                               (99092, 16_000_000, [1, 14]), (12, 16_000_000, [0, 3, 7])])
+def test_layout_equals_oracle(lib, vocab, base, layers):
+    ref = OL.build_layout(vocab, base, layers, 4, 8, pad_id=min(7, vocab - 1))
+    got = eg.build_layout(vocab, base, layers, 4, 8, pad_id=min(7, vocab - 1))
+    assert got.n_cols == 24 and got.n_layers == len(layers)
+    for li, x in enumerate(ref.layers):
+        assert got.layer_id(li) == x.layer_id
+        assert got.primes(li) == x.primes
+        assert got.offsets(li) == x.offsets
+        assert got.total_rows(li) == x.total_rows
+        assert got.multipliers(li) == x.multipliers
+        for j, p in enumerate(x.primes):
+            assert got._raw.reciprocal[li][j] == (2 ** 64 - 1) // p
+
+
+def test_layout_generic_orders_heads(lib):
+    for max_ngram, heads in [(2, 8), (3, 8), (4, 4), (3, 16)]:
+        ref = OL.build_layout(1000, 4099, [2, 15], max_ngram, heads)
+        got = eg.build_layout(1000, 4099, [2, 15], max_ngram, heads)
+        assert got.n_cols == (max_ngram - 1) * heads
+        for li, x in enumerate(ref.layers):
+            assert got.primes(li) == x.primes and got.multipliers(li) == x.multipliers
+
+
+def test_layout_override(lib):
+    got = eg.build_layout(1000, 4099, [1], multipliers=[[3, 5, 7, 9]])
+    assert got.multipliers(0) == [3, 5, 7, 9]
+    with pytest.raises(eg.EngramError, match="RANGE"):
+        eg.build_layout(1000, 4099, [1], multipliers=[[4, 5, 7, 9]])
+    with pytest.raises(eg.EngramError, match="RANGE"):
+        eg.build_layout(1000, 4099, [1], multipliers=[[(2 ** 63 - 1) // 999 + 2, 5, 7, 9]])
+
+
+def test_layout_errors(lib):
+    with pytest.raises(eg.EngramError, match="VOCAB"):
+        eg.build_layout(99091, 16_000_000, [1], expected_vocab=99092)
+    with pytest.raises(eg.EngramError, match="SHAPE"):
+        eg.build_layout(1000, 4099, [1], head_dim=128)
+    with pytest.raises(eg.EngramError, match="SHAPE"):
+        eg.build_layout(1000, 4099, [1], max_ngram=5)
+    with pytest.raises(eg.EngramError, match="INVALID"):
+        eg.build_layout(1000, 4099, [1], pad_id=1000)
+    with pytest.raises(eg.EngramError, match="RANGE"):
+        eg.build_layout(1000, 2 ** 31 - 1000, [1])  # row count would pass 2^31
+    assert lib.engram_build_layout(None, None) == -1
+    assert b"null" in lib.engram_last_error()
+
+
+def test_host_side_argument_checks(lib):
+    """Entry points reject bad sizes before touching a device."""
+    P = ctypes.c_void_p
+    assert lib.engram_gather_dequant(P(16), 10, 10 * 264, P(16), 4, 0, P(16), None, None) == -3
+    assert lib.engram_gather_dequant(P(16), 10, 10 * 264 - 1, P(16), 4, 24, P(16), None, None) == -3
+    assert lib.engram_project(P(16), 128, 6144, P(16), 100, 4, P(16), P(16), P(16), P(16), P(16), None, None) == -3
+    assert lib.engram_project(P(16), 128, 6100, P(16), 256, 4, P(16), P(16), P(16), P(16), P(16), None, None) == -3
+    assert lib.engram_gate_add(P(16), P(16), P(16), None, 4, 256, 9, 1e-6, 1e-6, 0.0625, None, None) == -3
+    lay = eg.build_layout(1000, 4099, [1])
+    assert lib.engram_hash(lay.ref, 3, P(16), 4, P(16), 1, P(16), 1300, None, P(16), P(16), None, None) == -1
+    assert lib.engram_project_partials_bytes(16384, 5120, 4) == 16384 * 4 * 20 * 16

@@ -1,0 +1,119 @@
+"""GPU parity of the tensor-core projection, the fused gate partials and the residual add."""
+import numpy as np
+import pytest
+import torch
+
+import hashed_gram_conditional_gb300 as eg
+from gpu_util import (DEV, GATE_ATOL, bf16, bits, dot_error_bound, f32, i32, require_gpu, residual_close,
+                      status, u8)
+from oracle import dequant as OD
+from oracle import gate as OG
+from workloads import bf16_bits_to_f64, normal_bf16_bits, uniform_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _gpu():
+    require_gpu()
+
+
+def _inputs(T, H, hc, K=6144, seed=0, e_std=1.0):
+    e = normal_bf16_bits((T, K), e_std, seed, 1)
+    w = normal_bf16_bits((K, (hc + 1) * H), 0.02, seed, 2)
+    h = normal_bf16_bits((T, hc, H), 1.0, seed, 3)
+    qw = uniform_f32((H, hc), 0.5, 1.5, seed, 4)
+    kw = uniform_f32((H, hc), 0.5, 1.5, seed, 5)
+    return e, w, h, qw, kw
+
+
+def _oracle(e, w, h, qw, kw, mask, T, H, hc):
+    ef, wf = bf16_bits_to_f64(e), bf16_bits_to_f64(w)
+    kv = OG.project(ef, wf)
+    k, v = OG.split_kv(kv, H, hc)
+    hf = bf16_bits_to_f64(h)
+    g = OG.gate(hf, k, qw, kw, mask)
+    out = OG.residual(hf, g, v, mask)
+    err = dot_error_bound(ef, wf)            # fp32 accumulation bound of every kv element
+    k_err, v_err = OG.split_kv(err, H, hc)
+    return k, v, hf, g, out, k_err, v_err
+
+
+@pytest.mark.parametrize("T,H,hc", [(128, 256, 4), (300, 256, 4), (1, 256, 4), (129, 512, 2), (257, 256, 1)])
+def test_project_partials_v_gate_residual(T, H, hc):
+    e, w, h, qw, kw = _inputs(T, H, hc, seed=T)
+    mask = np.zeros(T, dtype=bool)
+    mask[::17] = True
+    k, v, hf, g, out, k_err, v_err = _oracle(e, w, h, qw, kw, mask, T, H, hc)
+    wp = eg.engram_pack_wkv(bf16(w))
+    # the repack is a pure permutation of the bf16 bits
+    assert (bits(wp) == w.T).all()
+    h_d = bf16(h)
+    st = status()
+    partials, v_d = eg.engram_project(bf16(e), wp, h_d, f32(qw), f32(kw), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # v: fp32 accumulation then one bf16 rounding; the oracle rounds the exact value
+    vb = bf16_bits_to_f64(bits(v_d))
+    vr = OD.bf16_round(v)
+    assert (np.abs(vb - v) <= 2.0 ** -8 * np.abs(v) + v_err).all()   # one bf16 rounding + fp32 sum
+    assert np.mean(vb == vr) > 0.9
+    # partials per 256-column tile
+    P = partials.cpu().numpy().astype(np.float64)
+    ntile = H // 256
+    qk = (qw.astype(np.float64) * kw.astype(np.float64)).T.reshape(hc, ntile, 256)
+    kt = k.reshape(T, hc, ntile, 256)
+    ht = hf.reshape(T, hc, ntile, 256)
+    ke = k_err.reshape(T, hc, ntile, 256)
+    dot = np.einsum("tmqc,mqc,tmqc->tmq", ht, qk, kt)
+    dot_abs = np.einsum("tmqc,mqc,tmqc->tmq", np.abs(ht), qk, np.abs(kt))
+    dot_tol = np.einsum("tmqc,mqc,tmqc->tmq", np.abs(ht), qk, ke) + 1e-5 * dot_abs
+    assert (np.abs(P[..., 0] - dot) <= dot_tol).all()
+    kk = np.sum(kt * kt, axis=3)
+    assert (np.abs(P[..., 1] - kk) <= np.sum(2 * np.abs(kt) * ke + ke ** 2, axis=3) + 1e-5 * kk).all()
+    np.testing.assert_allclose(P[..., 2], np.sum(ht * ht, axis=3), rtol=1e-5)
+    # gate + residual
+    gate = torch.empty((T, hc), dtype=torch.float32, device=DEV)
+    eg.engram_gate_add(partials, v_d, h_d, u8(mask), gate_out=gate)
+    gg = gate.cpu().numpy()
+    assert np.abs(gg - g).max() <= GATE_ATOL
+    assert (gg[mask] == 0).all()
+    hb = bits(h_d)
+    assert (hb[mask] == h[mask]).all()                     # masked rows bit-identical
+    ok, worst, strict = residual_close(bf16_bits_to_f64(hb), out, hf, g, v, v_err)
+    assert ok, (worst, strict)
+
+
+def test_project_identity_selects_rows():
+    """e = one-hot rows: kv reproduces wkv rows exactly (checks operand order and tiling)."""
+    T, H, hc, K = 256, 256, 4, 6144
+    e = np.zeros((T, K), dtype=np.uint16)
+    sel = (np.arange(T) * 37) % K
+    e[np.arange(T), sel] = 0x3F80                          # 1.0
+    w = normal_bf16_bits((K, (hc + 1) * H), 0.02, 9, 1)
+    h = normal_bf16_bits((T, hc, H), 1.0, 9, 2)
+    ones = np.ones((H, hc), dtype=np.float32)
+    partials, v_d = eg.engram_project(bf16(e), eg.engram_pack_wkv(bf16(w)), bf16(h), f32(ones), f32(ones))
+    vb = bits(v_d)
+    assert (vb == w[sel, hc * H:]).all()
+    P = partials.cpu().numpy().astype(np.float64)
+    wf = bf16_bits_to_f64(w)
+    for m in range(hc):
+        km = wf[sel, m * H:(m + 1) * H]
+        np.testing.assert_allclose(P[:, m, 0, 1], np.sum(km * km, axis=1), rtol=1e-5)
+
+
+def test_project_large_m_tiles():
+    """T = 1024 over the full 5120-wide key/value layout (100 N tiles), sampled rows."""
+    T, H, hc = 1024, 5120, 4
+    e, w, h, qw, kw = _inputs(T, H, hc, seed=42)
+    h_d = bf16(h)
+    partials, v_d = eg.engram_project(bf16(e), eg.engram_pack_wkv(bf16(w)), h_d, f32(qw), f32(kw))
+    gate = torch.empty((T, hc), dtype=torch.float32, device=DEV)
+    mask = np.zeros(T, dtype=bool)
+    eg.engram_gate_add(partials, v_d, h_d, u8(mask), gate_out=gate)
+    idx = np.array([0, 1, 127, 128, 500, 1023])
+    k, v, hf, g, out, k_err, v_err = _oracle(e[idx], w, h[idx], qw, kw, mask[idx], len(idx), H, hc)
+    assert np.abs(gate.cpu().numpy()[idx] - g).max() <= GATE_ATOL
+    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
+    assert ok, (worst, strict)
