@@ -76,6 +76,9 @@ WORKLOADS = {
     # decode: 256 sequences, prefix lengths U[0, 8192], 1000 one-token steps
     "decode": Workload("decode", 129280, 99092, 2_000_000, 1, 256, 8192, 5120, 4, 0.0,
                        decode_steps=1000),
+    # profiling case: 4 x 1024 tokens over a 4.8M-row (1.27 GB) table, hidden 5120;
+    # small enough for multi-pass counter captures, every input still larger than L2
+    "profile": Workload("profile", 129280, 99092, 200_000, 1, 4, 1024, 5120, 4, 0.05),
     # full scale: primes above 16,000,000 (384,006,168 rows), 131072 tokens in 8 chunks
     "fullscale": Workload("fullscale", 129280, 99092, 16_000_000, 1, 1, 131072, 5120, 4, 0.0,
                           chunks=8),
