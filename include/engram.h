@@ -272,6 +272,41 @@ int engram_gate_add(const float* partials_d, const uint16_t* v_d, uint16_t* h_d,
                     float clamp, float score_scale, float* gate_out_d, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Projection + gate without device allocation                                */
+/* ------------------------------------------------------------------------ */
+
+/* Size of the library's static stage scratch (8 MiB). */
+#define ENGRAM_STAGE_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory where they run this stage, e.g. a
+ * serving engine that has reserved all of HBM for its own pools and forbids
+ * cudaMalloc on its hot path, or a plugin inside a host framework whose
+ * allocator it does not own.
+ *
+ * Same result as engram_project followed by engram_gate_add on the same
+ * arguments, but the two intermediates (partial sums and bf16 v) live in a
+ * file-scope device array of ENGRAM_STAGE_STATIC_SCRATCH_BYTES, so the
+ * caller passes only inputs and outputs and nothing is allocated.
+ *   e_d, wkv_packed_d, q_w_d, k_w_d, mask_d (nullable): as engram_project /
+ *   engram_gate_add; h_d: updated in place; gate_out_d: nullable.
+ * Limit: round_up(engram_project_partials_bytes(n_tokens, hidden, hc), 256)
+ *   + n_tokens * hidden * 2 must not exceed ENGRAM_STAGE_STATIC_SCRATCH_BYTES
+ *   (about 728 tokens at hidden 5120, hc 4); larger requests return
+ *   ENGRAM_E_RANGE with the limit in engram_last_error().
+ * The array is part of the library image, so every GPU that loads the
+ * library holds it until the process exits.  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  All calls share
+ * the array: calls that overlap on the GPU race on it.  Each call writes
+ * every scratch element it reads, so no clearing is needed between calls. */
+int engram_project_gate_add_noalloc(const uint16_t* e_d, int64_t n_tokens, int64_t K,
+                                    const uint16_t* wkv_packed_d, int32_t hidden, int32_t hc,
+                                    uint16_t* h_d, const float* q_w_d, const float* k_w_d,
+                                    const uint8_t* mask_d, float eps, float clamp, float score_scale,
+                                    float* gate_out_d, int32_t* status_d, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Test-data and diagnostics                                                  */
 /* ------------------------------------------------------------------------ */
 
