@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Engram layer tokens/s (hash+gather+gate) at T=16k; gather HBM GB/s vs peak"
 GATHER_BYTES_PER_TOKEN = 4 + 24 * 264 + 24 * 256 * 2   # raw id + 24 rows + bf16 e = 18,628 B
-KERNEL_FILES = ["project.cu", "gather.cu", "hash.cu", "gate.cu", "engram_internal.h"]
+KERNEL_FILES = ["project.cu", "gather.cu", "hash.cu", "engram_internal.h"]
 
 
 def parse():
@@ -202,12 +202,10 @@ def run_ours(args, rank, world, local):
         eg.engram_gather_dequant(layer.table, layer.total_rows, b_["rows"], b_["e"], status)
         if ev is not None:
             ev[2].record(stream)
-        eg.engram_project(b_["e"], layer.wkv_packed, h, layer.q_w, layer.k_w, b_["partials"], b_["v"], status)
+        eg.engram_project_gate(b_["e"], layer.wkv_packed, h, layer.q_w, layer.k_w, b_["mask"], layer.eps,
+                               layer.clamp, layer.score_scale, None, b_["work"], status)
         if ev is not None:
             ev[3].record(stream)
-        eg.engram_gate_add(b_["partials"], b_["v"], h, b_["mask"], layer.eps, layer.clamp, layer.score_scale)
-        if ev is not None:
-            ev[4].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -216,7 +214,7 @@ def run_ours(args, rank, world, local):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during warm-up")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     props = torch.cuda.get_device_properties(dev)
     gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) is not None else str(local)
     sampler = ClockSampler(gpu_id)
@@ -239,9 +237,9 @@ def run_ours(args, rank, world, local):
     def ms(k, i, j):
         return events[k][i].elapsed_time(events[k][j])
 
-    step_ms = [ms(k, 0, 4) for k in range(args.steps)]
+    step_ms = [ms(k, 0, 3) for k in range(args.steps)]
     stage = {name: [ms(k, i, i + 1) for k in range(args.steps)]
-             for i, name in enumerate(["hash", "gather", "project", "gate_add"])}
+             for i, name in enumerate(["hash", "gather", "project_gate"])}
     total_s = sum(step_ms) / 1e3
     if world > 1:
         t = torch.tensor([total_s], dtype=torch.float64, device=dev)
@@ -292,10 +290,10 @@ def run_ours(args, rank, world, local):
     sustained = total_s >= 2.0
     tf_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     flops = 2.0 * T * 6144 * (w.hc + 1) * w.hidden
-    proj_s = statistics.mean(stage["project"]) / 1e3
+    proj_s = statistics.mean(stage["project_gate"]) / 1e3
     gat_s = statistics.mean(stage["gather"]) / 1e3
     traffic = profiled_traffic()
-    roof = {"bound": "tensor", "kernel": "project_kernel (tcgen05 wkv GEMM + fused gate partials)",
+    roof = {"bound": "tensor", "kernel": "project_kernel<fused> (tcgen05 wkv GEMM, gate and residual in the epilogue)",
             "achieved": flops / proj_s / 1e12, "peak": tf_peak, "unit": "TFLOP/s",
             "frac": flops / proj_s / 1e12 / tf_peak, "traffic": traffic.get("project_kernel"),
             "algorithmic_per_launch": f"{flops:.4g} FLOP (2*T*6144*{(w.hc + 1) * w.hidden}, T={T})",
@@ -324,7 +322,7 @@ def run_ours(args, rank, world, local):
         "stages_ms": {k: statistics.mean(v) for k, v in stage.items()},
         "roofline": roof,
         "roofline_gather": roof_g,
-        "gpu_launches": args.steps * 5,
+        "gpu_launches": args.steps * 4,
         "clocks": clocks,
         "e2e": e2e,
         "wall_s_timed": wall1 - wall0,

@@ -21,8 +21,8 @@ import torch
 __all__ = [
     "EngramError", "Layout", "build_layout", "engram_hash", "engram_hash_step", "engram_gather_dequant",
     "engram_pack_wkv", "engram_project", "engram_gate_add", "engram_fill_synthetic_table",
-    "engram_selftest_mod", "partials_shape", "EngramLayer", "library_path", "ST_BAD_TOKEN", "ST_BAD_ROW",
-    "ST_BAD_SLOT", "ST_TIMEOUT", "DEAD", "ROW_BYTES",
+    "engram_selftest_mod", "engram_project_gate", "project_gate_workspace", "partials_shape", "EngramLayer",
+    "library_path", "ST_BAD_TOKEN", "ST_BAD_ROW", "ST_BAD_SLOT", "ST_TIMEOUT", "DEAD", "ROW_BYTES",
 ]
 
 MAX_LAYERS = 8
@@ -98,6 +98,8 @@ _SIGS = {
     "engram_gate_add": [_P, _P, _P, _P, _I64, _I32, _I32, _F32, _F32, _F32, _P, _P],
     "engram_fill_synthetic_table": [_P, _I64, ctypes.c_uint64, _P],
     "engram_selftest_mod": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _P],
+    "engram_project_gate": [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _P, _P, _F32, _F32, _F32, _P, _P,
+                            ctypes.c_size_t, _P, _P],
 }
 
 
@@ -119,6 +121,8 @@ def _load():
         lib.engram_status_string.argtypes = [ctypes.c_int]
         lib.engram_project_partials_bytes.restype = ctypes.c_size_t
         lib.engram_project_partials_bytes.argtypes = [_I64, _I32, _I32]
+        lib.engram_project_gate_workspace_bytes.restype = ctypes.c_size_t
+        lib.engram_project_gate_workspace_bytes.argtypes = [_I64, _I32, _I32]
         lib.engram_layout_size.restype = ctypes.c_size_t
         lib.engram_layout_params_size.restype = ctypes.c_size_t
         if lib.engram_layout_size() != ctypes.sizeof(_Layout) or \
@@ -380,6 +384,43 @@ def engram_gate_add(partials: torch.Tensor, v: torch.Tensor, h: torch.Tensor, ma
     return gate_out
 
 
+def project_gate_workspace(n_tokens: int, hidden: int, hc: int, device) -> torch.Tensor:
+    """Workspace tensor for engram_project_gate (torch allocations are 256-byte aligned)."""
+    n = _load().engram_project_gate_workspace_bytes(n_tokens, hidden, hc)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device)
+
+
+def engram_project_gate(e: torch.Tensor, wkv_packed: torch.Tensor, h: torch.Tensor, q_w: torch.Tensor,
+                        k_w: torch.Tensor, mask: Optional[torch.Tensor], eps: float = 1e-6, clamp: float = 1e-6,
+                        score_scale: Optional[float] = None, gate_out: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """Fused projection + gate + residual: h <- bf16(h + g * bf16(v)) in place; returns gate_out."""
+    L = _load()
+    dev = e.device
+    _need(e, "e", torch.bfloat16)
+    T, K = e.shape
+    _need(h, "h", torch.bfloat16, dev)
+    if h.dim() != 3 or h.shape[0] != T:
+        raise ValueError("h must be [T][hc][H]")
+    hc, H = h.shape[1], h.shape[2]
+    _need(wkv_packed, "wkv_packed", torch.bfloat16, dev, (hc + 1) * H * K)
+    _need(q_w, "q_w", torch.float32, dev, H * hc)
+    _need(k_w, "k_w", torch.float32, dev, H * hc)
+    if mask is not None:
+        _need(mask, "mask", torch.uint8, dev, T)
+    if gate_out is not None:
+        _need(gate_out, "gate_out", torch.float32, dev, T * hc)
+    if workspace is None:
+        workspace = project_gate_workspace(T, H, hc, dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if score_scale is None:
+        score_scale = H ** -0.5
+    _check(L.engram_project_gate(_ptr(e), T, K, _ptr(wkv_packed), H, hc, _ptr(h), _ptr(q_w), _ptr(k_w), _ptr(mask),
+                                 eps, clamp, score_scale, _ptr(gate_out), _ptr(workspace), workspace.numel(),
+                                 _ptr(status), _stream(dev)), "engram_project_gate")
+    return gate_out
+
+
 def engram_fill_synthetic_table(table: torch.Tensor, n_rows: int, seed: int) -> torch.Tensor:
     L = _load()
     _need(table, "table", torch.uint8)
@@ -406,13 +447,14 @@ def engram_selftest_mod(layout: Layout, layer: int, x: torch.Tensor) -> torch.Te
 class EngramLayer:
     """One Engram layer with resident weights: table, token map, packed wkv, q_w, k_w.
 
-    ``prefill`` runs hash -> gather -> project -> gate_add on the current
-    stream and updates the residual ``h`` in place.
+    ``prefill`` runs hash -> gather -> fused project/gate on the current
+    stream and updates the residual ``h`` in place (``fused=False`` runs the
+    projection and the gate kernel separately).
     """
 
     def __init__(self, layout: Layout, layer: int, table: torch.Tensor, token_map: torch.Tensor,
                  wkv_packed: torch.Tensor, q_w: torch.Tensor, k_w: torch.Tensor, eps: float = 1e-6,
-                 clamp: float = 1e-6, score_scale: Optional[float] = None):
+                 clamp: float = 1e-6, score_scale: Optional[float] = None, fused: bool = True):
         self.layout, self.layer = layout, layer
         self.table, self.token_map = table, token_map
         self.wkv_packed, self.q_w, self.k_w = wkv_packed, q_w, k_w
@@ -420,6 +462,7 @@ class EngramLayer:
         self.eps, self.clamp = eps, clamp
         self.score_scale = self.hidden ** -0.5 if score_scale is None else score_scale
         self.total_rows = layout.total_rows(layer)
+        self.fused = fused
         self._ws = {}
 
     def _buffers(self, T: int, device):
@@ -431,6 +474,7 @@ class EngramLayer:
                 e=torch.empty((T, self.layout.n_cols * HEAD_DIM), dtype=torch.bfloat16, device=device),
                 partials=torch.empty(partials_shape(T, self.hidden, self.hc), dtype=torch.float32, device=device),
                 v=torch.empty((T, self.hidden), dtype=torch.bfloat16, device=device),
+                work=project_gate_workspace(T, self.hidden, self.hc, device),
             )}
         return self._ws[key]
 
@@ -442,8 +486,7 @@ class EngramLayer:
         engram_hash(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, hist, b["rows"], b["mask"],
                     status)
         engram_gather_dequant(self.table, self.total_rows, b["rows"], b["e"], status)
-        engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
-        engram_gate_add(b["partials"], b["v"], h, b["mask"], self.eps, self.clamp, self.score_scale, gate_out)
+        self._gate(b, h, status, gate_out)
         return b
 
     def decode(self, raw_ids: torch.Tensor, slots: torch.Tensor, hist: torch.Tensor, h: torch.Tensor,
@@ -453,6 +496,13 @@ class EngramLayer:
         engram_hash_step(self.layout, self.layer, raw_ids, slots, self.token_map, hist, b["rows"], b["mask"],
                          status)
         engram_gather_dequant(self.table, self.total_rows, b["rows"], b["e"], status)
-        engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
-        engram_gate_add(b["partials"], b["v"], h, b["mask"], self.eps, self.clamp, self.score_scale, gate_out)
+        self._gate(b, h, status, gate_out)
         return b
+
+    def _gate(self, b, h, status, gate_out):
+        if self.fused:
+            engram_project_gate(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["mask"], self.eps, self.clamp,
+                                self.score_scale, gate_out, b["work"], status)
+        else:
+            engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
+            engram_gate_add(b["partials"], b["v"], h, b["mask"], self.eps, self.clamp, self.score_scale, gate_out)

@@ -23,6 +23,16 @@
 //               float4 partial per (position, stream, tile); keys never reach
 //               memory.  For a value tile it rounds v to bf16 and stores it.
 //   Two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// Fused mode (engram_project_gate): within each group of M-blocks every key
+// tile is scheduled before any value tile.  A key tile's epilogue warps
+// publish their partials and bump a per-M-block counter; a value tile's
+// epilogue waits (bounded) until all key tiles of its M-block are published,
+// forms the gates of its rows from the partials and applies
+// h <- bf16(h + g * bf16(v)) directly, so v never reaches memory and the
+// residual traffic overlaps tensor work.  The launch is cooperative, so every
+// CTA is resident and the wait always ends: the key tiles a value tile needs
+// come earlier in the static tile order, and the lowest-numbered waiting tile
+// only ever waits on CTAs that are not themselves waiting.
 // Every wait is bounded; a wait that runs out records ENGRAM_ST_TIMEOUT, the
 // roles unwind, in-flight copies and MMAs are drained and TMEM is freed.
 #include <cuda.h>
@@ -44,7 +54,7 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int kThreads = 192;
-constexpr int kGroupM = 32;  // M-blocks per raster group (L2 reuse of wkv)
+constexpr int kGroupM = 16;  // M-blocks per raster group: e group + wkv wave fit one die's L2 half
 constexpr int kMaxHc = 8;
 
 struct ProjArgs {
@@ -55,12 +65,22 @@ struct ProjArgs {
   int32_t mt;
   int32_t nt;
   int32_t num_tiles;
-  const uint16_t* h;
+  uint16_t* h;           // read (key tiles); updated in place by value tiles in fused mode
   const float* q_w;
   const float* k_w;
   float4* partials;
-  uint16_t* v;
+  uint16_t* v;           // unfused mode only
   int32_t* status;
+  // fused mode only
+  const uint8_t* mask;
+  float* gate_out;
+  int32_t* cnt;          // [mt][hc][4] published key-tile epilogue warps per (M-block, stream, quarter)
+  int32_t* ready;        // [mt] finished (stream, quarter) gate groups per M-block
+  int32_t* abort_g;      // one word: a CTA gave up (tells the others to stop waiting)
+  float* gates;          // [mt*128][hc] finished gates (-1 = masked row)
+  float eps;
+  float clamp;
+  float score_scale;
 };
 
 struct __align__(8) SmemCtl {
@@ -71,7 +91,9 @@ struct __align__(8) SmemCtl {
   uint64_t drain;
   uint32_t tmem_base;
   int32_t abort;
-  float qk[4][BN];  // q_w * k_w of the current key tile, one copy per epilogue warp
+  float qk[4][BN];            // q_w * k_w of the current key tile, one copy per epilogue warp
+  uint32_t sv[4][32][20];     // fused mode: a warp's 32 x 32 bf16 v chunk, rows padded to 80 B
+  float sg[4][32][kMaxHc];    // fused mode: gates of the warp's 32 rows (-1 = leave the row alone)
 };
 
 // Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
@@ -138,13 +160,37 @@ __device__ __forceinline__ void tile_coords(int tile, int mt, int nt, int& mb, i
   nb = local / gm;
 }
 
-__device__ __forceinline__ void raise_abort(SmemCtl* ctl, int32_t* status) {
+__device__ __forceinline__ void raise_abort(SmemCtl* ctl, const ProjArgs& a) {
   ctl->abort = 1;
-  if (status) atomicOr(status, static_cast<int>(ENGRAM_ST_TIMEOUT));
+  if (a.abort_g) atomicExch(a.abort_g, 1);  // tell the other CTAs (fused mode)
+  if (a.status) atomicOr(a.status, static_cast<int>(ENGRAM_ST_TIMEOUT));
+}
+
+// Waits until *cnt >= target (acquire), bounded; false on timeout or abort.
+__device__ bool wait_published(const int32_t* cnt, int target, const volatile int32_t* global_abort,
+                               const volatile int* cta_abort) {
+  const long long t0 = clock64();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    if (v >= target) return true;
+    if (*global_abort || *cta_abort) return false;
+    if (clock64() - t0 > kWaitBudgetCycles) return false;
+    __nanosleep(64);
+  }
 }
 
 __device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
+// Two bf16 lanes of h and v: bf16_rne(h + g * v) in fp32 per lane.
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t h, float g, uint32_t v) {
+  const float lo = __uint_as_float(h << 16) + g * __uint_as_float(v << 16);
+  const float hi = __uint_as_float(h & 0xffff0000u) + g * __uint_as_float(v & 0xffff0000u);
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+template <bool kFuse>
 __global__ void __launch_bounds__(kThreads, 1)
     project_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    ProjArgs a) {
@@ -197,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag)) {
-            if (!*abort_flag) raise_abort(ctl, a.status);
+            if (!*abort_flag) raise_abort(ctl, a);
             ok = false;
             break;
           }
@@ -221,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
         if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1, abort_flag)) {
-          if (!*abort_flag) raise_abort(ctl, a.status);
+          if (!*abort_flag) raise_abort(ctl, a);
           ok = false;
           break;
         }
@@ -231,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag)) {
-            if (!*abort_flag) raise_abort(ctl, a.status);
+            if (!*abort_flag) raise_abort(ctl, a);
             ok = false;
             break;
           }
@@ -278,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag);
       if (!ok) {
-        if (lane == 0 && !*abort_flag) raise_abort(ctl, a.status);
+        if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
         break;
       }
       tc_fence_after();
@@ -316,6 +362,113 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (live) a.partials[(t * a.hc + m) * ntile + c0 / BN] = make_float4(dot, kk, hh, 0.f);
+        if (kFuse) {
+          // Publish this warp's 32 partials; the warp that publishes the last
+          // tile of (M-block, stream, row quarter) finishes those 32 gates.
+          __threadfence();
+          __syncwarp();
+          int prev = 0;
+          if (lane == 0) prev = atomicAdd(a.cnt + (static_cast<int64_t>(mb) * a.hc + m) * 4 + q, 1);
+          prev = __shfl_sync(0xffffffffu, prev, 0);
+          if (prev == ntile - 1) {
+            __threadfence();  // acquire: every tile's partials of these rows are visible
+            if (live) {
+              const bool masked = a.mask != nullptr && a.mask[t] != 0;
+              float g = 0.0f;
+              if (!masked) {
+                const float4* p = a.partials + (t * a.hc + m) * ntile;
+                float sd = 0.f, sk = 0.f, sh = 0.f;
+                for (int q0 = 0; q0 < ntile; q0 += 8) {
+                  float4 x[8];
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) x[i] = (q0 + i < ntile) ? __ldcg(p + q0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {  // tile order: deterministic
+                    sd += x[i].x;
+                    sk += x[i].y;
+                    sh += x[i].z;
+                  }
+                }
+                const float inv_h = 1.0f / static_cast<float>(a.H);
+                const float sc = sd * (1.0f / sqrtf(sh * inv_h + a.eps)) * (1.0f / sqrtf(sk * inv_h + a.eps)) *
+                                 a.score_scale;
+                const float z = copysignf(sqrtf(fmaxf(fabsf(sc), a.clamp)), sc);
+                g = 1.0f / (1.0f + expf(-z));
+              }
+              a.gates[t * a.hc + m] = masked ? -1.0f : g;
+              if (a.gate_out != nullptr) a.gate_out[t * a.hc + m] = g;
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) atomicAdd(a.ready + mb, 1);
+          }
+        }
+      } else if (kFuse) {
+        // ---- value tile, fused: wait for the M-block's gates, then h <- bf16(h + g bf16(v))
+        bool ready = true;
+        if (lane == 0) ready = wait_published(a.ready + mb, 4 * a.hc, a.abort_g, abort_flag);
+        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+        if (!ready) {
+          if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+          break;
+        }
+        for (int mm = 0; mm < a.hc; ++mm) ctl->sg[q][lane][mm] = live ? __ldcg(a.gates + t * a.hc + mm) : -1.0f;
+        uint32_t(*sv)[20] = ctl->sv[q];
+        const int seg = static_cast<int>(lane & 3);
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          __syncwarp();
+          tc_ld32(taddr + ch * 32, r);
+          // v of this row's 32 columns, rounded to bf16, into the warp's staging rows
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[i * 8 + j * 2]),
+                                                       __uint_as_float(r[i * 8 + j * 2 + 1]));
+              pk[j] = *reinterpret_cast<uint32_t*>(&b);
+            }
+            *reinterpret_cast<uint4*>(&sv[lane][i * 4]) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          __syncwarp();
+          // Transposed pass: 4 lanes cover one row's 64-byte segment, 8 rows per
+          // step.  All loads of up to 4 streams are issued before any update.
+          for (int m0 = 0; m0 < a.hc; m0 += 4) {
+            uint4 hv[4][4];
+            float gg[4][4];
+#pragma unroll
+            for (int k8 = 0; k8 < 4; ++k8) {
+              const int rl = k8 * 8 + static_cast<int>(lane >> 2);
+              const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + rl;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int mm = m0 + j;
+                gg[k8][j] = (mm < a.hc && tr < a.M) ? ctl->sg[q][rl][mm] : -1.0f;
+                if (gg[k8][j] >= 0.0f)
+                  hv[k8][j] = *reinterpret_cast<const uint4*>(a.h + (tr * a.hc + mm) * a.H + c0 + ch * 32 + seg * 8);
+              }
+            }
+#pragma unroll
+            for (int k8 = 0; k8 < 4; ++k8) {
+              const int rl = k8 * 8 + static_cast<int>(lane >> 2);
+              const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + rl;
+              const uint4 vv = *reinterpret_cast<const uint4*>(&sv[rl][seg * 4]);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float g = gg[k8][j];
+                if (g < 0.0f) continue;
+                uint4 x = hv[k8][j];
+                x.x = fma_bf16x2(x.x, g, vv.x);
+                x.y = fma_bf16x2(x.y, g, vv.y);
+                x.z = fma_bf16x2(x.z, g, vv.z);
+                x.w = fma_bf16x2(x.w, g, vv.w);
+                *reinterpret_cast<uint4*>(a.h + (tr * a.hc + m0 + j) * a.H + c0 + ch * 32 + seg * 8) = x;
+              }
+            }
+          }
+        }
       } else {
         uint4* vrow = reinterpret_cast<uint4*>(a.v + t * a.H + c0);
 #pragma unroll 1
@@ -408,6 +561,46 @@ int make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, u
 
 size_t project_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + sizeof(SmemCtl); }
 
+// Shared argument checks and set-up of both projection entry points.
+int prepare(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint16_t* wkv_packed_d, int32_t hidden,
+            int32_t hc, const uint16_t* h_d, const float* q_w_d, const float* k_w_d, float* partials_d,
+            int32_t* status_d, ProjArgs* a, CUtensorMap* tmA, CUtensorMap* tmB, int* grid) {
+  if (n_tokens < 0) return fail(ENGRAM_E_INVALID, "n_tokens < 0");
+  if (K < BK || K % BK != 0 || K > (int64_t(1) << 20))
+    return fail(ENGRAM_E_SHAPE, "K %lld must be a positive multiple of 64", (long long)K);
+  if (hidden < BN || hidden % BN != 0) return fail(ENGRAM_E_SHAPE, "hidden %d must be a multiple of 256", hidden);
+  if (hc < 1 || hc > kMaxHc) return fail(ENGRAM_E_SHAPE, "hc %d not in [1, %d]", hc, kMaxHc);
+  if (n_tokens == 0) return ENGRAM_OK;
+  if (n_tokens > (int64_t(1) << 31) - BM) return fail(ENGRAM_E_SHAPE, "too many tokens");
+  if (!e_d || !wkv_packed_d || !h_d || !q_w_d || !k_w_d || !partials_d)
+    return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (!aligned(e_d, 16) || !aligned(wkv_packed_d, 16) || !aligned(h_d, 16) || !aligned(partials_d, 16))
+    return fail(ENGRAM_E_ALIGN, "e, wkv, h and partials must be 16-byte aligned");
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  const int64_t N = static_cast<int64_t>(hc + 1) * hidden;
+  if ((rc = make_tmap(tmA, e_d, static_cast<uint64_t>(n_tokens), static_cast<uint64_t>(K), BM))) return rc;
+  if ((rc = make_tmap(tmB, wkv_packed_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN))) return rc;
+  *a = ProjArgs{};
+  a->M = n_tokens;
+  a->K = static_cast<int32_t>(K);
+  a->H = hidden;
+  a->hc = hc;
+  a->mt = static_cast<int32_t>((n_tokens + BM - 1) / BM);
+  a->nt = static_cast<int32_t>(N / BN);
+  const int64_t tiles = static_cast<int64_t>(a->mt) * a->nt;
+  if (tiles > INT32_MAX) return fail(ENGRAM_E_SHAPE, "too many tiles");
+  a->num_tiles = static_cast<int32_t>(tiles);
+  a->h = const_cast<uint16_t*>(h_d);
+  a->q_w = q_w_d;
+  a->k_w = k_w_d;
+  a->partials = reinterpret_cast<float4*>(partials_d);
+  a->status = status_d;
+  *grid = static_cast<int>(a->num_tiles < sms ? a->num_tiles : sms);
+  return ENGRAM_OK;
+}
+
 }  // namespace
 }  // namespace engram
 
@@ -436,45 +629,93 @@ extern "C" int engram_project(const uint16_t* e_d, int64_t n_tokens, int64_t K,
                               const uint16_t* wkv_packed_d, int32_t hidden, int32_t hc,
                               const uint16_t* h_d, const float* q_w_d, const float* k_w_d,
                               float* partials_d, uint16_t* v_d, int32_t* status_d, void* stream) {
-  if (n_tokens < 0) return fail(ENGRAM_E_INVALID, "n_tokens < 0");
-  if (K < BK || K % BK != 0 || K > (int64_t(1) << 20)) return fail(ENGRAM_E_SHAPE, "K %lld must be a positive multiple of 64", (long long)K);
-  if (hidden < BN || hidden % BN != 0) return fail(ENGRAM_E_SHAPE, "hidden %d must be a multiple of 256", hidden);
-  if (hc < 1 || hc > kMaxHc) return fail(ENGRAM_E_SHAPE, "hc %d not in [1, %d]", hc, kMaxHc);
-  if (n_tokens == 0) return ENGRAM_OK;
-  if (n_tokens > (int64_t(1) << 31) - BM) return fail(ENGRAM_E_SHAPE, "too many tokens");
-  if (!e_d || !wkv_packed_d || !h_d || !q_w_d || !k_w_d || !partials_d || !v_d)
-    return fail(ENGRAM_E_INVALID, "null device pointer");
-  if (!aligned(e_d, 16) || !aligned(wkv_packed_d, 16) || !aligned(h_d, 16) || !aligned(partials_d, 16) ||
-      !aligned(v_d, 16))
-    return fail(ENGRAM_E_ALIGN, "e, wkv, h, partials and v must be 16-byte aligned");
-  int sms = 0;
-  int rc = check_device(&sms);
-  if (rc) return rc;
-  const int64_t N = static_cast<int64_t>(hc + 1) * hidden;
-  CUtensorMap tmA, tmB;
-  if ((rc = make_tmap(&tmA, e_d, static_cast<uint64_t>(n_tokens), static_cast<uint64_t>(K), BM))) return rc;
-  if ((rc = make_tmap(&tmB, wkv_packed_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN))) return rc;
+  if (!v_d && n_tokens > 0) return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (v_d && !aligned(v_d, 16)) return fail(ENGRAM_E_ALIGN, "v must be 16-byte aligned");
   ProjArgs a;
-  a.M = n_tokens;
-  a.K = static_cast<int32_t>(K);
-  a.H = hidden;
-  a.hc = hc;
-  a.mt = static_cast<int32_t>((n_tokens + BM - 1) / BM);
-  a.nt = static_cast<int32_t>(N / BN);
-  const int64_t tiles = static_cast<int64_t>(a.mt) * a.nt;
-  if (tiles > INT32_MAX) return fail(ENGRAM_E_SHAPE, "too many tiles");
-  a.num_tiles = static_cast<int32_t>(tiles);
-  a.h = h_d;
-  a.q_w = q_w_d;
-  a.k_w = k_w_d;
-  a.partials = reinterpret_cast<float4*>(partials_d);
+  CUtensorMap tmA, tmB;
+  int grid = 0;
+  int rc = prepare(e_d, n_tokens, K, wkv_packed_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d, status_d, &a, &tmA,
+                   &tmB, &grid);
+  if (rc || n_tokens == 0) return rc;
   a.v = v_d;
-  a.status = status_d;
   const size_t smem = project_smem_bytes();
-  cudaError_t err = cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t err = cudaFuncSetAttribute(project_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(project): %s", cudaGetErrorString(err));
-  const int grid = static_cast<int>(a.num_tiles < sms ? a.num_tiles : sms);
-  project_kernel<<<grid, kThreads, smem, as_stream(stream)>>>(tmA, tmB, a);
+  project_kernel<false><<<grid, kThreads, smem, as_stream(stream)>>>(tmA, tmB, a);
   return check_launch("project_kernel");
+}
+
+namespace {
+// Fused-mode workspace: [partials | counters: cnt[mt][hc][4], ready[mt], abort | gates[mt*128][hc]],
+// each part starting on a 256-byte boundary.
+struct FusedWs {
+  size_t partials, counters_off, counter_words, gates_off, total;
+};
+FusedWs fused_ws(int64_t n_tokens, int32_t hidden, int32_t hc) {
+  FusedWs w;
+  const size_t mt = static_cast<size_t>((n_tokens + BM - 1) / BM);
+  w.partials = engram_project_partials_bytes(n_tokens, hidden, hc);
+  w.counters_off = (w.partials + 255) / 256 * 256;
+  w.counter_words = mt * hc * 4 + mt + 1;
+  w.gates_off = w.counters_off + (w.counter_words * 4 + 255) / 256 * 256;
+  w.total = w.gates_off + mt * BM * hc * sizeof(float);
+  return w;
+}
+}  // namespace
+
+extern "C" size_t engram_project_gate_workspace_bytes(int64_t n_tokens, int32_t hidden, int32_t hc) {
+  if (n_tokens < 0 || hidden < 256 || hc < 1) return 0;
+  return fused_ws(n_tokens, hidden, hc).total;
+}
+
+extern "C" int engram_project_gate(const uint16_t* e_d, int64_t n_tokens, int64_t K,
+                                   const uint16_t* wkv_packed_d, int32_t hidden, int32_t hc, uint16_t* h_d,
+                                   const float* q_w_d, const float* k_w_d, const uint8_t* mask_d, float eps,
+                                   float clamp, float score_scale, float* gate_out_d, void* workspace_d,
+                                   size_t workspace_bytes, int32_t* status_d, void* stream) {
+  if (n_tokens > 0 && workspace_d == nullptr) return fail(ENGRAM_E_INVALID, "null workspace");
+  if (workspace_d && !aligned(workspace_d, 256)) return fail(ENGRAM_E_ALIGN, "workspace must be 256-byte aligned");
+  const size_t need = engram_project_gate_workspace_bytes(n_tokens, hidden, hc);
+  if (n_tokens > 0 && workspace_bytes < need)
+    return fail(ENGRAM_E_SHAPE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  ProjArgs a;
+  CUtensorMap tmA, tmB;
+  int grid = 0;
+  float* partials_d = static_cast<float*>(workspace_d);
+  int rc = prepare(e_d, n_tokens, K, wkv_packed_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d, status_d, &a, &tmA,
+                   &tmB, &grid);
+  if (rc || n_tokens == 0) return rc;
+  const FusedWs ws = fused_ws(n_tokens, hidden, hc);
+  unsigned char* base = static_cast<unsigned char*>(workspace_d);
+  a.cnt = reinterpret_cast<int32_t*>(base + ws.counters_off);
+  a.ready = a.cnt + static_cast<size_t>(a.mt) * hc * 4;
+  a.abort_g = a.ready + a.mt;
+  a.gates = reinterpret_cast<float*>(base + ws.gates_off);
+  a.mask = mask_d;
+  a.gate_out = gate_out_d;
+  a.eps = eps;
+  a.clamp = clamp;
+  a.score_scale = score_scale;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t err = cudaMemsetAsync(a.cnt, 0, ws.counter_words * sizeof(int32_t), st);
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaMemsetAsync(counters): %s", cudaGetErrorString(err));
+  const size_t smem = project_smem_bytes();
+  err = cudaFuncSetAttribute(project_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(project): %s", cudaGetErrorString(err));
+  // Cooperative: every CTA is resident at once, which the in-kernel wait of
+  // value tiles on key tiles relies on.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, project_kernel<true>, tmA, tmB, a);
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "project_kernel (fused) launch: %s", cudaGetErrorString(err));
+  return check_launch("project_kernel (fused)");
 }

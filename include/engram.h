@@ -272,6 +272,37 @@ int engram_gate_add(const float* partials_d, const uint16_t* v_d, uint16_t* h_d,
                     float clamp, float score_scale, float* gate_out_d, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Projection with the gate and residual fused (stage 5a-5c in one kernel)    */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of the workspace of engram_project_gate: the partial sums
+ * (engram_project_partials_bytes), then int32 counters
+ * (ceil(n_tokens/128) * (4*hc + 1) + 1 words), then fp32 gates
+ * (ceil(n_tokens/128) * 128 * hc), each part on a 256-byte boundary. */
+size_t engram_project_gate_workspace_bytes(int64_t n_tokens, int32_t hidden, int32_t hc);
+
+/* The same result as engram_project followed by engram_gate_add, computed in
+ * one cooperative tensor-core kernel ([P-V41] §门控; [P-DS4] §消费).  Key
+ * tiles publish their partial sums; the epilogue warp that publishes the last
+ * tile of a (128-row block, stream, 32-row quarter) sums that group's partials
+ * in tile order and writes its gates; each value tile waits (bounded) for its
+ * block's gates and applies h <- bf16(h + g * bf16(v)) directly, so v is never
+ * stored.  The gate kernel of the unfused path sums with a shuffle tree, so
+ * gates agree with engram_gate_add to fp32 rounding, not bit for bit; the
+ * fused result itself is deterministic.
+ *   e_d, wkv_packed_d, h_d, q_w_d, k_w_d   as engram_project (h_d updated in place)
+ *   mask_d, eps, clamp, score_scale,
+ *   gate_out_d                            as engram_gate_add
+ *   workspace_d  device buffer of engram_project_gate_workspace_bytes(...)
+ *                bytes, 256-byte aligned, owned by the caller; its contents
+ *                on entry do not matter (the counters are zeroed on the stream)
+ * A wait that runs out sets ENGRAM_ST_TIMEOUT in status_d. */
+int engram_project_gate(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint16_t* wkv_packed_d,
+                        int32_t hidden, int32_t hc, uint16_t* h_d, const float* q_w_d, const float* k_w_d,
+                        const uint8_t* mask_d, float eps, float clamp, float score_scale, float* gate_out_d,
+                        void* workspace_d, size_t workspace_bytes, int32_t* status_d, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Projection + gate without device allocation                                */
 /* ------------------------------------------------------------------------ */
 

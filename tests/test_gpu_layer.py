@@ -21,13 +21,13 @@ def _gpu():
     require_gpu()
 
 
-def _make_layer(name):
+def _make_layer(name, fused=True):
     w, tm, lay_o, lay = setup(name)
     lw = layer_weights(w)
     total = lay_o.layers[0].total_rows
     table = device_table(total, w.seed)
     layer = eg.EngramLayer(lay, 0, table, i32(tm), eg.engram_pack_wkv(bf16(lw.wkv_bits)), f32(lw.q_w),
-                           f32(lw.k_w))
+                           f32(lw.k_w), fused=fused)
     return w, tm, lay_o, lay, lw, layer
 
 
@@ -45,8 +45,8 @@ def _oracle_tokens(w, lay_o, lw, W, rows_o, mask_o, h_bits, idx):
     return e, g, v, hf, out, v_err
 
 
-def _check_layer(name, idx_fn):
-    w, tm, lay_o, lay, lw, layer = _make_layer(name)
+def _check_layer(name, idx_fn, fused=True):
+    w, tm, lay_o, lay, lw, layer = _make_layer(name, fused)
     b = prefill_batch(w)
     T = len(b.raw_ids)
     h_bits = residual_bits(T, w.hc, w.hidden, w.seed)
@@ -73,8 +73,9 @@ def _check_layer(name, idx_fn):
     assert ok, (worst, strict)
 
 
-def test_layer_tiny_all_tokens():
-    _check_layer("tiny", lambda T, m, cu: np.arange(T))
+@pytest.mark.parametrize("fused", [True, False])
+def test_layer_tiny_all_tokens(fused):
+    _check_layer("tiny", lambda T, m, cu: np.arange(T), fused)
 
 
 def test_layer_prefill_sampled():

@@ -117,3 +117,58 @@ def test_project_large_m_tiles():
     assert np.abs(gate.cpu().numpy()[idx] - g).max() <= GATE_ATOL
     ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
     assert ok, (worst, strict)
+
+
+@pytest.mark.parametrize("T,H,hc", [(128, 256, 4), (300, 256, 4), (1, 256, 4), (129, 512, 2), (257, 256, 1),
+                                    (2100, 256, 4)])
+def test_project_gate_fused(T, H, hc):
+    """Fused projection + gate + residual against the oracle and against the unfused kernels."""
+    e, w, h, qw, kw = _inputs(T, H, hc, seed=1000 + T)
+    mask = np.zeros(T, dtype=bool)
+    mask[5::11] = True
+    k, v, hf, g, out, k_err, v_err = _oracle(e, w, h, qw, kw, mask, T, H, hc)
+    wp = eg.engram_pack_wkv(bf16(w))
+    e_d, qw_d, kw_d, m_d = bf16(e), f32(qw), f32(kw), u8(mask)
+    h_f = bf16(h)
+    g_f = torch.empty((T, hc), dtype=torch.float32, device=DEV)
+    st = status()
+    eg.engram_project_gate(e_d, wp, h_f, qw_d, kw_d, m_d, gate_out=g_f, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    gf = g_f.cpu().numpy()
+    assert np.abs(gf - g).max() <= GATE_ATOL
+    assert (gf[mask] == 0).all()
+    hb = bits(h_f)
+    assert (hb[mask] == h[mask]).all()
+    ok, worst, strict = residual_close(bf16_bits_to_f64(hb), out, hf, g, v, v_err)
+    assert ok, (worst, strict)
+    # unfused kernels on the same inputs: gates agree to fp32 summation order
+    h_u = bf16(h)
+    g_u = torch.empty((T, hc), dtype=torch.float32, device=DEV)
+    partials, v_d = eg.engram_project(e_d, wp, h_u, qw_d, kw_d)
+    eg.engram_gate_add(partials, v_d, h_u, m_d, gate_out=g_u)
+    assert np.abs(g_u.cpu().numpy() - gf).max() <= 1e-5
+    hu = bf16_bits_to_f64(bits(h_u))
+    diff = np.abs(hu - bf16_bits_to_f64(hb))
+    assert (diff <= 2.0 ** -7 * np.maximum(np.abs(hu), 1e-30) + 1e-30).all()
+
+
+def test_project_gate_fused_many_groups():
+    """4133 tokens (33 M-blocks, three raster groups, ragged tail) at hidden 5120: sampled rows."""
+    T, H, hc = 4133, 5120, 4
+    e, w, h, qw, kw = _inputs(T, H, hc, seed=77)
+    mask = np.zeros(T, dtype=bool)
+    mask[[3, 2048, 4132]] = True
+    h_d = bf16(h)
+    gate = torch.empty((T, hc), dtype=torch.float32, device=DEV)
+    st = status()
+    eg.engram_project_gate(bf16(e), eg.engram_pack_wkv(bf16(w)), h_d, f32(qw), f32(kw), u8(mask), gate_out=gate,
+                           status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    idx = np.array([0, 3, 127, 128, 2047, 2048, 2049, 4095, 4096, 4131, 4132])
+    k, v, hf, g, out, k_err, v_err = _oracle(e[idx], w, h[idx], qw, kw, mask[idx], len(idx), H, hc)
+    assert np.abs(gate.cpu().numpy()[idx] - g).max() <= GATE_ATOL
+    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
+    assert ok, (worst, strict)
+    assert (bits(h_d)[mask] == h[mask]).all()
