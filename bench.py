@@ -45,6 +45,7 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="prefill")
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--micro-steps", type=int, default=30, help="steps of the hash+gather microbench phase")
     p.add_argument("--cpu-sample", type=int, default=8192, help="tokens of the oracle CPU baseline sample")
     p.add_argument("--ref-sample", type=int, default=128, help="tokens per reference-arm step")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -139,6 +140,30 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------------------- ranks
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each replica draws its own batch (weak scaling, no shared data)."""
+    return base_seed + rank
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    """Largest value over ranks (the slowest rank's time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(tokens_per_step: int, steps: int, world: int, max_total_s: float) -> float:
+    """Whole-job tokens/s: every rank processed tokens_per_step per step."""
+    return world * tokens_per_step * steps / max_total_s
+
+
 # ------------------------------------------------------------------------- inputs
 
 
@@ -178,7 +203,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = WORKLOADS[args.workload]
-    inp = make_inputs(w, w.seed + rank, dev)
+    inp = make_inputs(w, rank_seed(w.seed, rank), dev)
     layer, b = inp["layer"], inp["batch"]
     T = len(b.raw_ids)
     raw = torch.from_numpy(b.raw_ids).to(dev)
@@ -240,11 +265,7 @@ def run_ours(args, rank, world, local):
     step_ms = [ms(k, 0, 3) for k in range(args.steps)]
     stage = {name: [ms(k, i, i + 1) for k in range(args.steps)]
              for i, name in enumerate(["hash", "gather", "project_gate"])}
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = reduce_max(sum(step_ms) / 1e3, world, dev)
 
     # ---- end to end: host buffers through the public layer API
     e2e = None
@@ -274,19 +295,22 @@ def run_ours(args, rank, world, local):
             e1.record(stream)
             e1.synchronize()
             tot += e0.elapsed_time(e1) / 1e3
-        if world > 1:
-            t = torch.tensor([tot], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            tot = float(t.item())
+        tot = reduce_max(tot, world, dev)
         h2d = raw_h.numel() * 4 + cu_h.numel() * 8 + h_host.numel() * 2
-        e2e = {"value": world * T * args.e2e_steps / tot, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        e2e = {"value": aggregate_value(T, args.e2e_steps, world, tot), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(out_host.numel() * 2), "steps": args.e2e_steps,
                "api": "EngramLayer.prefill with pinned host inputs/outputs"}
+
+    micro = microbench(args, w, inp, layer, flush, dev) if args.micro_steps > 0 else None
 
     if rank != 0:
         return None
 
     peaks, peak_src = load_peaks()
+    if micro is not None:
+        micro["frac"] = micro["gather_gbs"] / peaks["hbm_gbs"]
+        micro["peak_gbs"] = peaks["hbm_gbs"]
     sustained = total_s >= 2.0
     tf_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     flops = 2.0 * T * 6144 * (w.hc + 1) * w.hidden
@@ -306,7 +330,7 @@ def run_ours(args, rank, world, local):
               "peak_source": f"{peak_src} hbm_gbs"}
     out = {
         "metric": METRIC,
-        "value": world * T * args.steps / total_s,
+        "value": aggregate_value(T, args.steps, world, total_s),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -322,6 +346,7 @@ def run_ours(args, rank, world, local):
         "stages_ms": {k: statistics.mean(v) for k, v in stage.items()},
         "roofline": roof,
         "roofline_gather": roof_g,
+        "microbench_hash_gather": micro,
         "gpu_launches": args.steps * 4,
         "clocks": clocks,
         "e2e": e2e,
@@ -331,6 +356,50 @@ def run_ours(args, rank, world, local):
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_sample)
     return out
+
+
+def microbench(args, w, inp, layer, flush, dev):
+    """Hash + gather only on the 65,536-token microbench workload (same table)."""
+    import torch
+    import hashed_gram_conditional_gb300 as eg
+    from workloads import WORKLOADS, prefill_batch
+
+    wm = WORKLOADS["microbench"]
+    if (wm.base_rows, wm.v, wm.v_raw, wm.layer_id, wm.seed) != (w.base_rows, w.v, w.v_raw, w.layer_id, w.seed):
+        return None
+    bm = prefill_batch(wm)
+    T = len(bm.raw_ids)
+    raw = torch.from_numpy(bm.raw_ids).to(dev)
+    cu = torch.from_numpy(bm.cu_seqlens).to(dev)
+    rows = torch.empty((T, 24), dtype=torch.int32, device=dev)
+    mask = torch.empty(T, dtype=torch.uint8, device=dev)
+    e = torch.empty((T, 6144), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def run(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        eg.engram_hash(layer.layout, 0, raw, cu, layer.token_map, None, rows, mask)
+        if ev is not None:
+            ev[1].record(stream)
+        eg.engram_gather_dequant(layer.table, layer.total_rows, rows, e)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(3):
+        flush.zero_()
+        run()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.micro_steps)]
+    for k in range(args.micro_steps):
+        flush.zero_()
+        run(evs[k])
+    torch.cuda.synchronize()
+    step = statistics.mean(ev[0].elapsed_time(ev[2]) for ev in evs) / 1e3
+    gat = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs) / 1e3
+    gbytes = GATHER_BYTES_PER_TOKEN * T
+    return {"workload": f"microbench: 1 x {T} Zipf(1.1) tokens, same 12.67 GB table", "steps": args.micro_steps,
+            "hash_gather_tokens_per_s": T / step, "hash_ms": (step - gat) * 1e3, "gather_ms": gat * 1e3,
+            "gather_gbs": gbytes / gat / 1e9, "algorithmic_bytes": gbytes}
 
 
 # ------------------------------------------------------------------------- oracle timing
