@@ -40,6 +40,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstdlib>
+
 #include "engram_internal.h"
 
 namespace engram {
@@ -55,6 +57,12 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int kThreads = 192;
 constexpr int kGroupM = 16;  // M-blocks per raster group: e group + wkv wave fit one die's L2 half
+// CTA pair (cta_group::2): a 256 x 256 tile per pair; each CTA stages its own
+// 128 rows of e and its half (128 rows) of the 256 wkv rows per k-block.
+constexpr int STAGES2 = 6;
+constexpr int B2_BYTES = (BN / 2) * BK * 2;
+constexpr int STAGE2_BYTES = A_BYTES + B2_BYTES;
+constexpr int kGroupM2 = 8;  // pair M-blocks (256 rows) per raster group
 constexpr int kMaxHc = 8;
 
 struct ProjArgs {
@@ -62,9 +70,10 @@ struct ProjArgs {
   int32_t K;
   int32_t H;
   int32_t hc;
-  int32_t mt;
+  int32_t mt;           // 128-row blocks
+  int32_t mt2;          // 256-row blocks (CTA-pair kernel)
   int32_t nt;
-  int32_t num_tiles;
+  int32_t num_tiles;    // tiles of the kernel that runs (128x256 or 256x256)
   uint16_t* h;           // read (key tiles); updated in place by value tiles in fused mode
   const float* q_w;
   const float* k_w;
@@ -84,8 +93,8 @@ struct ProjArgs {
 };
 
 struct __align__(8) SmemCtl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[STAGES2];
+  uint64_t empty[STAGES2];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -114,6 +123,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 // both K-major, N = BN, M = BM.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
                             (static_cast<uint32_t>(BM >> 4) << 24);
+// Same for the CTA pair: M = 256 (128 rows per CTA), N = 256.
+constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                             (static_cast<uint32_t>((2 * BM) >> 4) << 24);
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -150,11 +162,63 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tile_coords(int tile, int mt, int nt, int& mb, int& nb) {
-  const int per_group = kGroupM * nt;
+
+// ---- CTA-pair primitives
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 2-D TMA load into this CTA's shared memory whose completion is counted on
+// the mbarrier at cluster address `bar` (the leader CTA's barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc2), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the barrier at this shared offset in both CTAs of the pair
+// when every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(static_cast<unsigned short>(3))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ void tile_coords(int tile, int mt, int nt, int group, int& mb, int& nb) {
+  const int per_group = group * nt;
   const int g = tile / per_group;
-  const int first_m = g * kGroupM;
-  const int gm = min(kGroupM, mt - first_m);
+  const int first_m = g * group;
+  const int gm = min(group, mt - first_m);
   const int local = tile - g * per_group;
   mb = first_m + local % gm;
   nb = local / gm;
@@ -188,6 +252,215 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t h, float g, uint32_t v) 
   const float hi = __uint_as_float(h & 0xffff0000u) + g * __uint_as_float(v & 0xffff0000u);
   __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// Tile geometry shared by the epilogue helpers.
+struct EpiTile {
+  int m;         // key stream of a key tile
+  int c0;        // first column of the tile within its key stream / within v
+  bool key_tile;
+};
+
+__device__ __forceinline__ EpiTile epi_tile(const ProjArgs& a, int nb) {
+  EpiTile e;
+  const int n0 = nb * BN;
+  const int key_cols = a.hc * a.H;
+  e.key_tile = n0 < key_cols;
+  e.m = e.key_tile ? n0 / a.H : 0;
+  e.c0 = e.key_tile ? n0 - e.m * a.H : n0 - key_cols;
+  return e;
+}
+
+// Before the accumulator is ready: stage q_w * k_w of a key tile's 256
+// columns in the warp's own copy (no cross-warp barrier).
+__device__ __forceinline__ void epilogue_stage(const ProjArgs& a, SmemCtl* ctl, int q, uint32_t lane,
+                                               const EpiTile& et) {
+  if (!et.key_tile) return;
+  float* qk = ctl->qk[q];
+  __syncwarp();
+  for (int c = static_cast<int>(lane); c < BN; c += 32) {
+    const int64_t idx = static_cast<int64_t>(et.c0 + c) * a.hc + et.m;
+    qk[c] = __ldg(a.q_w + idx) * __ldg(a.k_w + idx);
+  }
+  __syncwarp();
+}
+
+// Epilogue of one 128 x 256 accumulator (TMEM address taddr of this warp's
+// 32 lanes): output rows mb*128 + q*32 + lane, columns nb*256 .. +255.
+// Returns false when a bounded wait gave up.
+template <bool kFuse>
+__device__ __forceinline__ bool epilogue_tile(const ProjArgs& a, SmemCtl* ctl, int q, uint32_t lane,
+                                              uint32_t taddr, int mb, const EpiTile& et,
+                                              const volatile int* abort_flag) {
+  const int row = q * 32 + static_cast<int>(lane);
+  const int ntile = a.H / BN;
+  const bool key_tile = et.key_tile;
+  const int m = et.m;
+  const int c0 = et.c0;
+  const float* qk = ctl->qk[q];
+  const int64_t t = static_cast<int64_t>(mb) * BM + row;
+  const bool live = t < a.M;
+  if (key_tile) {
+    const uint4* hrow = reinterpret_cast<const uint4*>(a.h + (t * a.hc + m) * a.H + c0);
+    float dot = 0.f, kk = 0.f, hh = 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      uint4 hv[4];
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hv[i] = __ldg(hrow + ch * 4 + i);
+      }
+      uint32_t r[32];
+      __syncwarp();
+      tc_ld32(taddr + ch * 32, r);
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t w4[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int col = ch * 32 + i * 8 + j * 2;
+            const float h0 = bf16f(w4[j] & 0xffffu), h1 = bf16f(w4[j] >> 16);
+            const float k0 = __uint_as_float(r[i * 8 + j * 2]);
+            const float k1 = __uint_as_float(r[i * 8 + j * 2 + 1]);
+            dot += h0 * qk[col] * k0 + h1 * qk[col + 1] * k1;
+            kk += k0 * k0 + k1 * k1;
+            hh += h0 * h0 + h1 * h1;
+          }
+        }
+      }
+    }
+    if (live) a.partials[(t * a.hc + m) * ntile + c0 / BN] = make_float4(dot, kk, hh, 0.f);
+    if (kFuse) {
+      // Publish this warp's 32 partials; the warp that publishes the last
+      // tile of (M-block, stream, row quarter) finishes those 32 gates.
+      __threadfence();
+      __syncwarp();
+      int prev = 0;
+      if (lane == 0) prev = atomicAdd(a.cnt + (static_cast<int64_t>(mb) * a.hc + m) * 4 + q, 1);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == ntile - 1) {
+        __threadfence();  // acquire: every tile's partials of these rows are visible
+        if (live) {
+          const bool masked = a.mask != nullptr && a.mask[t] != 0;
+          float g = 0.0f;
+          if (!masked) {
+            const float4* p = a.partials + (t * a.hc + m) * ntile;
+            float sd = 0.f, sk = 0.f, sh = 0.f;
+            for (int q0 = 0; q0 < ntile; q0 += 8) {
+              float4 x[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[i] = (q0 + i < ntile) ? __ldcg(p + q0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {  // tile order: deterministic
+                sd += x[i].x;
+                sk += x[i].y;
+                sh += x[i].z;
+              }
+            }
+            const float inv_h = 1.0f / static_cast<float>(a.H);
+            const float sc = sd * (1.0f / sqrtf(sh * inv_h + a.eps)) * (1.0f / sqrtf(sk * inv_h + a.eps)) *
+                             a.score_scale;
+            const float z = copysignf(sqrtf(fmaxf(fabsf(sc), a.clamp)), sc);
+            g = 1.0f / (1.0f + expf(-z));
+          }
+          a.gates[t * a.hc + m] = masked ? -1.0f : g;
+          if (a.gate_out != nullptr) a.gate_out[t * a.hc + m] = g;
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(a.ready + mb, 1);
+      }
+    }
+  } else if (kFuse) {
+    // ---- value tile, fused: wait for the M-block's gates, then h <- bf16(h + g bf16(v))
+    bool ready = true;
+    if (lane == 0) ready = wait_published(a.ready + mb, 4 * a.hc, a.abort_g, abort_flag);
+    ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+    if (!ready) {
+      if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+      return false;
+    }
+    for (int mm = 0; mm < a.hc; ++mm) ctl->sg[q][lane][mm] = live ? __ldcg(a.gates + t * a.hc + mm) : -1.0f;
+    uint32_t(*sv)[20] = ctl->sv[q];
+    const int seg = static_cast<int>(lane & 3);
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      uint32_t r[32];
+      __syncwarp();
+      tc_ld32(taddr + ch * 32, r);
+      // v of this row's 32 columns, rounded to bf16, into the warp's staging rows
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[i * 8 + j * 2]),
+                                                   __uint_as_float(r[i * 8 + j * 2 + 1]));
+          pk[j] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        *reinterpret_cast<uint4*>(&sv[lane][i * 4]) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      __syncwarp();
+      // Transposed pass: 4 lanes cover one row's 64-byte segment, 8 rows per
+      // step.  All loads of up to 4 streams are issued before any update.
+      for (int m0 = 0; m0 < a.hc; m0 += 4) {
+        uint4 hv[4][4];
+        float gg[4][4];
+#pragma unroll
+        for (int k8 = 0; k8 < 4; ++k8) {
+          const int rl = k8 * 8 + static_cast<int>(lane >> 2);
+          const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + rl;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int mm = m0 + j;
+            gg[k8][j] = (mm < a.hc && tr < a.M) ? ctl->sg[q][rl][mm] : -1.0f;
+            if (gg[k8][j] >= 0.0f)
+              hv[k8][j] = *reinterpret_cast<const uint4*>(a.h + (tr * a.hc + mm) * a.H + c0 + ch * 32 + seg * 8);
+          }
+        }
+#pragma unroll
+        for (int k8 = 0; k8 < 4; ++k8) {
+          const int rl = k8 * 8 + static_cast<int>(lane >> 2);
+          const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + rl;
+          const uint4 vv = *reinterpret_cast<const uint4*>(&sv[rl][seg * 4]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float g = gg[k8][j];
+            if (g < 0.0f) continue;
+            uint4 x = hv[k8][j];
+            x.x = fma_bf16x2(x.x, g, vv.x);
+            x.y = fma_bf16x2(x.y, g, vv.y);
+            x.z = fma_bf16x2(x.z, g, vv.z);
+            x.w = fma_bf16x2(x.w, g, vv.w);
+            *reinterpret_cast<uint4*>(a.h + (tr * a.hc + m0 + j) * a.H + c0 + ch * 32 + seg * 8) = x;
+          }
+        }
+      }
+    }
+  } else {
+    uint4* vrow = reinterpret_cast<uint4*>(a.v + t * a.H + c0);
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      uint32_t r[32];
+      __syncwarp();
+      tc_ld32(taddr + ch * 32, r);
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[i * 8 + j * 2]),
+                                                     __uint_as_float(r[i * 8 + j * 2 + 1]));
+            pk[j] = *reinterpret_cast<uint32_t*>(&b);
+          }
+          vrow[ch * 4 + i] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+    }
+  }
+  return true;
 }
 
 template <bool kFuse>
@@ -238,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
         int mb, nb;
-        tile_coords(tile, a.mt, a.nt, mb, nb);
+        tile_coords(tile, a.mt, a.nt, kGroupM, mb, nb);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -299,198 +572,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row = q * 32 + static_cast<int>(lane);
-    const int ntile = a.H / BN;
-    const int key_cols = a.hc * a.H;
     int local = 0;
     for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++local) {
       int mb, nb;
-      tile_coords(tile, a.mt, a.nt, mb, nb);
+      tile_coords(tile, a.mt, a.nt, kGroupM, mb, nb);
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
-      const int n0 = nb * BN;
-      const bool key_tile = n0 < key_cols;
-      const int m = key_tile ? n0 / a.H : 0;
-      const int c0 = key_tile ? n0 - m * a.H : n0 - key_cols;
-      float* qk = ctl->qk[q];
-      if (key_tile) {
-        // q_w * k_w of the tile's 256 columns, staged per warp (no cross-warp barrier)
-        __syncwarp();
-        for (int c = static_cast<int>(lane); c < BN; c += 32) {
-          const int64_t idx = static_cast<int64_t>(c0 + c) * a.hc + m;
-          qk[c] = __ldg(a.q_w + idx) * __ldg(a.k_w + idx);
-        }
-        __syncwarp();
-      }
-      const bool ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag);
-      if (!ok) {
+      const EpiTile et = epi_tile(a, nb);
+      epilogue_stage(a, ctl, q, lane, et);
+      if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag)) {
         if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
         break;
       }
       tc_fence_after();
-      const int64_t t = static_cast<int64_t>(mb) * BM + row;
-      const bool live = t < a.M;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      if (key_tile) {
-        const uint4* hrow = reinterpret_cast<const uint4*>(a.h + (t * a.hc + m) * a.H + c0);
-        float dot = 0.f, kk = 0.f, hh = 0.f;
-#pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
-          uint4 hv[4];
-          if (live) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) hv[i] = __ldg(hrow + ch * 4 + i);
-          }
-          uint32_t r[32];
-          __syncwarp();
-          tc_ld32(taddr + ch * 32, r);
-          if (live) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t w4[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int col = ch * 32 + i * 8 + j * 2;
-                const float h0 = bf16f(w4[j] & 0xffffu), h1 = bf16f(w4[j] >> 16);
-                const float k0 = __uint_as_float(r[i * 8 + j * 2]);
-                const float k1 = __uint_as_float(r[i * 8 + j * 2 + 1]);
-                dot += h0 * qk[col] * k0 + h1 * qk[col + 1] * k1;
-                kk += k0 * k0 + k1 * k1;
-                hh += h0 * h0 + h1 * h1;
-              }
-            }
-          }
-        }
-        if (live) a.partials[(t * a.hc + m) * ntile + c0 / BN] = make_float4(dot, kk, hh, 0.f);
-        if (kFuse) {
-          // Publish this warp's 32 partials; the warp that publishes the last
-          // tile of (M-block, stream, row quarter) finishes those 32 gates.
-          __threadfence();
-          __syncwarp();
-          int prev = 0;
-          if (lane == 0) prev = atomicAdd(a.cnt + (static_cast<int64_t>(mb) * a.hc + m) * 4 + q, 1);
-          prev = __shfl_sync(0xffffffffu, prev, 0);
-          if (prev == ntile - 1) {
-            __threadfence();  // acquire: every tile's partials of these rows are visible
-            if (live) {
-              const bool masked = a.mask != nullptr && a.mask[t] != 0;
-              float g = 0.0f;
-              if (!masked) {
-                const float4* p = a.partials + (t * a.hc + m) * ntile;
-                float sd = 0.f, sk = 0.f, sh = 0.f;
-                for (int q0 = 0; q0 < ntile; q0 += 8) {
-                  float4 x[8];
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) x[i] = (q0 + i < ntile) ? __ldcg(p + q0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {  // tile order: deterministic
-                    sd += x[i].x;
-                    sk += x[i].y;
-                    sh += x[i].z;
-                  }
-                }
-                const float inv_h = 1.0f / static_cast<float>(a.H);
-                const float sc = sd * (1.0f / sqrtf(sh * inv_h + a.eps)) * (1.0f / sqrtf(sk * inv_h + a.eps)) *
-                                 a.score_scale;
-                const float z = copysignf(sqrtf(fmaxf(fabsf(sc), a.clamp)), sc);
-                g = 1.0f / (1.0f + expf(-z));
-              }
-              a.gates[t * a.hc + m] = masked ? -1.0f : g;
-              if (a.gate_out != nullptr) a.gate_out[t * a.hc + m] = g;
-            }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) atomicAdd(a.ready + mb, 1);
-          }
-        }
-      } else if (kFuse) {
-        // ---- value tile, fused: wait for the M-block's gates, then h <- bf16(h + g bf16(v))
-        bool ready = true;
-        if (lane == 0) ready = wait_published(a.ready + mb, 4 * a.hc, a.abort_g, abort_flag);
-        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-        if (!ready) {
-          if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
-          break;
-        }
-        for (int mm = 0; mm < a.hc; ++mm) ctl->sg[q][lane][mm] = live ? __ldcg(a.gates + t * a.hc + mm) : -1.0f;
-        uint32_t(*sv)[20] = ctl->sv[q];
-        const int seg = static_cast<int>(lane & 3);
-#pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
-          uint32_t r[32];
-          __syncwarp();
-          tc_ld32(taddr + ch * 32, r);
-          // v of this row's 32 columns, rounded to bf16, into the warp's staging rows
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[i * 8 + j * 2]),
-                                                       __uint_as_float(r[i * 8 + j * 2 + 1]));
-              pk[j] = *reinterpret_cast<uint32_t*>(&b);
-            }
-            *reinterpret_cast<uint4*>(&sv[lane][i * 4]) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
-          __syncwarp();
-          // Transposed pass: 4 lanes cover one row's 64-byte segment, 8 rows per
-          // step.  All loads of up to 4 streams are issued before any update.
-          for (int m0 = 0; m0 < a.hc; m0 += 4) {
-            uint4 hv[4][4];
-            float gg[4][4];
-#pragma unroll
-            for (int k8 = 0; k8 < 4; ++k8) {
-              const int rl = k8 * 8 + static_cast<int>(lane >> 2);
-              const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + rl;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int mm = m0 + j;
-                gg[k8][j] = (mm < a.hc && tr < a.M) ? ctl->sg[q][rl][mm] : -1.0f;
-                if (gg[k8][j] >= 0.0f)
-                  hv[k8][j] = *reinterpret_cast<const uint4*>(a.h + (tr * a.hc + mm) * a.H + c0 + ch * 32 + seg * 8);
-              }
-            }
-#pragma unroll
-            for (int k8 = 0; k8 < 4; ++k8) {
-              const int rl = k8 * 8 + static_cast<int>(lane >> 2);
-              const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + rl;
-              const uint4 vv = *reinterpret_cast<const uint4*>(&sv[rl][seg * 4]);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float g = gg[k8][j];
-                if (g < 0.0f) continue;
-                uint4 x = hv[k8][j];
-                x.x = fma_bf16x2(x.x, g, vv.x);
-                x.y = fma_bf16x2(x.y, g, vv.y);
-                x.z = fma_bf16x2(x.z, g, vv.z);
-                x.w = fma_bf16x2(x.w, g, vv.w);
-                *reinterpret_cast<uint4*>(a.h + (tr * a.hc + m0 + j) * a.H + c0 + ch * 32 + seg * 8) = x;
-              }
-            }
-          }
-        }
-      } else {
-        uint4* vrow = reinterpret_cast<uint4*>(a.v + t * a.H + c0);
-#pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
-          uint32_t r[32];
-          __syncwarp();
-          tc_ld32(taddr + ch * 32, r);
-          if (live) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[i * 8 + j * 2]),
-                                                         __uint_as_float(r[i * 8 + j * 2 + 1]));
-                pk[j] = *reinterpret_cast<uint32_t*>(&b);
-              }
-              vrow[ch * 4 + i] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-          }
-        }
-      }
+      if (!epilogue_tile<kFuse>(a, ctl, q, lane, taddr, mb, et, abort_flag)) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
@@ -503,6 +599,170 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+
+// CTA-pair variant: clusters of 2 CTAs; the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256, N = 256) reading e rows from both CTAs
+// and each CTA's half of the 256 wkv rows, so each SM streams half the wkv
+// bytes of the single-CTA kernel through shared memory and can keep 6 stages.
+// Both CTAs' loads complete on the even CTA's "full" barrier; MMA completion
+// is multicast to both CTAs' "empty" / "tfull" barriers; both CTAs' epilogue
+// warps release an accumulator on the even CTA's "tempty" barrier (count 8).
+template <bool kFuse>
+__global__ void __launch_bounds__(kThreads, 1)
+    project2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    ProjArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + STAGES2 * A_BYTES;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + STAGES2 * STAGE2_BYTES);
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t rank = cluster_rank();
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int nkb = a.K / BK;
+  volatile int* abort_flag = &ctl->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctl->tfull[i]), 1);
+      mbar_init(smem_u32(&ctl->tempty[i]), 8);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  // Both CTAs' barriers are initialised and their TMEM allocated before any
+  // cross-CTA signal.
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs)
+      int it = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < a.num_tiles; tile += npairs) {
+        int mb2, nb;
+        tile_coords(tile, a.mt2, a.nt, kGroupM2, mb2, nb);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES2;
+          const uint32_t ph = (it / STAGES2) & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag)) {
+            if (!*abort_flag) raise_abort(ctl, a);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * STAGE2_BYTES);
+          const uint32_t leader_fb = map_to_cta(fb, 0);
+          tma_load_2d_pair(smem_u32(smA + s * A_BYTES), &tmA, kb * BK, mb2 * (2 * BM) + static_cast<int>(rank) * BM,
+                           leader_fb);
+          tma_load_2d_pair(smem_u32(smB + s * B2_BYTES), &tmB, kb * BK, nb * BN + static_cast<int>(rank) * (BN / 2),
+                           leader_fb);
+        }
+      }
+      if (rank == 0) {
+        // the last stages issued (both CTAs' halves) have landed before exit
+        for (int j = (it > STAGES2 ? it - STAGES2 : 0); j < it; ++j)
+          mbar_wait_bounded(smem_u32(&ctl->full[j % STAGES2]), (j / STAGES2) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA only)
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < a.num_tiles; tile += npairs, ++local) {
+        const int acc = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1, abort_flag)) {
+          if (!*abort_flag) raise_abort(ctl, a);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES2;
+          const uint32_t ph = (it / STAGES2) & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag)) {
+            if (!*abort_flag) raise_abort(ctl, a);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smA + s * A_BYTES);
+          const uint32_t b0 = smem_u32(smB + s * B2_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            tc_mma_pair(d, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair(smem_u32(&ctl->empty[s]));
+        }
+        if (ok) tc_commit_pair(smem_u32(&ctl->tfull[acc]));
+      }
+      // every MMA issued so far completes before TMEM is released
+      tc_commit_pair(smem_u32(&ctl->drain));
+      mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5 of both CTAs; each its own 128 rows)
+    const int q = warp & 3;
+    const uint32_t leader_tempty0 = map_to_cta(smem_u32(&ctl->tempty[0]), 0);
+    const uint32_t leader_tempty1 = map_to_cta(smem_u32(&ctl->tempty[1]), 0);
+    int local = 0;
+    for (int tile = pair; tile < a.num_tiles; tile += npairs, ++local) {
+      int mb2, nb;
+      tile_coords(tile, a.mt2, a.nt, kGroupM2, mb2, nb);
+      const int mb = mb2 * 2 + static_cast<int>(rank);
+      const int acc = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      const EpiTile et = epi_tile(a, nb);
+      epilogue_stage(a, ctl, q, lane, et);
+      if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag)) {
+        if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if (!epilogue_tile<kFuse>(a, ctl, q, lane, taddr, mb, et, abort_flag)) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc ? leader_tempty1 : leader_tempty0);
+    }
+  }
+
+  // No CTA leaves while its partner may still signal its barriers or read its
+  // shared memory; then both free their TMEM.
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
                  : "memory");
   }
 }
@@ -559,37 +819,50 @@ int make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, u
   return ENGRAM_OK;
 }
 
-size_t project_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + sizeof(SmemCtl); }
+size_t project_smem_bytes(bool pair) {
+  return 1024 + (pair ? STAGES2 * STAGE2_BYTES : STAGES * STAGE_BYTES) + sizeof(SmemCtl);
+}
+
+// The CTA-pair kernel is the default; ENGRAM_SINGLE_CTA_MMA=1 selects the
+// single-CTA kernel (for comparisons).
+bool use_pair_kernel() {
+  static const bool pair = [] {
+    const char* v = std::getenv("ENGRAM_SINGLE_CTA_MMA");
+    return !(v != nullptr && v[0] == '1');
+  }();
+  return pair;
+}
 
 // Shared argument checks and set-up of both projection entry points.
 int prepare(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint16_t* wkv_packed_d, int32_t hidden,
             int32_t hc, const uint16_t* h_d, const float* q_w_d, const float* k_w_d, float* partials_d,
-            int32_t* status_d, ProjArgs* a, CUtensorMap* tmA, CUtensorMap* tmB, int* grid) {
+            int32_t* status_d, bool pair, ProjArgs* a, CUtensorMap* tmA, CUtensorMap* tmB) {
   if (n_tokens < 0) return fail(ENGRAM_E_INVALID, "n_tokens < 0");
   if (K < BK || K % BK != 0 || K > (int64_t(1) << 20))
     return fail(ENGRAM_E_SHAPE, "K %lld must be a positive multiple of 64", (long long)K);
   if (hidden < BN || hidden % BN != 0) return fail(ENGRAM_E_SHAPE, "hidden %d must be a multiple of 256", hidden);
   if (hc < 1 || hc > kMaxHc) return fail(ENGRAM_E_SHAPE, "hc %d not in [1, %d]", hc, kMaxHc);
   if (n_tokens == 0) return ENGRAM_OK;
-  if (n_tokens > (int64_t(1) << 31) - BM) return fail(ENGRAM_E_SHAPE, "too many tokens");
+  if (n_tokens > (int64_t(1) << 31) - 2 * BM) return fail(ENGRAM_E_SHAPE, "too many tokens");
   if (!e_d || !wkv_packed_d || !h_d || !q_w_d || !k_w_d || !partials_d)
     return fail(ENGRAM_E_INVALID, "null device pointer");
   if (!aligned(e_d, 16) || !aligned(wkv_packed_d, 16) || !aligned(h_d, 16) || !aligned(partials_d, 16))
     return fail(ENGRAM_E_ALIGN, "e, wkv, h and partials must be 16-byte aligned");
-  int sms = 0;
-  int rc = check_device(&sms);
+  int rc = check_device(nullptr);
   if (rc) return rc;
   const int64_t N = static_cast<int64_t>(hc + 1) * hidden;
   if ((rc = make_tmap(tmA, e_d, static_cast<uint64_t>(n_tokens), static_cast<uint64_t>(K), BM))) return rc;
-  if ((rc = make_tmap(tmB, wkv_packed_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN))) return rc;
+  if ((rc = make_tmap(tmB, wkv_packed_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), pair ? BN / 2 : BN)))
+    return rc;
   *a = ProjArgs{};
   a->M = n_tokens;
   a->K = static_cast<int32_t>(K);
   a->H = hidden;
   a->hc = hc;
   a->mt = static_cast<int32_t>((n_tokens + BM - 1) / BM);
+  a->mt2 = static_cast<int32_t>((n_tokens + 2 * BM - 1) / (2 * BM));
   a->nt = static_cast<int32_t>(N / BN);
-  const int64_t tiles = static_cast<int64_t>(a->mt) * a->nt;
+  const int64_t tiles = static_cast<int64_t>(pair ? a->mt2 : a->mt) * a->nt;
   if (tiles > INT32_MAX) return fail(ENGRAM_E_SHAPE, "too many tiles");
   a->num_tiles = static_cast<int32_t>(tiles);
   a->h = const_cast<uint16_t*>(h_d);
@@ -597,8 +870,59 @@ int prepare(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint16_t* wk
   a->k_w = k_w_d;
   a->partials = reinterpret_cast<float4*>(partials_d);
   a->status = status_d;
-  *grid = static_cast<int>(a->num_tiles < sms ? a->num_tiles : sms);
   return ENGRAM_OK;
+}
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, ProjArgs);
+
+// Launches one of the four projection kernels: single CTA or CTA pair,
+// unfused or fused.  Fused launches are cooperative (every CTA resident).
+int launch(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB, const ProjArgs& a,
+           cudaStream_t st) {
+  const void* fn = pair ? (fused ? reinterpret_cast<const void*>(&project2_kernel<true>)
+                                 : reinterpret_cast<const void*>(&project2_kernel<false>))
+                        : (fused ? reinterpret_cast<const void*>(&project_kernel<true>)
+                                 : reinterpret_cast<const void*>(&project_kernel<false>));
+  const size_t smem = project_smem_bytes(pair);
+  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(project): %s", cudaGetErrorString(err));
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int nattr = 0;
+  int units = sms;  // CTAs (single) or CTA pairs that can be resident at once
+  if (pair) {
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = 2;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+    cfg.gridDim = dim3(2 * (sms / 2));
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    int clusters = 0;
+    err = cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg);
+    if (err != cudaSuccess || clusters < 1)
+      return fail(ENGRAM_E_CUDA, "no resident CTA pair for the projection: %s", cudaGetErrorString(err));
+    units = clusters;
+  }
+  if (fused) {
+    attr[nattr].id = cudaLaunchAttributeCooperative;
+    attr[nattr].val.cooperative = 1;
+    ++nattr;
+  }
+  const int n = a.num_tiles < units ? a.num_tiles : units;
+  cfg.gridDim = dim3(pair ? 2 * n : n);
+  cfg.attrs = attr;
+  cfg.numAttrs = nattr;
+  err = cudaLaunchKernelEx(&cfg, reinterpret_cast<KernelFn>(const_cast<void*>(fn)), tmA, tmB, a);
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "project kernel launch: %s", cudaGetErrorString(err));
+  return check_launch("project kernel");
 }
 
 }  // namespace
@@ -631,19 +955,14 @@ extern "C" int engram_project(const uint16_t* e_d, int64_t n_tokens, int64_t K,
                               float* partials_d, uint16_t* v_d, int32_t* status_d, void* stream) {
   if (!v_d && n_tokens > 0) return fail(ENGRAM_E_INVALID, "null device pointer");
   if (v_d && !aligned(v_d, 16)) return fail(ENGRAM_E_ALIGN, "v must be 16-byte aligned");
+  const bool pair = use_pair_kernel();
   ProjArgs a;
   CUtensorMap tmA, tmB;
-  int grid = 0;
-  int rc = prepare(e_d, n_tokens, K, wkv_packed_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d, status_d, &a, &tmA,
-                   &tmB, &grid);
+  int rc = prepare(e_d, n_tokens, K, wkv_packed_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d, status_d, pair, &a,
+                   &tmA, &tmB);
   if (rc || n_tokens == 0) return rc;
   a.v = v_d;
-  const size_t smem = project_smem_bytes();
-  cudaError_t err = cudaFuncSetAttribute(project_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(project): %s", cudaGetErrorString(err));
-  project_kernel<false><<<grid, kThreads, smem, as_stream(stream)>>>(tmA, tmB, a);
-  return check_launch("project_kernel");
+  return launch(pair, false, tmA, tmB, a, as_stream(stream));
 }
 
 namespace {
@@ -654,7 +973,8 @@ struct FusedWs {
 };
 FusedWs fused_ws(int64_t n_tokens, int32_t hidden, int32_t hc) {
   FusedWs w;
-  const size_t mt = static_cast<size_t>((n_tokens + BM - 1) / BM);
+  // 128-row blocks; the CTA-pair kernel's last 256-row tile may reach one past ceil(M/128)
+  const size_t mt = 2 * static_cast<size_t>((n_tokens + 2 * BM - 1) / (2 * BM));
   w.partials = engram_project_partials_bytes(n_tokens, hidden, hc);
   w.counters_off = (w.partials + 255) / 256 * 256;
   w.counter_words = mt * hc * 4 + mt + 1;
@@ -679,18 +999,19 @@ extern "C" int engram_project_gate(const uint16_t* e_d, int64_t n_tokens, int64_
   const size_t need = engram_project_gate_workspace_bytes(n_tokens, hidden, hc);
   if (n_tokens > 0 && workspace_bytes < need)
     return fail(ENGRAM_E_SHAPE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  const bool pair = use_pair_kernel();
   ProjArgs a;
   CUtensorMap tmA, tmB;
-  int grid = 0;
   float* partials_d = static_cast<float*>(workspace_d);
-  int rc = prepare(e_d, n_tokens, K, wkv_packed_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d, status_d, &a, &tmA,
-                   &tmB, &grid);
+  int rc = prepare(e_d, n_tokens, K, wkv_packed_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d, status_d, pair, &a,
+                   &tmA, &tmB);
   if (rc || n_tokens == 0) return rc;
   const FusedWs ws = fused_ws(n_tokens, hidden, hc);
   unsigned char* base = static_cast<unsigned char*>(workspace_d);
+  const int mt_ws = 2 * a.mt2;
   a.cnt = reinterpret_cast<int32_t*>(base + ws.counters_off);
-  a.ready = a.cnt + static_cast<size_t>(a.mt) * hc * 4;
-  a.abort_g = a.ready + a.mt;
+  a.ready = a.cnt + static_cast<size_t>(mt_ws) * hc * 4;
+  a.abort_g = a.ready + mt_ws;
   a.gates = reinterpret_cast<float*>(base + ws.gates_off);
   a.mask = mask_d;
   a.gate_out = gate_out_d;
@@ -700,22 +1021,5 @@ extern "C" int engram_project_gate(const uint16_t* e_d, int64_t n_tokens, int64_
   cudaStream_t st = as_stream(stream);
   cudaError_t err = cudaMemsetAsync(a.cnt, 0, ws.counter_words * sizeof(int32_t), st);
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaMemsetAsync(counters): %s", cudaGetErrorString(err));
-  const size_t smem = project_smem_bytes();
-  err = cudaFuncSetAttribute(project_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(project): %s", cudaGetErrorString(err));
-  // Cooperative: every CTA is resident at once, which the in-kernel wait of
-  // value tiles on key tiles relies on.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, project_kernel<true>, tmA, tmB, a);
-  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "project_kernel (fused) launch: %s", cudaGetErrorString(err));
-  return check_launch("project_kernel (fused)");
+  return launch(pair, true, tmA, tmB, a, st);
 }

@@ -1,0 +1,23 @@
+"""The single-CTA projection kernels (selected with ENGRAM_SINGLE_CTA_MMA=1)
+pass the same projection parity tests as the default CTA-pair kernels.
+
+The selection is read once per process, so the tests run in a child process.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+from gpu_util import require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_single_cta_kernels_pass_projection_parity():
+    require_gpu()
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, ENGRAM_SINGLE_CTA_MMA="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_project.py"), "-m", "gpu", "-q",
+                        "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
