@@ -40,7 +40,7 @@ KERNEL_FILES = ["project.cu", "gather.cu", "hash.cu", "engram_internal.h"]
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--steps", type=int, default=700)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="prefill")
@@ -308,24 +308,31 @@ def run_ours(args, rank, world, local):
         return None
 
     peaks, peak_src = load_peaks()
+    timed_s = wall1 - wall0
     if micro is not None:
         micro["frac"] = micro["gather_gbs"] / peaks["hbm_gbs"]
         micro["peak_gbs"] = peaks["hbm_gbs"]
-    sustained = total_s >= 2.0
+    # A timed region of 2 s or more of back-to-back steps runs under the power
+    # cap like the driver's sustained GEMM loop; shorter ones compare to burst.
+    sustained = timed_s >= 2.0
     tf_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     flops = 2.0 * T * 6144 * (w.hc + 1) * w.hidden
     proj_s = statistics.mean(stage["project_gate"]) / 1e3
     gat_s = statistics.mean(stage["gather"]) / 1e3
     traffic = profiled_traffic()
-    roof = {"bound": "tensor", "kernel": "project_kernel<fused> (tcgen05 wkv GEMM, gate and residual in the epilogue)",
+    roof = {"bound": "tensor",
+            "kernel": "project2_kernel<fused> (CTA-pair tcgen05 wkv GEMM, gate and residual in the epilogue)",
             "achieved": flops / proj_s / 1e12, "peak": tf_peak, "unit": "TFLOP/s",
-            "frac": flops / proj_s / 1e12 / tf_peak, "traffic": traffic.get("project_kernel"),
+            "frac": flops / proj_s / 1e12 / tf_peak, "frac_vs_burst": flops / proj_s / 1e12 / peaks["bf16_tflops"],
+            "traffic": traffic.get("project2_kernel"),
             "algorithmic_per_launch": f"{flops:.4g} FLOP (2*T*6144*{(w.hc + 1) * w.hidden}, T={T})",
             "peak_source": f"{peak_src} bf16_tflops{'_sustained' if sustained else ''}"}
     gbytes = GATHER_BYTES_PER_TOKEN * T
-    roof_g = {"bound": "hbm", "kernel": "gather_dequant_kernel", "achieved": gbytes / gat_s / 1e9,
+    gather_kernel = "gather_dequant_kernel" if os.environ.get("ENGRAM_GATHER", "").startswith("b") \
+        else "gather_ldgsts_kernel"
+    roof_g = {"bound": "hbm", "kernel": gather_kernel, "achieved": gbytes / gat_s / 1e9,
               "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbytes / gat_s / 1e9 / peaks["hbm_gbs"],
-              "traffic": traffic.get("gather_dequant_kernel"),
+              "traffic": traffic.get(gather_kernel),
               "algorithmic_per_launch": f"{gbytes} B ({GATHER_BYTES_PER_TOKEN} B/token, T={T})",
               "peak_source": f"{peak_src} hbm_gbs"}
     out = {

@@ -23,6 +23,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstdlib>
+
 #include "engram_internal.h"
 
 namespace engram {
@@ -184,6 +186,119 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_dequant_kernel(GatherAr
   }
 }
 
+
+// 16-byte (or 8-byte) asynchronous global -> shared copies through the L1/LSU
+// path; completion of a thread's earlier copies is signalled on an mbarrier.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Same pipeline as gather_dequant_kernel, but each row window moves as 17
+// 16-byte cp.async copies spread over the warp's lanes (a flat list of
+// n_cols * 17 pieces per position) instead of one bulk copy per row: many
+// small requests go through the LSU rather than the TMA unit.
+__global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int w = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t stage_bytes = static_cast<uint32_t>(a.n_cols) * kSlot;
+  const int S = a.stages;
+  uint8_t* wbuf = smem + static_cast<size_t>(w) * S * stage_bytes;
+  uint8_t* meta = smem + static_cast<size_t>(kWarps) * S * stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(meta) + w * S;
+  uint32_t* masks = reinterpret_cast<uint32_t*>(meta + kWarps * S * 8) + w * S * 2;
+
+  if (lane == 0)
+    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 32);  // one async arrival per lane
+  fence_mbar_init();
+  __syncwarp();
+
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + w;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int n_cols = a.n_cols;
+  const int pieces = n_cols * 17;
+
+  auto issue = [&](int64_t t, int s) {
+    int32_t r = -1;
+    bool valid = false;
+    if (lane < static_cast<uint32_t>(n_cols)) {
+      r = __ldg(a.rows + t * n_cols + lane);
+      valid = r >= 0 && static_cast<int64_t>(r) < a.total_rows;
+      if (!valid && a.status) atomicOr(a.status, static_cast<int>(ENGRAM_ST_BAD_ROW));
+    }
+    // an even row whose 272-byte window passes the end of the allocation
+    // copies its last piece as the 8 scale bytes only
+    const bool tail = valid && !(r & 1) && static_cast<int64_t>(r) * kRowBytes + kSlot > a.table_bytes;
+    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+    const uint32_t odd = __ballot_sync(0xffffffffu, valid && (r & 1));
+    const uint32_t tmask = __ballot_sync(0xffffffffu, tail);
+    if (lane == 0) {
+      masks[2 * s] = odd;
+      masks[2 * s + 1] = vmask;
+    }
+    const uint32_t sbase = smem_u32(wbuf + static_cast<size_t>(s) * stage_bytes);
+    for (int p0 = 0; p0 < pieces; p0 += 32) {
+      const int p = p0 + static_cast<int>(lane);
+      const int row = p / 17;
+      const int piece = p - 17 * row;
+      const int rr = __shfl_sync(0xffffffffu, r, row < 32 ? row : 0);
+      if (p < pieces && ((vmask >> row) & 1u)) {
+        const uint8_t* src = a.table + ((static_cast<int64_t>(rr) * kRowBytes) & ~int64_t(15)) + piece * 16;
+        const uint32_t dst = sbase + row * kSlot + piece * 16;
+        if (piece == 16 && ((tmask >> row) & 1u)) cp_async8(dst, src);
+        else cp_async16(dst, src);
+      }
+    }
+    cp_async_arrive(smem_u32(&bars[s]));
+  };
+
+  for (int s = 0; s < S; ++s) {
+    const int64_t t = gw + s * nw;
+    if (t < a.n_tokens) issue(t, s);
+  }
+
+  int64_t k = 0;
+  bool timed_out = false;
+  for (;; ++k) {
+    const int64_t t = gw + k * nw;
+    if (t >= a.n_tokens) break;
+    const int s = static_cast<int>(k % S);
+    const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
+    if (!mbar_wait_bounded(smem_u32(&bars[s]), parity, nullptr)) {
+      timed_out = true;
+      break;
+    }
+    const uint32_t odd = masks[2 * s];
+    const uint32_t vm = masks[2 * s + 1];
+    const uint8_t* sb = wbuf + static_cast<size_t>(s) * stage_bytes;
+    uint16_t* out = a.e + t * static_cast<int64_t>(n_cols) * ENGRAM_HEAD_DIM;
+#pragma unroll 4
+    for (int j = 0; j < n_cols; ++j) {
+      const uint8_t* row = sb + j * kSlot + (((odd >> j) & 1u) ? 8 : 0);
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if ((vm >> j) & 1u) {
+        const uint2 wv = *reinterpret_cast<const uint2*>(row + lane * 8);
+        const uint32_t sbyte = row[256 + (lane >> 2)];
+        o = dequant8(wv, sbyte);
+      }
+      *reinterpret_cast<uint4*>(out + j * ENGRAM_HEAD_DIM + lane * 8) = o;
+    }
+    __syncwarp();
+    const int64_t t2 = t + static_cast<int64_t>(S) * nw;
+    if (t2 < a.n_tokens) issue(t2, s);
+  }
+  if (timed_out) {
+    if (lane == 0 && a.status) atomicOr(a.status, static_cast<int>(ENGRAM_ST_TIMEOUT));
+    asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's copies land before exit
+  }
+}
+
 // SplitMix64 output number n+1 of a stream starting at `seed` (Steele, Lea &
 // Flood 2014): finaliser applied to seed + (n+1) * golden gamma.
 __device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t n) {
@@ -217,6 +332,16 @@ __global__ void fill_table_kernel(uint8_t* table, int64_t n_words, uint64_t seed
   }
 }
 
+// The cp.async row copies are the default; ENGRAM_GATHER=bulk selects one
+// bulk (TMA) copy per row instead.  Both measure the same on GB300.
+bool use_ldgsts() {
+  static const bool v = [] {
+    const char* e = std::getenv("ENGRAM_GATHER");
+    return !(e != nullptr && e[0] == 'b');
+  }();
+  return v;
+}
+
 }  // namespace
 }  // namespace engram
 
@@ -243,13 +368,17 @@ extern "C" int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows,
   if (stages > 4) stages = 4;
   if (stages < 1) return fail(ENGRAM_E_SHAPE, "n_cols %d does not fit shared memory", n_cols);
   const size_t smem = static_cast<size_t>(kWarps) * stages * per_stage;
-  cudaError_t err = cudaFuncSetAttribute(gather_dequant_kernel,
+  cudaError_t err = cudaFuncSetAttribute(use_ldgsts() ? gather_ldgsts_kernel : gather_dequant_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
   if (err != cudaSuccess)
     return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(gather): %s", cudaGetErrorString(err));
   GatherArgs a{table_d, total_rows, table_bytes, row_ids_d, n_tokens, n_cols, stages, e_d, status_d};
   const int64_t want = (n_tokens + kWarps - 1) / kWarps;
   const int blocks = static_cast<int>(want < sms ? want : sms);
+  if (use_ldgsts()) {
+    gather_ldgsts_kernel<<<blocks, kWarps * 32, smem, as_stream(stream)>>>(a);
+    return check_launch("gather_ldgsts_kernel");
+  }
   gather_dequant_kernel<<<blocks, kWarps * 32, smem, as_stream(stream)>>>(a);
   return check_launch("gather_dequant_kernel");
 }

@@ -873,6 +873,17 @@ int prepare(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint16_t* wk
   return ENGRAM_OK;
 }
 
+// Fused launches are cooperative unless ENGRAM_COOPERATIVE=0 (for profilers
+// that cannot replay a cooperative cluster launch).  The grid never exceeds
+// the resident capacity either way, and every in-kernel wait is bounded.
+bool use_cooperative() {
+  static const bool v = [] {
+    const char* e = std::getenv("ENGRAM_COOPERATIVE");
+    return !(e != nullptr && e[0] == '0');
+  }();
+  return v;
+}
+
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, ProjArgs);
 
 // Launches one of the four projection kernels: single CTA or CTA pair,
@@ -911,7 +922,7 @@ int launch(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB
       return fail(ENGRAM_E_CUDA, "no resident CTA pair for the projection: %s", cudaGetErrorString(err));
     units = clusters;
   }
-  if (fused) {
+  if (fused && use_cooperative()) {
     attr[nattr].id = cudaLaunchAttributeCooperative;
     attr[nattr].val.cooperative = 1;
     ++nattr;
