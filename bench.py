@@ -46,6 +46,7 @@ def parse():
     p.add_argument("--workload", default="prefill")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--micro-steps", type=int, default=30, help="steps of the hash+gather microbench phase")
+    p.add_argument("--decode-steps", type=int, default=200, help="steps of the decode phase")
     p.add_argument("--cpu-sample", type=int, default=8192, help="tokens of the oracle CPU baseline sample")
     p.add_argument("--ref-sample", type=int, default=128, help="tokens per reference-arm step")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -303,6 +304,7 @@ def run_ours(args, rank, world, local):
                "api": "EngramLayer.prefill with pinned host inputs/outputs"}
 
     micro = microbench(args, w, inp, layer, flush, dev) if args.micro_steps > 0 else None
+    dec = decode_bench(args, w, inp, layer, flush, dev) if args.decode_steps > 0 else None
 
     if rank != 0:
         return None
@@ -312,6 +314,8 @@ def run_ours(args, rank, world, local):
     if micro is not None:
         micro["frac"] = micro["gather_gbs"] / peaks["hbm_gbs"]
         micro["peak_gbs"] = peaks["hbm_gbs"]
+    if dec is not None:
+        dec["wkv_frac_hbm"] = dec["wkv_gbs"] / peaks["hbm_gbs"]
     # A timed region of 2 s or more of back-to-back steps runs under the power
     # cap like the driver's sustained GEMM loop; shorter ones compare to burst.
     sustained = timed_s >= 2.0
@@ -354,6 +358,7 @@ def run_ours(args, rank, world, local):
         "roofline": roof,
         "roofline_gather": roof_g,
         "microbench_hash_gather": micro,
+        "decode_step": dec,
         "gpu_launches": args.steps * 4,
         "clocks": clocks,
         "e2e": e2e,
@@ -407,6 +412,63 @@ def microbench(args, w, inp, layer, flush, dev):
     return {"workload": f"microbench: 1 x {T} Zipf(1.1) tokens, same 12.67 GB table", "steps": args.micro_steps,
             "hash_gather_tokens_per_s": T / step, "hash_ms": (step - gat) * 1e3, "gather_ms": gat * 1e3,
             "gather_gbs": gbytes / gat / 1e9, "algorithmic_bytes": gbytes}
+
+
+def decode_bench(args, w, inp, layer, flush, dev):
+    """Decode steps: 256 sequences of the decode workload, one token each, over the bench's table."""
+    import torch
+    import hashed_gram_conditional_gb300 as eg
+    from workloads import WORKLOADS, decode_workload
+
+    wd = WORKLOADS["decode"]
+    if (wd.v, wd.v_raw, wd.hidden, wd.hc) != (w.v, w.v_raw, w.hidden, w.hc):
+        return None
+    n = args.decode_steps
+    dw = decode_workload(wd, n_steps=n + 3)
+    B = wd.n_seqs
+    hist = torch.full((B, 3), layer.layout.pad_id, dtype=torch.int32, device=dev)
+    eg.engram_hash(layer.layout, 0, torch.from_numpy(dw.prefix.raw_ids).to(dev),
+                   torch.from_numpy(dw.prefix.cu_seqlens).to(dev), layer.token_map, hist)
+    steps = torch.from_numpy(dw.steps).to(dev)
+    slots = torch.arange(B, dtype=torch.int32, device=dev)
+    rows = torch.empty((B, 24), dtype=torch.int32, device=dev)
+    mask = torch.empty(B, dtype=torch.uint8, device=dev)
+    e = torch.empty((B, 6144), dtype=torch.bfloat16, device=dev)
+    h = torch.randn((B, wd.hc, wd.hidden), device=dev).to(torch.bfloat16)
+    work = eg.project_gate_workspace(B, wd.hidden, wd.hc, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def run(k, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        eg.engram_hash_step(layer.layout, 0, steps[k], slots, layer.token_map, hist, rows, mask)
+        if ev is not None:
+            ev[1].record(stream)
+        eg.engram_gather_dequant(layer.table, layer.total_rows, rows, e)
+        if ev is not None:
+            ev[2].record(stream)
+        eg.engram_project_gate(e, layer.wkv_packed, h, layer.q_w, layer.k_w, mask, layer.eps, layer.clamp,
+                               layer.score_scale, None, work)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for k in range(3):
+        flush.zero_()
+        run(k)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    for k in range(n):
+        flush.zero_()
+        run(3 + k, evs[k])
+    torch.cuda.synchronize()
+    step = statistics.mean(ev[0].elapsed_time(ev[3]) for ev in evs) / 1e3
+    proj = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs) / 1e3
+    wkv_bytes = 6144 * (wd.hc + 1) * wd.hidden * 2
+    return {"workload": f"decode: {B} sequences x 1 token, histories from U[0, 8192] prefixes, table of the "
+                        f"{w.name} workload", "steps": n,
+            "step_ms": step * 1e3, "steps_per_s": 1 / step, "tokens_per_s": B / step,
+            "hash_step_ms": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
+            "gather_ms": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs),
+            "project_gate_ms": proj * 1e3, "wkv_gbs": wkv_bytes / proj / 1e9}
 
 
 # ------------------------------------------------------------------------- oracle timing

@@ -192,6 +192,23 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// 4-D tiled TMA loads of the packed wkv ([N/128][K/64][128][64]).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int32_t c2, int32_t c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(tmap), "r"(0), "r"(0), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap, int32_t c2, int32_t c3,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5}], [%6];" ::"r"(dst),
+      "l"(tmap), "r"(0), "r"(0), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -303,12 +320,20 @@ __device__ __forceinline__ bool epilogue_tile(const ProjArgs& a, SmemCtl* ctl, i
   if (key_tile) {
     const uint4* hrow = reinterpret_cast<const uint4*>(a.h + (t * a.hc + m) * a.H + c0);
     float dot = 0.f, kk = 0.f, hh = 0.f;
+    // h of chunk ch+1 is requested while chunk ch is processed (one chunk ahead)
+    uint4 hnext[4];
+    if (live) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hnext[i] = __ldg(hrow + i);
+    }
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
       uint4 hv[4];
-      if (live) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) hv[i] = __ldg(hrow + ch * 4 + i);
+      for (int i = 0; i < 4; ++i) hv[i] = hnext[i];
+      if (live && ch + 1 < BN / 32) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hnext[i] = __ldg(hrow + (ch + 1) * 4 + i);
       }
       uint32_t r[32];
       __syncwarp();
@@ -347,12 +372,13 @@ __device__ __forceinline__ bool epilogue_tile(const ProjArgs& a, SmemCtl* ctl, i
           if (!masked) {
             const float4* p = a.partials + (t * a.hc + m) * ntile;
             float sd = 0.f, sk = 0.f, sh = 0.f;
-            for (int q0 = 0; q0 < ntile; q0 += 8) {
-              float4 x[8];
+            for (int q0 = 0; q0 < ntile; q0 += 24) {  // 24 loads in flight: one round trip at hidden <= 6144
+              float4 x[24];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) x[i] = (q0 + i < ntile) ? __ldcg(p + q0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int i = 0; i < 24; ++i)
+                x[i] = (q0 + i < ntile) ? __ldcg(p + q0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {  // tile order: deterministic
+              for (int i = 0; i < 24; ++i) {  // tile order: deterministic
                 sd += x[i].x;
                 sk += x[i].y;
                 sh += x[i].z;
@@ -373,7 +399,26 @@ __device__ __forceinline__ bool epilogue_tile(const ProjArgs& a, SmemCtl* ctl, i
       }
     }
   } else if (kFuse) {
-    // ---- value tile, fused: wait for the M-block's gates, then h <- bf16(h + g bf16(v))
+    // ---- value tile, fused: wait for the M-block's gates, then h <- bf16(h + g bf16(v)).
+    // The transposed pass gives lane l the 16-byte segment (l & 3) of rows
+    // rl = 8 k8 + l / 4; h of those rows is written only by this tile, so the
+    // first chunk's h is requested before the gates are, and every later
+    // chunk's h one chunk ahead of its update (streams 0..3; more streams use
+    // a plain loop).
+    const int seg = static_cast<int>(lane & 3);
+    const int hc4 = a.hc < 4 ? a.hc : 4;
+    uint4 hn[4][4];
+    auto load_chunk = [&](int ch, uint4 (&dst)[4][4]) {
+#pragma unroll
+      for (int k8 = 0; k8 < 4; ++k8) {
+        const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + k8 * 8 + static_cast<int>(lane >> 2);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < hc4 && tr < a.M)
+            dst[k8][j] = *reinterpret_cast<const uint4*>(a.h + (tr * a.hc + j) * a.H + c0 + ch * 32 + seg * 8);
+      }
+    };
+    load_chunk(0, hn);
     bool ready = true;
     if (lane == 0) ready = wait_published(a.ready + mb, 4 * a.hc, a.abort_g, abort_flag);
     ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
@@ -382,10 +427,16 @@ __device__ __forceinline__ bool epilogue_tile(const ProjArgs& a, SmemCtl* ctl, i
       return false;
     }
     for (int mm = 0; mm < a.hc; ++mm) ctl->sg[q][lane][mm] = live ? __ldcg(a.gates + t * a.hc + mm) : -1.0f;
+    __syncwarp();
     uint32_t(*sv)[20] = ctl->sv[q];
-    const int seg = static_cast<int>(lane & 3);
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
+      uint4 hv[4][4];
+#pragma unroll
+      for (int k8 = 0; k8 < 4; ++k8)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hv[k8][j] = hn[k8][j];
+      if (ch + 1 < BN / 32) load_chunk(ch + 1, hn);
       uint32_t r[32];
       __syncwarp();
       tc_ld32(taddr + ch * 32, r);
@@ -402,39 +453,33 @@ __device__ __forceinline__ bool epilogue_tile(const ProjArgs& a, SmemCtl* ctl, i
         *reinterpret_cast<uint4*>(&sv[lane][i * 4]) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       __syncwarp();
-      // Transposed pass: 4 lanes cover one row's 64-byte segment, 8 rows per
-      // step.  All loads of up to 4 streams are issued before any update.
-      for (int m0 = 0; m0 < a.hc; m0 += 4) {
-        uint4 hv[4][4];
-        float gg[4][4];
 #pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8) {
-          const int rl = k8 * 8 + static_cast<int>(lane >> 2);
-          const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + rl;
+      for (int k8 = 0; k8 < 4; ++k8) {
+        const int rl = k8 * 8 + static_cast<int>(lane >> 2);
+        const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + rl;
+        const uint4 vv = *reinterpret_cast<const uint4*>(&sv[rl][seg * 4]);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int mm = m0 + j;
-            gg[k8][j] = (mm < a.hc && tr < a.M) ? ctl->sg[q][rl][mm] : -1.0f;
-            if (gg[k8][j] >= 0.0f)
-              hv[k8][j] = *reinterpret_cast<const uint4*>(a.h + (tr * a.hc + mm) * a.H + c0 + ch * 32 + seg * 8);
-          }
+        for (int j = 0; j < 4; ++j) {
+          const float g = ctl->sg[q][rl][j];
+          if (j >= hc4 || tr >= a.M || g < 0.0f) continue;
+          uint4 x = hv[k8][j];
+          x.x = fma_bf16x2(x.x, g, vv.x);
+          x.y = fma_bf16x2(x.y, g, vv.y);
+          x.z = fma_bf16x2(x.z, g, vv.z);
+          x.w = fma_bf16x2(x.w, g, vv.w);
+          *reinterpret_cast<uint4*>(a.h + (tr * a.hc + j) * a.H + c0 + ch * 32 + seg * 8) = x;
         }
-#pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8) {
-          const int rl = k8 * 8 + static_cast<int>(lane >> 2);
-          const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + rl;
-          const uint4 vv = *reinterpret_cast<const uint4*>(&sv[rl][seg * 4]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float g = gg[k8][j];
-            if (g < 0.0f) continue;
-            uint4 x = hv[k8][j];
-            x.x = fma_bf16x2(x.x, g, vv.x);
-            x.y = fma_bf16x2(x.y, g, vv.y);
-            x.z = fma_bf16x2(x.z, g, vv.z);
-            x.w = fma_bf16x2(x.w, g, vv.w);
-            *reinterpret_cast<uint4*>(a.h + (tr * a.hc + m0 + j) * a.H + c0 + ch * 32 + seg * 8) = x;
-          }
+        // streams beyond the fourth (hidden-connection counts above 4)
+        for (int mm = 4; mm < a.hc; ++mm) {
+          const float g = ctl->sg[q][rl][mm];
+          if (tr >= a.M || g < 0.0f) continue;
+          uint4* hp = reinterpret_cast<uint4*>(a.h + (tr * a.hc + mm) * a.H + c0 + ch * 32 + seg * 8);
+          uint4 x = *hp;
+          x.x = fma_bf16x2(x.x, g, vv.x);
+          x.y = fma_bf16x2(x.y, g, vv.y);
+          x.z = fma_bf16x2(x.z, g, vv.z);
+          x.w = fma_bf16x2(x.w, g, vv.w);
+          *hp = x;
         }
       }
     }
@@ -523,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_u32(&ctl->full[s]);
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           tma_load_2d(smem_u32(smA + s * A_BYTES), &tmA, kb * BK, mb * BM, fb);
-          tma_load_2d(smem_u32(smB + s * B_BYTES), &tmB, kb * BK, nb * BN, fb);
+          tma_load_4d(smem_u32(smB + s * B_BYTES), &tmB, kb, nb * (BN / 128), fb);
         }
       }
       // Drain: the last STAGES loads issued must have landed before the CTA
@@ -679,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t leader_fb = map_to_cta(fb, 0);
           tma_load_2d_pair(smem_u32(smA + s * A_BYTES), &tmA, kb * BK, mb2 * (2 * BM) + static_cast<int>(rank) * BM,
                            leader_fb);
-          tma_load_2d_pair(smem_u32(smB + s * B2_BYTES), &tmB, kb * BK, nb * BN + static_cast<int>(rank) * (BN / 2),
+          tma_load_4d_pair(smem_u32(smB + s * B2_BYTES), &tmB, kb, nb * (BN / 128) + static_cast<int>(rank),
                            leader_fb);
         }
       }
@@ -767,6 +812,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// wkv [K][N] -> tiled K-major operand layout [N/128][K/64][128][64]: the
+// 128 x 64 tile (rows n, columns k) of every k-block is 16 KB contiguous and a
+// 128-row block of wkv^T is one contiguous 1.5 MB run, so operand loads stream
+// whole DRAM pages instead of 128-byte pieces of rows 12 KB apart.
 __global__ void pack_wkv_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
                                 uint16_t* __restrict__ wt) {
   __shared__ uint16_t tile[32][33];
@@ -777,9 +826,13 @@ __global__ void pack_wkv_kernel(const uint16_t* __restrict__ w, int64_t K, int64
     if (k < K && n < N) tile[i][threadIdx.x] = w[k * N + n];
   }
   __syncthreads();
+  const int64_t kblocks = K / 64;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int64_t n = n0 + i, k = k0 + threadIdx.x;
-    if (k < K && n < N) wt[n * K + k] = tile[threadIdx.x][i];
+    if (k < K && n < N) {
+      const int64_t idx = (((n >> 7) * kblocks + (k >> 6)) << 13) + ((n & 127) << 6) + (k & 63);
+      wt[idx] = tile[threadIdx.x][i];
+    }
   }
 }
 
@@ -819,6 +872,23 @@ int make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, u
   return ENGRAM_OK;
 }
 
+// Packed wkv as a 4-D tensor {64, 128, K/64, N/128} (innermost first); a box
+// covers one k-block of `nblocks` consecutive 128-row blocks, 128-byte swizzle.
+int make_tmap_wkv(CUtensorMap* tm, const void* base, uint64_t N, uint64_t K, uint32_t nblocks) {
+  EncodeTiledFn enc;
+  int rc = get_encode_fn(&enc);
+  if (rc) return rc;
+  const cuuint64_t dims[4] = {64, 128, K / 64, N / 128};
+  const cuuint64_t strides[3] = {128, 128 * 128, (K / 64) * 128 * 128};
+  const cuuint32_t box[4] = {64, 128, 1, nblocks};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ENGRAM_E_CUDA, "cuTensorMapEncodeTiled(wkv) failed (%d)", static_cast<int>(r));
+  return ENGRAM_OK;
+}
+
 size_t project_smem_bytes(bool pair) {
   return 1024 + (pair ? STAGES2 * STAGE2_BYTES : STAGES * STAGE_BYTES) + sizeof(SmemCtl);
 }
@@ -852,7 +922,7 @@ int prepare(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint16_t* wk
   if (rc) return rc;
   const int64_t N = static_cast<int64_t>(hc + 1) * hidden;
   if ((rc = make_tmap(tmA, e_d, static_cast<uint64_t>(n_tokens), static_cast<uint64_t>(K), BM))) return rc;
-  if ((rc = make_tmap(tmB, wkv_packed_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), pair ? BN / 2 : BN)))
+  if ((rc = make_tmap_wkv(tmB, wkv_packed_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), pair ? 1 : 2)))
     return rc;
   *a = ProjArgs{};
   a->M = n_tokens;
@@ -944,6 +1014,7 @@ using namespace engram;
 extern "C" int engram_pack_wkv(const uint16_t* wkv_d, int64_t K, int64_t N, uint16_t* wkv_packed_d,
                                void* stream) {
   if (K < 1 || N < 1) return fail(ENGRAM_E_INVALID, "K and N must be positive");
+  if (K % 64 != 0 || N % 128 != 0) return fail(ENGRAM_E_SHAPE, "K must be a multiple of 64 and N of 128");
   if (!wkv_d || !wkv_packed_d) return fail(ENGRAM_E_INVALID, "null device pointer");
   if (wkv_d == wkv_packed_d) return fail(ENGRAM_E_INVALID, "in-place repack is not supported");
   int rc = check_device(nullptr);
@@ -979,8 +1050,16 @@ extern "C" int engram_project(const uint16_t* e_d, int64_t n_tokens, int64_t K,
 namespace {
 // Fused-mode workspace: [partials | counters: cnt[mt][hc][4], ready[mt], abort | gates[mt*128][hc]],
 // each part starting on a 256-byte boundary.
+// Up to this many tokens engram_project_gate runs the two-kernel path (the
+// projection storing v, then the gate kernel) inside its workspace: at decode
+// sizes the whole projection is one or two waves of tiles and the fused
+// kernel's key-then-value dependency costs more than the separate gate pass
+// (measured on GB300: 256 tokens 114 us fused vs ~99 us two-kernel; break-even
+// near 2048 tokens).
+constexpr int64_t kTwoKernelMaxTokens = 1536;
+
 struct FusedWs {
-  size_t partials, counters_off, counter_words, gates_off, total;
+  size_t partials, counters_off, counter_words, gates_off, v_off, total;
 };
 FusedWs fused_ws(int64_t n_tokens, int32_t hidden, int32_t hc) {
   FusedWs w;
@@ -990,7 +1069,8 @@ FusedWs fused_ws(int64_t n_tokens, int32_t hidden, int32_t hc) {
   w.counters_off = (w.partials + 255) / 256 * 256;
   w.counter_words = mt * hc * 4 + mt + 1;
   w.gates_off = w.counters_off + (w.counter_words * 4 + 255) / 256 * 256;
-  w.total = w.gates_off + mt * BM * hc * sizeof(float);
+  w.v_off = w.gates_off + (mt * BM * hc * sizeof(float) + 255) / 256 * 256;
+  w.total = w.v_off + (n_tokens <= kTwoKernelMaxTokens ? static_cast<size_t>(n_tokens) * hidden * 2 : 0);
   return w;
 }
 }  // namespace
@@ -1010,6 +1090,17 @@ extern "C" int engram_project_gate(const uint16_t* e_d, int64_t n_tokens, int64_
   const size_t need = engram_project_gate_workspace_bytes(n_tokens, hidden, hc);
   if (n_tokens > 0 && workspace_bytes < need)
     return fail(ENGRAM_E_SHAPE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  if (n_tokens > 0 && n_tokens <= kTwoKernelMaxTokens) {
+    const FusedWs ws = fused_ws(n_tokens, hidden, hc);
+    unsigned char* base = static_cast<unsigned char*>(workspace_d);
+    float* partials_d = reinterpret_cast<float*>(base);
+    uint16_t* v_d = reinterpret_cast<uint16_t*>(base + ws.v_off);
+    int rc = engram_project(e_d, n_tokens, K, wkv_packed_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d, v_d,
+                            status_d, stream);
+    if (rc) return rc;
+    return engram_gate_add(partials_d, v_d, h_d, mask_d, n_tokens, hidden, hc, eps, clamp, score_scale, gate_out_d,
+                           stream);
+  }
   const bool pair = use_pair_kernel();
   ProjArgs a;
   CUtensorMap tmA, tmB;

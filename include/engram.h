@@ -216,8 +216,11 @@ int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows, int64_t ta
 /* ------------------------------------------------------------------------ */
 
 /* Repack wkv from [K][N] (kv = e @ wkv, [P-V41] §"每条流一个 key 的设计":
- * one [6144, 25600] matrix) to the K-major [N][K] operand layout of the
- * tensor-core projection.  One-time, for static weights.  Both bf16. */
+ * one [6144, 25600] matrix) to the tiled K-major operand layout of the
+ * tensor-core projection: [N/128][K/64][128][64], i.e. element (k, n) lands at
+ * ((n/128 * K/64 + k/64) * 128 + n%128) * 64 + k%64, so every 128 x 64 operand
+ * tile is 16 KB contiguous.  One-time, for static weights.  Both bf16, N*K
+ * elements; requires K % 64 == 0 and N % 128 == 0 (ENGRAM_E_SHAPE). */
 int engram_pack_wkv(const uint16_t* wkv_d, int64_t K, int64_t N, uint16_t* wkv_packed_d,
                     void* stream);
 
@@ -235,7 +238,7 @@ size_t engram_project_partials_bytes(int64_t n_tokens, int32_t hidden, int32_t h
  *   keys are not stored.  The value is stored as v_d[t][i] = bf16_rne(v_i).
  *
  *   e_d          bf16 [n_tokens][K], K = n_cols*256, 16-byte aligned
- *   wkv_packed_d bf16 [(hc+1)*hidden][K] from engram_pack_wkv, 16-byte aligned
+ *   wkv_packed_d bf16, (hc+1)*hidden*K elements from engram_pack_wkv, 16-byte aligned
  *   h_d          bf16 [n_tokens][hc][hidden] residual streams (read only here)
  *   q_w_d, k_w_d float32 [hidden][hc]
  *   partials_d   float32, engram_project_partials_bytes(...) bytes
@@ -277,8 +280,9 @@ int engram_gate_add(const float* partials_d, const uint16_t* v_d, uint16_t* h_d,
 
 /* Bytes of the workspace of engram_project_gate: the partial sums
  * (engram_project_partials_bytes), then int32 counters
- * (ceil(n_tokens/128) * (4*hc + 1) + 1 words), then fp32 gates
- * (ceil(n_tokens/128) * 128 * hc), each part on a 256-byte boundary. */
+ * (2*ceil(n_tokens/256) * (4*hc + 1) + 1 words), then fp32 gates
+ * (2*ceil(n_tokens/256) * 128 * hc), then, for at most 1536 tokens, bf16 v
+ * (n_tokens * hidden); each part on a 256-byte boundary. */
 size_t engram_project_gate_workspace_bytes(int64_t n_tokens, int32_t hidden, int32_t hc);
 
 /* The same result as engram_project followed by engram_gate_add, computed in
@@ -289,7 +293,10 @@ size_t engram_project_gate_workspace_bytes(int64_t n_tokens, int32_t hidden, int
  * block's gates and applies h <- bf16(h + g * bf16(v)) directly, so v is never
  * stored.  The gate kernel of the unfused path sums with a shuffle tree, so
  * gates agree with engram_gate_add to fp32 rounding, not bit for bit; the
- * fused result itself is deterministic.
+ * fused result itself is deterministic.  For at most 1536 tokens (decode
+ * sizes, where the projection is only a wave or two of tiles) the call runs
+ * engram_project and engram_gate_add inside the workspace instead, which is
+ * faster there; the results agree to the same rounding.
  *   e_d, wkv_packed_d, h_d, q_w_d, k_w_d   as engram_project (h_d updated in place)
  *   mask_d, eps, clamp, score_scale,
  *   gate_out_d                            as engram_gate_add

@@ -46,8 +46,10 @@ def test_project_partials_v_gate_residual(T, H, hc):
     mask[::17] = True
     k, v, hf, g, out, k_err, v_err = _oracle(e, w, h, qw, kw, mask, T, H, hc)
     wp = eg.engram_pack_wkv(bf16(w))
-    # the repack is a pure permutation of the bf16 bits
-    assert (bits(wp) == w.T).all()
+    # the repack is a pure permutation of the bf16 bits into 128 x 64 tiles of w^T
+    Kd, Nd = w.shape
+    tiled = w.T.reshape(Nd // 128, 128, Kd // 64, 64).transpose(0, 2, 1, 3)
+    assert (bits(wp).reshape(-1) == tiled.reshape(-1)).all()
     h_d = bf16(h)
     st = status()
     partials, v_d = eg.engram_project(bf16(e), wp, h_d, f32(qw), f32(kw), status=st)
@@ -120,9 +122,13 @@ def test_project_large_m_tiles():
 
 
 @pytest.mark.parametrize("T,H,hc", [(128, 256, 4), (300, 256, 4), (1, 256, 4), (129, 512, 2), (257, 256, 1),
-                                    (2100, 256, 4)])
+                                    (1537, 256, 4), (1600, 512, 2), (2100, 256, 4)])
 def test_project_gate_fused(T, H, hc):
-    """Fused projection + gate + residual against the oracle and against the unfused kernels."""
+    """engram_project_gate against the oracle and against the unfused kernels.
+
+    Up to 1536 tokens the entry point runs the two-kernel path in its
+    workspace; from 1537 tokens on (ragged: 6 pair blocks + 1 row) the fused
+    cooperative kernel."""
     e, w, h, qw, kw = _inputs(T, H, hc, seed=1000 + T)
     mask = np.zeros(T, dtype=bool)
     mask[5::11] = True
