@@ -19,7 +19,8 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "EngramError", "Layout", "build_layout", "engram_hash", "engram_hash_step", "engram_gather_dequant",
+    "EngramError", "Layout", "build_layout", "engram_hash", "engram_hash_all_layers", "engram_hash_step",
+    "engram_gather_dequant",
     "engram_pack_wkv", "engram_project", "engram_gate_add", "engram_fill_synthetic_table",
     "engram_selftest_mod", "engram_project_gate", "project_gate_workspace", "partials_shape", "EngramLayer",
     "library_path", "ST_BAD_TOKEN", "ST_BAD_ROW", "ST_BAD_SLOT", "ST_TIMEOUT", "DEAD", "ROW_BYTES",
@@ -100,6 +101,7 @@ _SIGS = {
     "engram_selftest_mod": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _P],
     "engram_project_gate": [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _P, _P, _F32, _F32, _F32, _P, _P,
                             ctypes.c_size_t, _P, _P],
+    "engram_hash_all_layers": [ctypes.POINTER(_Layout), _P, _I64, _P, _I32, _P, _I64, _P, _P, _P, _P, _P],
 }
 
 
@@ -276,6 +278,32 @@ def engram_hash(layout: Layout, layer: int, raw_ids: torch.Tensor, cu_seqlens: t
     _check(L.engram_hash(layout.ref, layer, _ptr(raw_ids), T, _ptr(cu_seqlens), n_seqs, _ptr(token_map),
                          token_map.numel(), _ptr(hist), _ptr(row_ids), _ptr(mask), _ptr(status), _stream(dev)),
            "engram_hash")
+    return row_ids, mask
+
+
+def engram_hash_all_layers(layout: Layout, raw_ids: torch.Tensor, cu_seqlens: torch.Tensor,
+                           token_map: torch.Tensor, hist: Optional[torch.Tensor] = None,
+                           row_ids: Optional[torch.Tensor] = None, mask: Optional[torch.Tensor] = None,
+                           status: Optional[torch.Tensor] = None):
+    """Prefill hash of every layer; returns (row_ids int32 [n_layers][T][n_cols], mask uint8 [T])."""
+    L = _load()
+    dev = raw_ids.device
+    T = raw_ids.numel()
+    n_seqs = cu_seqlens.numel() - 1
+    _need(raw_ids, "raw_ids", torch.int32)
+    _need(cu_seqlens, "cu_seqlens", torch.int64, dev)
+    _need(token_map, "token_map", torch.int32, dev)
+    if hist is not None:
+        _need(hist, "hist", torch.int32, dev, n_seqs * (layout.max_ngram - 1))
+    if row_ids is None:
+        row_ids = torch.empty((layout.n_layers, T, layout.n_cols), dtype=torch.int32, device=dev)
+    if mask is None:
+        mask = torch.empty(T, dtype=torch.uint8, device=dev)
+    _need(row_ids, "row_ids", torch.int32, dev, layout.n_layers * T * layout.n_cols)
+    _need(mask, "mask", torch.uint8, dev, T)
+    _check(L.engram_hash_all_layers(layout.ref, _ptr(raw_ids), T, _ptr(cu_seqlens), n_seqs, _ptr(token_map),
+                                    token_map.numel(), _ptr(hist), _ptr(row_ids), _ptr(mask), _ptr(status),
+                                    _stream(dev)), "engram_hash_all_layers")
     return row_ids, mask
 
 

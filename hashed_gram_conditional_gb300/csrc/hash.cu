@@ -169,6 +169,46 @@ __global__ void __launch_bounds__(256) hash_prefill_kernel(
   }
 }
 
+// Every Engram layer of the layout in one pass over the tokens: the window
+// (token map, history, pad, DEAD cascade) does not depend on the layer, only
+// the multipliers, primes and offsets do ([P-O1] §2.4: the indices depend
+// only on the token ids, so all layers are hashed before the layer loop).
+struct HashConstsAll {
+  HashConsts l[ENGRAM_MAX_LAYERS];
+  int32_t n_layers;
+};
+
+__global__ void __launch_bounds__(256) hash_all_layers_kernel(
+    HashConstsAll ca, const int32_t* __restrict__ raw, int64_t n_tokens, const int64_t* __restrict__ cu,
+    int32_t n_seqs, const int32_t* __restrict__ tmap, const int32_t* __restrict__ hist,
+    int32_t* __restrict__ rows, uint8_t* __restrict__ mask, int32_t* status) {
+  const HashConsts& c = ca.l[0];
+  const uint32_t lane = lane_id();
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  const int depth = c.max_ngram - 1;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; t < n_tokens;
+       t += warps) {
+    int lo = 0, hi = n_seqs - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    const int64_t start = __ldg(cu + lo);
+    int32_t slot = c.pad_id;
+    if (lane < static_cast<uint32_t>(c.max_ngram)) {
+      const int64_t src = t - static_cast<int64_t>(lane);
+      if (src >= start) {
+        slot = compress_id(__ldg(raw + src), tmap, c, status);
+      } else if (hist != nullptr) {
+        const int64_t hidx = static_cast<int64_t>(lane) - 1 - (t - start);
+        slot = check_hist(__ldg(hist + static_cast<int64_t>(lo) * depth + hidx), c, status);
+      }
+    }
+    for (int li = 0; li < ca.n_layers; ++li)
+      hash_window(slot, ca.l[li], rows + (static_cast<int64_t>(li) * n_tokens + t) * c.n_cols, mask + t, false);
+  }
+}
+
 // History after a chunk: the last `depth` compressed ids of each sequence,
 // most recent first, falling back to the previous history for short chunks.
 // One thread per sequence reads all it needs before writing its own row.
@@ -311,4 +351,38 @@ extern "C" int engram_selftest_mod(const engram_layout* layout, int32_t layer, c
   selftest_mod_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, as_stream(stream)>>>(c, x_d, n,
                                                                                             out_d);
   return check_launch("selftest_mod_kernel");
+}
+
+extern "C" int engram_hash_all_layers(const engram_layout* layout, const int32_t* raw_ids_d, int64_t n_tokens,
+                                      const int64_t* cu_seqlens_d, int32_t n_seqs, const int32_t* token_map_d,
+                                      int64_t vocab_raw, int32_t* hist_d, int32_t* row_ids_d, uint8_t* mask_d,
+                                      int32_t* status_d, void* stream) {
+  if (layout == nullptr) return fail(ENGRAM_E_INVALID, "null layout");
+  HashConstsAll ca;
+  ca.n_layers = layout->n_layers;
+  for (int li = 0; li < layout->n_layers; ++li) {
+    int rc = make_consts(layout, li, vocab_raw, &ca.l[li]);
+    if (rc) return rc;
+  }
+  if (n_tokens < 0 || n_seqs < 1) return fail(ENGRAM_E_INVALID, "n_tokens < 0 or n_seqs < 1");
+  if (n_tokens == 0 && hist_d == nullptr) return ENGRAM_OK;
+  if (!cu_seqlens_d || !token_map_d || (n_tokens > 0 && (!raw_ids_d || !row_ids_d || !mask_d)))
+    return fail(ENGRAM_E_INVALID, "null device pointer");
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  cudaStream_t st = as_stream(stream);
+  if (n_tokens > 0) {
+    const int64_t want = (n_tokens + 7) / 8;
+    const int blocks = static_cast<int>(want < int64_t(sms) * 16 ? want : int64_t(sms) * 16);
+    hash_all_layers_kernel<<<blocks, 256, 0, st>>>(ca, raw_ids_d, n_tokens, cu_seqlens_d, n_seqs, token_map_d,
+                                                   hist_d, row_ids_d, mask_d, status_d);
+    if ((rc = check_launch("hash_all_layers_kernel"))) return rc;
+  }
+  if (hist_d != nullptr) {
+    hash_commit_kernel<<<(n_seqs + 127) / 128, 128, 0, st>>>(ca.l[0], raw_ids_d, cu_seqlens_d, n_seqs,
+                                                            token_map_d, hist_d, status_d);
+    if ((rc = check_launch("hash_commit_kernel"))) return rc;
+  }
+  return ENGRAM_OK;
 }

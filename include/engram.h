@@ -171,6 +171,16 @@ int engram_hash(const engram_layout* layout, int32_t layer, const int32_t* raw_i
                 const int32_t* token_map_d, int64_t vocab_raw, int32_t* hist_d,
                 int32_t* row_ids_d, uint8_t* mask_d, int32_t* status_d, void* stream);
 
+/* engram_hash for every layer of the layout in one launch ([P-O1] §2.4: the
+ * row ids depend only on the token ids, so serving code hashes all Engram
+ * layers before the layer loop).  The window and the history are shared by
+ * the layers; row_ids_d is int32 [n_layers][n_tokens][n_cols] (layer-major),
+ * mask_d and hist_d as engram_hash (hist_d advanced once). */
+int engram_hash_all_layers(const engram_layout* layout, const int32_t* raw_ids_d, int64_t n_tokens,
+                           const int64_t* cu_seqlens_d, int32_t n_seqs, const int32_t* token_map_d,
+                           int64_t vocab_raw, int32_t* hist_d, int32_t* row_ids_d, uint8_t* mask_d,
+                           int32_t* status_d, void* stream);
+
 /* One decode step: one new raw id per batch entry, hashed against the
  * sequence's rolling history and committed in the same launch ([P-O1] §4.4;
  * [P-DS4] §布局与哈希探测: the hash state is the last 3 ids and a copy of it is
