@@ -14,6 +14,10 @@ step, outside the events.  Under torchrun every rank runs its own batch (no
 collective on the data path, weak scaling) and the slowest rank's time is
 used.  ``--impl reference`` times the CPU oracle on a bounded sample of the
 same workload instead (rank 0 only).
+
+Side phases, reported next to the headline: hash + gather on the 65,536-token
+microbench batch, decode steps, and the same table kept in pinned host memory
+(zero-copy gather over NVLink-C2C, and the prefetch pipeline).
 """
 from __future__ import annotations
 
@@ -47,6 +51,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--micro-steps", type=int, default=30, help="steps of the hash+gather microbench phase")
     p.add_argument("--decode-steps", type=int, default=200, help="steps of the decode phase")
+    p.add_argument("--host-steps", type=int, default=20,
+                   help="steps of the host-resident table phase (0 skips it and its pinned allocation)")
     p.add_argument("--cpu-sample", type=int, default=8192, help="tokens of the oracle CPU baseline sample")
     p.add_argument("--ref-sample", type=int, default=128, help="tokens per reference-arm step")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -305,6 +311,8 @@ def run_ours(args, rank, world, local):
 
     micro = microbench(args, w, inp, layer, flush, dev) if args.micro_steps > 0 else None
     dec = decode_bench(args, w, inp, layer, flush, dev) if args.decode_steps > 0 else None
+    host = host_table_bench(args, w, inp, layer, flush, dev, statistics.mean(step_ms)) \
+        if args.host_steps > 0 else None
 
     if rank != 0:
         return None
@@ -359,6 +367,7 @@ def run_ours(args, rank, world, local):
         "roofline_gather": roof_g,
         "microbench_hash_gather": micro,
         "decode_step": dec,
+        "host_table": host,
         "gpu_launches": args.steps * 4,
         "clocks": clocks,
         "e2e": e2e,
@@ -469,6 +478,105 @@ def decode_bench(args, w, inp, layer, flush, dev):
             "hash_step_ms": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
             "gather_ms": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs),
             "project_gate_ms": proj * 1e3, "wkv_gbs": wkv_bytes / proj / 1e9}
+
+
+def host_table_bench(args, w, inp, layer, flush, dev, device_step_ms):
+    """The same table in pinned host memory (Grace LPDDR).
+
+    (a) zero-copy: the gather kernel reads the rows over NVLink-C2C;
+    (b) prefetch (``EngramLayer.prefetch``): the hash on the compute stream,
+        then on a copy stream the row ids go to the host, host threads copy the
+        rows into pinned staging, one DMA moves them to HBM and they are
+        dequantised; timed alone, then double-buffered so that fetching batch
+        k+1 runs while batch k is projected.
+    Four batches of the workload's shape (different seeds) rotate, so the rows
+    gathered by the host do not stay in its caches from one step to the next.
+    """
+    import torch
+    import hashed_gram_conditional_gb300 as eg
+    from workloads import prefill_batch
+
+    total = layer.total_rows
+    t0 = time.perf_counter()
+    try:
+        host = torch.empty(total * eg.ROW_BYTES, dtype=torch.uint8, pin_memory=True)
+    except RuntimeError as ex:
+        return {"skipped": f"pinned host table of {total * eg.ROW_BYTES / 1e9:.2f} GB unavailable: {ex}"}
+    pin_s = time.perf_counter() - t0
+    eg.engram_fill_synthetic_table(host, total, w.seed, dev)
+    torch.cuda.synchronize()
+    hl = eg.EngramLayer(layer.layout, layer.layer, host, layer.token_map, layer.wkv_packed, layer.q_w, layer.k_w)
+    n = args.host_steps
+    batches = [prefill_batch(w, seed=w.seed + 1000 + i) for i in range(4)]
+    T = len(batches[0].raw_ids)
+    raws = [torch.from_numpy(b.raw_ids).to(dev) for b in batches]
+    cus = [torch.from_numpy(b.cu_seqlens).to(dev) for b in batches]
+    C = layer.layout.n_cols
+    rows = torch.empty((T, C), dtype=torch.int32, device=dev)
+    e = torch.empty((T, C * 256), dtype=torch.bfloat16, device=dev)
+    h = inp["bf16"](inp["h_bits"][:T])
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    main = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+    row_bytes = T * C * eg.ROW_BYTES
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    # (a) zero-copy gather over NVLink-C2C
+    zc = []
+    for k in range(n + 3):
+        eg.engram_hash(layer.layout, 0, raws[k % 4], cus[k % 4], layer.token_map, None, rows, None)
+        flush.zero_()
+        ev[0].record(main)
+        eg.engram_gather_dequant(host, total, rows, e, status)
+        ev[1].record(main)
+        ev[1].synchronize()
+        if k >= 3:
+            zc.append(ev[0].elapsed_time(ev[1]))
+
+    # (b1) the prefetch alone: from the hash to the rows being ready
+    fe, bad = [], 0
+    for k in range(n + 3):
+        ev[0].record(main)
+        pf = hl.prefetch(raws[k % 4], cus[k % 4], status=status, copy_stream=side)
+        main.wait_event(pf.ready)
+        ev[1].record(main)
+        ev[1].synchronize()
+        bad += pf.bad_rows
+        hl.prefill_prefetched(pf, h, status)
+        if k >= 3:
+            fe.append(ev[0].elapsed_time(ev[1]))
+    torch.cuda.synchronize()
+
+    # (b2) double-buffered: the fetch of batch k+1 overlaps the projection of batch k
+    def pipeline(steps):
+        pf = hl.prefetch(raws[0], cus[0], status=status, copy_stream=side)
+        for k in range(steps):
+            nxt = hl.prefetch(raws[(k + 1) % 4], cus[(k + 1) % 4], status=status, copy_stream=side) \
+                if k + 1 < steps else None
+            hl.prefill_prefetched(pf, h, status)
+            pf = nxt
+
+    pipeline(3)
+    flush.zero_()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ev[0].record(main)
+    pipeline(n)
+    ev[1].record(main)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    pipe_ms = ev[0].elapsed_time(ev[1]) / n
+    zc_ms, fetch_ms = statistics.mean(zc), statistics.mean(fe)
+    return {"workload": f"{w.name}: 4 rotating batches of {T} tokens, {total * eg.ROW_BYTES / 1e9:.2f} GB table "
+                        "in pinned host memory", "steps": n, "pin_alloc_s": pin_s,
+            "zero_copy_gather_ms": zc_ms, "zero_copy_row_gbs": row_bytes / zc_ms / 1e6,
+            "prefetch_ms": fetch_ms, "prefetch_row_gbs": row_bytes / fetch_ms / 1e6,
+            "pipelined_step_ms": pipe_ms, "pipelined_tokens_per_s": T / pipe_ms * 1e3,
+            "pipelined_wall_tokens_per_s": T * n / wall,
+            "device_table_step_ms": device_step_ms,
+            "host_threads": int(os.environ.get("OMP_NUM_THREADS", "0")) or os.cpu_count(),
+            "bad_rows": bad, "device_status": int(status.item()), "row_bytes_per_step": row_bytes,
+            "note": "L2 flushed before each zero-copy gather; the pipelined steps run back to back"}
 
 
 # ------------------------------------------------------------------------- oracle timing

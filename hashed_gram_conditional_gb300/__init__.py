@@ -20,7 +20,7 @@ import torch
 
 __all__ = [
     "EngramError", "Layout", "build_layout", "engram_hash", "engram_hash_all_layers", "engram_hash_step",
-    "engram_gather_dequant",
+    "engram_gather_dequant", "engram_dequant_rows", "engram_host_gather", "engram_host_gather_async",
     "engram_pack_wkv", "engram_project", "engram_gate_add", "engram_fill_synthetic_table",
     "engram_selftest_mod", "engram_project_gate", "project_gate_workspace", "partials_shape", "EngramLayer",
     "library_path", "ST_BAD_TOKEN", "ST_BAD_ROW", "ST_BAD_SLOT", "ST_TIMEOUT", "DEAD", "ROW_BYTES",
@@ -102,6 +102,9 @@ _SIGS = {
     "engram_project_gate": [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _P, _P, _F32, _F32, _F32, _P, _P,
                             ctypes.c_size_t, _P, _P],
     "engram_hash_all_layers": [ctypes.POINTER(_Layout), _P, _I64, _P, _I32, _P, _I64, _P, _P, _P, _P, _P],
+    "engram_dequant_rows": [_P, _I64, _I64, _I32, _P, _P, _P],
+    "engram_host_gather": [_P, _I64, _P, _I64, _P, _I32, _P],
+    "engram_host_gather_async": [_P, _I64, _P, _I64, _P, _I32, _P, _P],
 }
 
 
@@ -338,7 +341,10 @@ def engram_gather_dequant(table: torch.Tensor, total_rows: int, row_ids: torch.T
     """Gather and dequantise: returns e bf16 [T][n_cols*256]."""
     L = _load()
     dev = row_ids.device
-    _need(table, "table", torch.uint8, dev)
+    if table.is_cuda:
+        _need(table, "table", torch.uint8, dev)
+    elif not (table.dtype == torch.uint8 and table.is_pinned() and table.is_contiguous()):
+        raise ValueError("a host table must be a contiguous pinned uint8 tensor (read over NVLink-C2C)")
     _need(row_ids, "row_ids", torch.int32)
     T, C = row_ids.shape
     if e is None:
@@ -347,6 +353,59 @@ def engram_gather_dequant(table: torch.Tensor, total_rows: int, row_ids: torch.T
     _check(L.engram_gather_dequant(_ptr(table), total_rows, table.numel(), _ptr(row_ids), T, C, _ptr(e),
                                    _ptr(status), _stream(dev)), "engram_gather_dequant")
     return e
+
+
+def engram_dequant_rows(rows: torch.Tensor, n_cols: int, e: Optional[torch.Tensor] = None,
+                        status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Dequantise contiguous device rows uint8 [n][264] -> e bf16 [n/n_cols][n_cols*256]."""
+    L = _load()
+    dev = rows.device
+    _need(rows, "rows", torch.uint8)
+    n = rows.numel() // ROW_BYTES
+    if e is None:
+        e = torch.empty((n // n_cols, n_cols * HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    _need(e, "e", torch.bfloat16, dev, n * HEAD_DIM)
+    _check(L.engram_dequant_rows(_ptr(rows), n, rows.numel(), n_cols, _ptr(e), _ptr(status), _stream(dev)),
+           "engram_dequant_rows")
+    return e
+
+
+def _host_ptr(a):
+    """Address of a host buffer: a CPU torch tensor or a numpy array (contiguous)."""
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda or not a.is_contiguous():
+            raise ValueError("host buffers must be contiguous CPU tensors")
+        return ctypes.c_void_p(a.data_ptr())
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("host buffers must be C-contiguous")
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def engram_host_gather(table, total_rows: int, row_ids, staging, n_threads: int = 0) -> int:
+    """Copy table rows row_ids (host) into staging (host); returns the count of out-of-range ids."""
+    L = _load()
+    n = (row_ids.numel() if isinstance(row_ids, torch.Tensor) else row_ids.size)
+    nbytes = staging.numel() if isinstance(staging, torch.Tensor) else staging.nbytes
+    if nbytes < n * ROW_BYTES:
+        raise ValueError("staging buffer too small")
+    bad = ctypes.c_int64(0)
+    _check(L.engram_host_gather(_host_ptr(table), total_rows, _host_ptr(row_ids), n, _host_ptr(staging), n_threads,
+                                ctypes.byref(bad)), "engram_host_gather")
+    return bad.value
+
+
+def engram_host_gather_async(table: torch.Tensor, total_rows: int, row_ids: torch.Tensor, staging: torch.Tensor,
+                             bad_rows: torch.Tensor, stream: torch.cuda.Stream, n_threads: int = 0):
+    """Enqueue the host gather on `stream` (after work already on it); bad_rows: int64 CPU tensor [1]."""
+    L = _load()
+    if bad_rows.dtype != torch.int64 or bad_rows.is_cuda:
+        raise TypeError("bad_rows must be a CPU int64 tensor")
+    n = row_ids.numel()
+    if staging.numel() < n * ROW_BYTES:
+        raise ValueError("staging buffer too small")
+    _check(L.engram_host_gather_async(_host_ptr(table), total_rows, _host_ptr(row_ids), n, _host_ptr(staging),
+                                      n_threads, ctypes.c_void_p(bad_rows.data_ptr()),
+                                      ctypes.c_void_p(stream.cuda_stream)), "engram_host_gather_async")
 
 
 def engram_pack_wkv(wkv: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -449,12 +508,21 @@ def engram_project_gate(e: torch.Tensor, wkv_packed: torch.Tensor, h: torch.Tens
     return gate_out
 
 
-def engram_fill_synthetic_table(table: torch.Tensor, n_rows: int, seed: int) -> torch.Tensor:
+def engram_fill_synthetic_table(table: torch.Tensor, n_rows: int, seed: int,
+                                device: Optional[torch.device] = None) -> torch.Tensor:
+    """Fill a device table, or a pinned host table (written by the kernel through
+    its mapped address), with the seeded synthetic rows."""
     L = _load()
-    _need(table, "table", torch.uint8)
+    if table.is_cuda:
+        _need(table, "table", torch.uint8)
+        device = table.device
+    elif not (table.dtype == torch.uint8 and table.is_pinned() and table.is_contiguous()):
+        raise ValueError("a host table must be a contiguous pinned uint8 tensor")
+    elif device is None:
+        device = torch.device("cuda", torch.cuda.current_device())
     if table.numel() < n_rows * ROW_BYTES:
         raise ValueError("table too small")
-    _check(L.engram_fill_synthetic_table(_ptr(table), n_rows, seed, _stream(table.device)),
+    _check(L.engram_fill_synthetic_table(_ptr(table), n_rows, seed, _stream(device)),
            "engram_fill_synthetic_table")
     return table
 
@@ -478,6 +546,12 @@ class EngramLayer:
     ``prefill`` runs hash -> gather -> fused project/gate on the current
     stream and updates the residual ``h`` in place (``fused=False`` runs the
     projection and the gate kernel separately).
+
+    The table may be a device tensor or a pinned host tensor (Grace memory).
+    ``prefetch`` + ``prefill_prefetched`` split the layer at the point the
+    Engram pages use for offloading: the rows a batch needs depend only on its
+    token ids, so they can be fetched while earlier work runs, and the layer
+    later only waits for them.
     """
 
     def __init__(self, layout: Layout, layer: int, table: torch.Tensor, token_map: torch.Tensor,
@@ -492,6 +566,8 @@ class EngramLayer:
         self.total_rows = layout.total_rows(layer)
         self.fused = fused
         self._ws = {}
+        self._pf = {}          # T -> [two prefetch slots]
+        self._pf_next = 0
 
     def _buffers(self, T: int, device):
         key = (T, str(device))
@@ -517,6 +593,82 @@ class EngramLayer:
         self._gate(b, h, status, gate_out)
         return b
 
+    def _prefetch_slot(self, T: int, device):
+        key = (T, str(device))
+        if key not in self._pf:
+            C = self.layout.n_cols
+            host = not self.table.is_cuda
+            self._pf = {key: [dict(
+                rows=torch.empty((T, C), dtype=torch.int32, device=device),
+                mask=torch.empty(T, dtype=torch.uint8, device=device),
+                e=torch.empty((T, C * HEAD_DIM), dtype=torch.bfloat16, device=device),
+                rows_h=torch.empty((T, C), dtype=torch.int32, pin_memory=True) if host else None,
+                staging=torch.empty(T * C * ROW_BYTES, dtype=torch.uint8, pin_memory=True) if host else None,
+                staged=torch.empty(T * C * ROW_BYTES, dtype=torch.uint8, device=device) if host else None,
+                bad=torch.zeros(1, dtype=torch.int64),
+                consumed=torch.cuda.Event(), busy=False) for _ in range(2)]}
+        slot = self._pf[key][self._pf_next]
+        if slot["busy"]:
+            raise EngramError("two prefetched batches are already waiting; run prefill_prefetched first")
+        self._pf_next ^= 1
+        return slot
+
+    def prefetch(self, raw_ids: torch.Tensor, cu_seqlens: torch.Tensor, hist: Optional[torch.Tensor] = None,
+                 status: Optional[torch.Tensor] = None, copy_stream: Optional[torch.cuda.Stream] = None,
+                 n_threads: int = 0) -> "Prefetched":
+        """Start fetching the rows of a prefill batch.
+
+        The hash runs on the current stream (a few microseconds: enqueue it
+        ahead of the work the fetch should overlap, since it needs SMs).  With
+        a pinned host table the rest runs on ``copy_stream``: the row ids go to
+        the host, ``n_threads`` host threads gather the 264-byte rows into a
+        pinned staging buffer, one DMA moves it to the device and the rows are
+        dequantised there.  With a device table the gather follows the hash on
+        the current stream.  At most two batches may be waiting at a time.
+        """
+        dev = raw_ids.device
+        T = raw_ids.numel()
+        slot = self._prefetch_slot(T, dev)
+        cur = torch.cuda.current_stream(dev)
+        cur.wait_event(slot["consumed"])
+        engram_hash(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, hist, slot["rows"], slot["mask"],
+                    status)
+        ready = torch.cuda.Event()
+        if self.table.is_cuda:
+            engram_gather_dequant(self.table, self.total_rows, slot["rows"], slot["e"], status)
+            ready.record(cur)
+        else:
+            cs = copy_stream if copy_stream is not None else torch.cuda.Stream(dev)
+            hashed = torch.cuda.Event()
+            hashed.record(cur)
+            cs.wait_event(hashed)
+            with torch.cuda.stream(cs):
+                slot["rows_h"].copy_(slot["rows"], non_blocking=True)
+                engram_host_gather_async(self.table, self.total_rows, slot["rows_h"], slot["staging"], slot["bad"],
+                                         cs, n_threads)
+                slot["staged"].copy_(slot["staging"], non_blocking=True)
+                engram_dequant_rows(slot["staged"], self.layout.n_cols, slot["e"], status)
+                ready.record(cs)
+        slot["busy"] = True
+        return Prefetched(slot, T, ready)
+
+    def prefill_prefetched(self, pf: "Prefetched", h: torch.Tensor, status: Optional[torch.Tensor] = None,
+                           gate_out: Optional[torch.Tensor] = None):
+        """The projection, gate and residual update of a prefetched batch on the
+        current stream, after its rows are ready.  ``pf.bad_rows`` (host) holds
+        the count of out-of-range row ids once this stream has passed it."""
+        if not pf.slot["busy"]:
+            raise EngramError("this prefetched batch was already consumed")
+        dev = h.device
+        cur = torch.cuda.current_stream(dev)
+        cur.wait_event(pf.ready)
+        b = dict(self._buffers(pf.T, dev))
+        b.update(e=pf.slot["e"], mask=pf.slot["mask"], rows=pf.slot["rows"])
+        self._gate(b, h, status, gate_out)
+        pf.slot["consumed"].record(cur)
+        pf.slot["busy"] = False
+        return b
+
     def decode(self, raw_ids: torch.Tensor, slots: torch.Tensor, hist: torch.Tensor, h: torch.Tensor,
                status: Optional[torch.Tensor] = None, gate_out: Optional[torch.Tensor] = None):
         B = raw_ids.numel()
@@ -534,3 +686,26 @@ class EngramLayer:
         else:
             engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
             engram_gate_add(b["partials"], b["v"], h, b["mask"], self.eps, self.clamp, self.score_scale, gate_out)
+
+
+class Prefetched:
+    """A batch whose rows are being fetched by ``EngramLayer.prefetch``."""
+
+    def __init__(self, slot: dict, T: int, ready: torch.cuda.Event):
+        self.slot, self.T, self.ready = slot, T, ready
+
+    @property
+    def e(self) -> torch.Tensor:
+        return self.slot["e"]
+
+    @property
+    def mask(self) -> torch.Tensor:
+        return self.slot["mask"]
+
+    @property
+    def row_ids(self) -> torch.Tensor:
+        return self.slot["rows"]
+
+    @property
+    def bad_rows(self) -> int:
+        return int(self.slot["bad"].item())

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_dequant_kernel(GatherAr
     int32_t r = -1;
     bool valid = false;
     if (lane < static_cast<uint32_t>(n_cols)) {
-      r = __ldg(a.rows + t * n_cols + lane);
+      r = a.rows != nullptr ? __ldg(a.rows + t * n_cols + lane) : static_cast<int32_t>(t * n_cols + lane);
       valid = r >= 0 && static_cast<int64_t>(r) < a.total_rows;
       if (!valid && a.status) atomicOr(a.status, static_cast<int>(ENGRAM_ST_BAD_ROW));
     }
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArg
     int32_t r = -1;
     bool valid = false;
     if (lane < static_cast<uint32_t>(n_cols)) {
-      r = __ldg(a.rows + t * n_cols + lane);
+      r = a.rows != nullptr ? __ldg(a.rows + t * n_cols + lane) : static_cast<int32_t>(t * n_cols + lane);
       valid = r >= 0 && static_cast<int64_t>(r) < a.total_rows;
       if (!valid && a.status) atomicOr(a.status, static_cast<int>(ENGRAM_ST_BAD_ROW));
     }
@@ -356,7 +356,7 @@ extern "C" int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows,
   if (table_bytes < total_rows * kRowBytes)
     return fail(ENGRAM_E_SHAPE, "table_bytes %lld < total_rows * 264", (long long)table_bytes);
   if (n_tokens == 0) return ENGRAM_OK;
-  if (!table_d || !row_ids_d || !e_d) return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (!table_d || !e_d) return fail(ENGRAM_E_INVALID, "null device pointer");  // row_ids_d NULL: identity ids
   if (!aligned(table_d, 16) || !aligned(e_d, 16))
     return fail(ENGRAM_E_ALIGN, "table and e must be 16-byte aligned");
   int sms = 0;
@@ -381,6 +381,15 @@ extern "C" int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows,
   }
   gather_dequant_kernel<<<blocks, kWarps * 32, smem, as_stream(stream)>>>(a);
   return check_launch("gather_dequant_kernel");
+}
+
+extern "C" int engram_dequant_rows(const uint8_t* rows_d, int64_t n_rows, int64_t rows_bytes, int32_t n_cols,
+                                  uint16_t* e_d, int32_t* status_d, void* stream) {
+  if (n_cols < 1 || n_cols > ENGRAM_MAX_COLS) return fail(ENGRAM_E_SHAPE, "n_cols %d", n_cols);
+  if (n_rows < 0 || n_rows % n_cols != 0) return fail(ENGRAM_E_SHAPE, "n_rows must be a multiple of n_cols");
+  if (n_rows >= (int64_t(1) << 31)) return fail(ENGRAM_E_RANGE, "too many rows");
+  // the gather kernel with row ids t*n_cols + j over the contiguous rows
+  return engram_gather_dequant(rows_d, n_rows, rows_bytes, nullptr, n_rows / n_cols, n_cols, e_d, status_d, stream);
 }
 
 extern "C" int engram_fill_synthetic_table(uint8_t* table_d, int64_t n_rows, uint64_t seed,

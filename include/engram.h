@@ -211,15 +211,55 @@ int engram_hash_step(const engram_layout* layout, int32_t layer, const int32_t* 
  * E4M3 is OCP FP8 E4M3 (no infinities, 0x7F/0xFF NaN), E8M0 is the OCP scale
  * (0xFF NaN).  The result is the exact product rounded once to bf16.
  *
- *   table_d      uint8 [total_rows][264], 16-byte aligned (ENGRAM_E_ALIGN)
+ *   table_d      uint8 [total_rows][264], 16-byte aligned (ENGRAM_E_ALIGN);
+ *                device memory, or pinned / ATS-visible host memory that the
+ *                kernel reads over NVLink-C2C
  *   table_bytes  size of the table allocation in bytes, >= total_rows * 264
- *   row_ids_d    int32 [n_tokens][n_cols]
+ *   row_ids_d    int32 [n_tokens][n_cols], or NULL for the ids t*n_cols + j
  *   e_d          bf16 [n_tokens][n_cols*256] out, 16-byte aligned
  * A row id outside [0, total_rows) sets ENGRAM_ST_BAD_ROW and its 256 outputs
  * are +0. */
 int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows, int64_t table_bytes,
                           const int32_t* row_ids_d, int64_t n_tokens, int32_t n_cols,
                           uint16_t* e_d, int32_t* status_d, void* stream);
+
+/* Dequantise rows that already sit contiguously in device memory (e.g. after
+ * a host-side gather and one DMA): e_d[i/n_cols][256*(i%n_cols) + c] from
+ * row i of rows_d, for i < n_rows (a multiple of n_cols).  Same arithmetic as
+ * engram_gather_dequant.  rows_d is uint8 [n_rows][264], 16-byte aligned;
+ * rows_bytes is its allocation size (>= n_rows * 264). */
+int engram_dequant_rows(const uint8_t* rows_d, int64_t n_rows, int64_t rows_bytes, int32_t n_cols,
+                        uint16_t* e_d, int32_t* status_d, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Host-resident table (Grace memory)                                         */
+/* ------------------------------------------------------------------------ */
+
+/* The rows to fetch depend only on the token ids, so the table can live in
+ * host memory and be fetched while earlier layers compute ([P-V41]
+ * §"196B 参数怎么存、怎么取"; [P-O1] §4.1; [P-DETAIL] §8.2).  A pinned or
+ * ATS-visible host table can be passed directly to engram_gather_dequant
+ * (reads over NVLink-C2C).  Alternatively the rows are gathered by host
+ * threads into a contiguous staging buffer, moved by one DMA and
+ * dequantised with engram_dequant_rows:
+ *
+ * engram_host_gather copies row row_ids_h[i] of table_h (uint8 [total_rows]
+ * [264], host) to staging_h + 264 i for i < n_rows, with n_threads OpenMP
+ * threads (0: the OpenMP default).  Rows outside [0, total_rows) become 264
+ * zero bytes (they dequantise to +0) and are counted in *bad_rows (nullable).
+ * Runs on the calling thread; all pointers are host pointers. */
+int engram_host_gather(const uint8_t* table_h, int64_t total_rows, const int32_t* row_ids_h, int64_t n_rows,
+                       uint8_t* staging_h, int32_t n_threads, int64_t* bad_rows);
+
+/* engram_host_gather enqueued on `stream` with cudaLaunchHostFunc: it runs
+ * after the work already on the stream (for instance the device-to-host copy
+ * of row_ids_h) and before the work enqueued later (the host-to-device copy of
+ * staging_h), on CUDA's host-callback thread.  The buffers must stay valid
+ * until the stream reaches it; *bad_rows is written before later stream work
+ * starts (left untouched when n_rows == 0, which enqueues nothing). */
+int engram_host_gather_async(const uint8_t* table_h, int64_t total_rows, const int32_t* row_ids_h,
+                             int64_t n_rows, uint8_t* staging_h, int32_t n_threads, int64_t* bad_rows,
+                             void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* wkv projection with the gate reduction fused (stage 5a/5b)                */
@@ -363,7 +403,8 @@ int engram_project_gate_add_noalloc(const uint16_t* e_d, int64_t n_tokens, int64
  * starts at `seed`; weight bytes equal to an E4M3 NaN code (0x7F, 0xFF) are
  * replaced by byte ^ 1 and each scale byte b becomes 120 + (b mod 11).  This
  * is input generation for tests and benchmarks, not part of the method.
- *   table_d  uint8 [n_rows][264], 8-byte aligned */
+ *   table_d  uint8 [n_rows][264], 8-byte aligned; device memory or a pinned
+ *            (mapped) host buffer, which the kernel writes over NVLink-C2C */
 int engram_fill_synthetic_table(uint8_t* table_d, int64_t n_rows, uint64_t seed, void* stream);
 
 /* Diagnostic of the on-device modulo: out_d[i][j] = x_d[i] mod p_j + offset_j
