@@ -22,7 +22,8 @@ Modules
   hashing  token map, suffix windows with pad/DEAD, multiplicative-XOR mix, row ids, history
   dequant  E4M3 x E8M0 row decode, bf16 round-to-nearest-even
   gate     wkv projection, signed-sqrt sigmoid gate, gated residual add
-  pipeline the five stages composed
+  shortconv the original Engram's short causal convolution on the gated value
+  pipeline the five stages composed (with or without the short convolution)
 
 Parity status: every function is pinned by tests in tests/test_oracle_*.py
 except the multiplier generator, whose values cannot be pinned against a

@@ -13,7 +13,7 @@ from typing import Optional
 
 import numpy as np
 
-from . import dequant, gate, hashing
+from . import dequant, gate, hashing, shortconv
 from .layout import Layout
 
 
@@ -43,3 +43,31 @@ def layer_forward(layout: Layout, layer: int, raw_ids, cu_seqlens, token_map, ta
     g = gate.gate(h, k, q_w, k_w, mask, eps, clamp, score_scale)
     h_out = gate.residual(h, g, v, mask)
     return LayerResult(rows, mask, new_hist, e, g, v, h_out)
+
+
+@dataclasses.dataclass
+class ConvParams:
+    """The short convolution of the original Engram layer ([P-DETAIL] §4.2)."""
+    w: np.ndarray          # float64 [K][hc][H], w[k] multiplies the value k*dilation positions back
+    gamma: np.ndarray      # float64 [hc][H] RMSNorm weight
+    dilation: int
+    eps: float = 1e-6
+
+
+def layer_forward_conv(layout: Layout, layer: int, raw_ids, cu_seqlens, token_map, table_rows, wkv, h, q_w, k_w,
+                       conv: ConvParams, hist: Optional[np.ndarray] = None, conv_state=None, eps: float = 1e-6,
+                       clamp: float = 1e-6, score_scale=None):
+    """Prefill of the original Engram layer: the gated value is refined by the
+    short convolution and H <- bf16(H + V~ + SiLU(conv(RMSNorm(V~)))) at every
+    position ([P-DETAIL] §4.2 and the pseudo code of §五).
+
+    Returns (LayerResult with h_out of this variant, new conv state per sequence).
+    """
+    rows, mask, new_hist = hashing.hash_prefill(raw_ids, cu_seqlens, token_map, layout, layer, hist)
+    e = dequant.gather_dequant(rows, table_rows)
+    hc, H = h.shape[1], h.shape[2]
+    k, v = gate.split_kv(gate.project(e, wkv), H, hc)
+    g = gate.gate(h, k, q_w, k_w, mask, eps, clamp, score_scale)
+    y, state = shortconv.short_conv(shortconv.gated_value(g, v), cu_seqlens, conv.w, conv.gamma, conv.dilation,
+                                    conv.eps, conv_state)
+    return LayerResult(rows, mask, new_hist, e, g, v, shortconv.conv_residual(h, y)), state
