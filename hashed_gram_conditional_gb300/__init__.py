@@ -105,6 +105,8 @@ _SIGS = {
     "engram_dequant_rows": [_P, _I64, _I64, _I32, _P, _P, _P],
     "engram_host_gather": [_P, _I64, _P, _I64, _P, _I32, _P],
     "engram_host_gather_async": [_P, _I64, _P, _I64, _P, _I32, _P, _P],
+    "engram_short_conv_add": [_P, _P, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _I32, _I32, _F32, _P, _P,
+                              _I64, _P, ctypes.c_size_t, _P, _P],
 }
 
 
@@ -128,6 +130,8 @@ def _load():
         lib.engram_project_partials_bytes.argtypes = [_I64, _I32, _I32]
         lib.engram_project_gate_workspace_bytes.restype = ctypes.c_size_t
         lib.engram_project_gate_workspace_bytes.argtypes = [_I64, _I32, _I32]
+        lib.engram_short_conv_workspace_bytes.restype = ctypes.c_size_t
+        lib.engram_short_conv_workspace_bytes.argtypes = [_I64, _I32]
         lib.engram_layout_size.restype = ctypes.c_size_t
         lib.engram_layout_params_size.restype = ctypes.c_size_t
         if lib.engram_layout_size() != ctypes.sizeof(_Layout) or \
@@ -471,6 +475,74 @@ def engram_gate_add(partials: torch.Tensor, v: torch.Tensor, h: torch.Tensor, ma
     return gate_out
 
 
+def engram_gates(partials: torch.Tensor, n_tokens: int, hidden: int, hc: int, mask: Optional[torch.Tensor],
+                 eps: float = 1e-6, clamp: float = 1e-6, score_scale: Optional[float] = None,
+                 gate_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The gates alone (engram_gate_add without h): f32 [T][hc]."""
+    L = _load()
+    dev = partials.device
+    T = n_tokens
+    _need(partials, "partials", torch.float32, dev, T * hc * (hidden // 256) * 4)
+    if mask is not None:
+        _need(mask, "mask", torch.uint8, dev, T)
+    if gate_out is None:
+        gate_out = torch.empty((T, hc), dtype=torch.float32, device=dev)
+    _need(gate_out, "gate_out", torch.float32, dev, T * hc)
+    if score_scale is None:
+        score_scale = hidden ** -0.5
+    _check(L.engram_gate_add(_ptr(partials), None, None, _ptr(mask), T, hidden, hc, eps, clamp, score_scale,
+                             _ptr(gate_out), _stream(dev)), "engram_gate_add")
+    return gate_out
+
+
+def short_conv_workspace(n_tokens: int, hc: int, device) -> torch.Tensor:
+    n = _load().engram_short_conv_workspace_bytes(n_tokens, hc)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device)
+
+
+def engram_short_conv_add(gate: torch.Tensor, v: torch.Tensor, h: torch.Tensor, mask: Optional[torch.Tensor],
+                          conv_w: torch.Tensor, gamma: torch.Tensor, dilation: int, eps: float = 1e-6,
+                          cu_seqlens: Optional[torch.Tensor] = None, slots: Optional[torch.Tensor] = None,
+                          state: Optional[torch.Tensor] = None, state_head: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """h <- bf16(h + g*bf16(v) + SiLU(conv(RMSNorm(g*bf16(v))))) in place.
+
+    gate f32 [T][hc]; v bf16 [T][H]; h bf16 [T][hc][H]; conv_w f32 [K][hc][H];
+    gamma f32 [hc][H]; cu_seqlens int64 [S+1] (None: each position is its own
+    sequence); slots int32 [S]; state f32 [n_slots][(K-1)*dilation][hc][H] with
+    state_head int32 [n_slots], or None.
+    """
+    L = _load()
+    dev = h.device
+    _need(h, "h", torch.bfloat16)
+    T, hc, H = h.shape
+    _need(gate, "gate", torch.float32, dev, T * hc)
+    _need(v, "v", torch.bfloat16, dev, T * H)
+    if mask is not None:
+        _need(mask, "mask", torch.uint8, dev, T)
+    K = conv_w.shape[0]
+    _need(conv_w, "conv_w", torch.float32, dev, K * hc * H)
+    _need(gamma, "gamma", torch.float32, dev, hc * H)
+    n_seqs = T
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int64, dev)
+        n_seqs = cu_seqlens.numel() - 1
+    if slots is not None:
+        _need(slots, "slots", torch.int32, dev, n_seqs)
+    n_slots = 0
+    if state is not None:
+        n_slots = state.shape[0]
+        _need(state, "state", torch.float32, dev, n_slots * max((K - 1) * dilation, 1) * hc * H)
+        _need(state_head, "state_head", torch.int32, dev, n_slots)
+    if workspace is None:
+        workspace = short_conv_workspace(T, hc, dev)
+    _check(L.engram_short_conv_add(_ptr(gate), _ptr(v), _ptr(h), _ptr(mask), T, H, hc, _ptr(cu_seqlens), n_seqs,
+                                   _ptr(slots), _ptr(conv_w), _ptr(gamma), K, dilation, eps, _ptr(state),
+                                   _ptr(state_head), n_slots, _ptr(workspace), workspace.numel(), _ptr(status),
+                                   _stream(dev)), "engram_short_conv_add")
+    return h
+
+
 def project_gate_workspace(n_tokens: int, hidden: int, hc: int, device) -> torch.Tensor:
     """Workspace tensor for engram_project_gate (torch allocations are 256-byte aligned)."""
     n = _load().engram_project_gate_workspace_bytes(n_tokens, hidden, hc)
@@ -556,7 +628,9 @@ class EngramLayer:
 
     def __init__(self, layout: Layout, layer: int, table: torch.Tensor, token_map: torch.Tensor,
                  wkv_packed: torch.Tensor, q_w: torch.Tensor, k_w: torch.Tensor, eps: float = 1e-6,
-                 clamp: float = 1e-6, score_scale: Optional[float] = None, fused: bool = True):
+                 clamp: float = 1e-6, score_scale: Optional[float] = None, fused: bool = True,
+                 conv: Optional["ShortConv"] = None):
+        self.conv = conv
         self.layout, self.layer = layout, layer
         self.table, self.token_map = table, token_map
         self.wkv_packed, self.q_w, self.k_w = wkv_packed, q_w, k_w
@@ -579,18 +653,29 @@ class EngramLayer:
                 partials=torch.empty(partials_shape(T, self.hidden, self.hc), dtype=torch.float32, device=device),
                 v=torch.empty((T, self.hidden), dtype=torch.bfloat16, device=device),
                 work=project_gate_workspace(T, self.hidden, self.hc, device),
+                gate=torch.empty((T, self.hc), dtype=torch.float32, device=device),
+                conv_ws=short_conv_workspace(T, self.hc, device),
             )}
         return self._ws[key]
 
+    def new_conv_state(self, n_slots: int, device) -> tuple:
+        """A zeroed short-convolution state (ring, head) for n_slots sequences."""
+        c = self.conv
+        R = (c.w.shape[0] - 1) * c.dilation
+        return (torch.zeros((n_slots, max(R, 1), self.hc, self.hidden), dtype=torch.float32, device=device),
+                torch.zeros(n_slots, dtype=torch.int32, device=device))
+
     def prefill(self, raw_ids: torch.Tensor, cu_seqlens: torch.Tensor, h: torch.Tensor,
                 hist: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                gate_out: Optional[torch.Tensor] = None):
+                gate_out: Optional[torch.Tensor] = None, conv_state: Optional[tuple] = None):
+        """conv_state: (ring, head) from new_conv_state, one slot per sequence, for a
+        layer with the short convolution (None: zeros before every sequence)."""
         T = raw_ids.numel()
         b = self._buffers(T, raw_ids.device)
         engram_hash(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, hist, b["rows"], b["mask"],
                     status)
         engram_gather_dequant(self.table, self.total_rows, b["rows"], b["e"], status)
-        self._gate(b, h, status, gate_out)
+        self._gate(b, h, status, gate_out, cu_seqlens=cu_seqlens, conv_state=conv_state)
         return b
 
     def _prefetch_slot(self, T: int, device):
@@ -650,10 +735,10 @@ class EngramLayer:
                 engram_dequant_rows(slot["staged"], self.layout.n_cols, slot["e"], status)
                 ready.record(cs)
         slot["busy"] = True
-        return Prefetched(slot, T, ready)
+        return Prefetched(slot, T, ready, cu_seqlens)
 
     def prefill_prefetched(self, pf: "Prefetched", h: torch.Tensor, status: Optional[torch.Tensor] = None,
-                           gate_out: Optional[torch.Tensor] = None):
+                           gate_out: Optional[torch.Tensor] = None, conv_state: Optional[tuple] = None):
         """The projection, gate and residual update of a prefetched batch on the
         current stream, after its rows are ready.  ``pf.bad_rows`` (host) holds
         the count of out-of-range row ids once this stream has passed it."""
@@ -664,22 +749,34 @@ class EngramLayer:
         cur.wait_event(pf.ready)
         b = dict(self._buffers(pf.T, dev))
         b.update(e=pf.slot["e"], mask=pf.slot["mask"], rows=pf.slot["rows"])
-        self._gate(b, h, status, gate_out)
+        self._gate(b, h, status, gate_out, cu_seqlens=pf.cu_seqlens, conv_state=conv_state)
         pf.slot["consumed"].record(cur)
         pf.slot["busy"] = False
         return b
 
     def decode(self, raw_ids: torch.Tensor, slots: torch.Tensor, hist: torch.Tensor, h: torch.Tensor,
-               status: Optional[torch.Tensor] = None, gate_out: Optional[torch.Tensor] = None):
+               status: Optional[torch.Tensor] = None, gate_out: Optional[torch.Tensor] = None,
+               conv_state: Optional[tuple] = None):
         B = raw_ids.numel()
         b = self._buffers(B, raw_ids.device)
         engram_hash_step(self.layout, self.layer, raw_ids, slots, self.token_map, hist, b["rows"], b["mask"],
                          status)
         engram_gather_dequant(self.table, self.total_rows, b["rows"], b["e"], status)
-        self._gate(b, h, status, gate_out)
+        self._gate(b, h, status, gate_out, slots=slots, conv_state=conv_state)
         return b
 
-    def _gate(self, b, h, status, gate_out):
+    def _gate(self, b, h, status, gate_out, cu_seqlens=None, slots=None, conv_state=None):
+        if self.conv is not None:
+            # the original layer: gates, then the short convolution with the residual add
+            c = self.conv
+            T = h.shape[0]
+            engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
+            g = engram_gates(b["partials"], T, self.hidden, self.hc, b["mask"], self.eps, self.clamp,
+                             self.score_scale, gate_out if gate_out is not None else b["gate"])
+            state, head = conv_state if conv_state is not None else (None, None)
+            engram_short_conv_add(g, b["v"], h, b["mask"], c.w, c.gamma, c.dilation, c.eps, cu_seqlens,
+                                  slots if cu_seqlens is None else None, state, head, b["conv_ws"], status)
+            return
         if self.fused:
             engram_project_gate(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["mask"], self.eps, self.clamp,
                                 self.score_scale, gate_out, b["work"], status)
@@ -688,11 +785,21 @@ class EngramLayer:
             engram_gate_add(b["partials"], b["v"], h, b["mask"], self.eps, self.clamp, self.score_scale, gate_out)
 
 
+class ShortConv:
+    """Filters of the original Engram layer's short convolution: w f32
+    [K][hc][H] (w[k] multiplies the value k*dilation positions back), RMSNorm
+    weight gamma f32 [hc][H], dilation (the pages use the largest n-gram
+    order) and the RMSNorm eps."""
+
+    def __init__(self, w: torch.Tensor, gamma: torch.Tensor, dilation: int, eps: float = 1e-6):
+        self.w, self.gamma, self.dilation, self.eps = w, gamma, dilation, eps
+
+
 class Prefetched:
     """A batch whose rows are being fetched by ``EngramLayer.prefetch``."""
 
-    def __init__(self, slot: dict, T: int, ready: torch.cuda.Event):
-        self.slot, self.T, self.ready = slot, T, ready
+    def __init__(self, slot: dict, T: int, ready: torch.cuda.Event, cu_seqlens: torch.Tensor):
+        self.slot, self.T, self.ready, self.cu_seqlens = slot, T, ready, cu_seqlens
 
     @property
     def e(self) -> torch.Tensor:

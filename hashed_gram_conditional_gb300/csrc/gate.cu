@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(256) gate_add_kernel(
     for (int m = 0; m < kMaxHc; ++m) g[m] = (m < hc) ? gs[m] : 0.f;
     const uint4* vt = v + t * nvec;
     uint4* ht = h + t * static_cast<int64_t>(hc) * nvec;
-    for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+    for (int i = threadIdx.x; h != nullptr && i < nvec; i += blockDim.x) {  // no h: gates only
       const uint4 vv = vt[i];
 #pragma unroll
       for (int m = 0; m < kMaxHc; ++m) {
@@ -115,8 +115,10 @@ extern "C" int engram_gate_add(const float* partials_d, const uint16_t* v_d, uin
   if (hidden < 256 || hidden % 256 != 0) return fail(ENGRAM_E_SHAPE, "hidden %d % 256 != 0", hidden);
   if (hc < 1 || hc > kMaxHc) return fail(ENGRAM_E_SHAPE, "hc %d not in [1, %d]", hc, kMaxHc);
   if (n_tokens == 0) return ENGRAM_OK;
-  if (!partials_d || !v_d || !h_d) return fail(ENGRAM_E_INVALID, "null device pointer");
-  if (!aligned(partials_d, 16) || !aligned(v_d, 16) || !aligned(h_d, 16))
+  if (!partials_d) return fail(ENGRAM_E_INVALID, "null partials");
+  if (!h_d && !gate_out_d) return fail(ENGRAM_E_INVALID, "gates only (h = NULL) needs gate_out");
+  if (h_d && !v_d) return fail(ENGRAM_E_INVALID, "null v");
+  if (!aligned(partials_d, 16) || (h_d && (!aligned(v_d, 16) || !aligned(h_d, 16))))
     return fail(ENGRAM_E_ALIGN, "partials, v and h must be 16-byte aligned");
   int sms = 0;
   int rc = check_device(&sms);

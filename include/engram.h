@@ -319,10 +319,63 @@ int engram_project(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint1
  *   v_d          bf16 [n_tokens][hidden]
  *   h_d          bf16 [n_tokens][hc][hidden], updated in place, 16-byte aligned
  *   mask_d       uint8 [n_tokens], or NULL (no masked positions)
- *   gate_out_d   float32 [n_tokens][hc] out, or NULL */
+ *   gate_out_d   float32 [n_tokens][hc] out, or NULL
+ * With h_d = NULL only the gates are computed (gate_out_d required, v_d may
+ * be NULL): the first half of the short-convolution variant below. */
 int engram_gate_add(const float* partials_d, const uint16_t* v_d, uint16_t* h_d,
                     const uint8_t* mask_d, int64_t n_tokens, int32_t hidden, int32_t hc, float eps,
                     float clamp, float score_scale, float* gate_out_d, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Short causal convolution (the original Engram layer's stage 5c)            */
+/* ------------------------------------------------------------------------ */
+
+/* The original Engram layer refines the gated value before the residual add
+ * ([P-DETAIL] §4.2 and the pseudo code of §五; [P-V41] §"V4.1 相对原版的两处改动"
+ * names it as the step V4.1 dropped).  For every position t of a sequence and
+ * stream m, with V~ = g * bf16(v):
+ *   n_t = gamma[m] * V~_t / sqrt(mean_i(V~_t,i^2) + eps)         (RMSNorm)
+ *   c_t = sum_{k < kernel_size} w[k][m] * n_{t - k*dilation}     (depthwise, causal)
+ *   h_d[t][m][i] <- bf16_rne(h + (V~_t,i + SiLU(c_t,i)))         in fp32
+ * w[k] multiplies the value k*dilation positions back (a PyTorch Conv1d
+ * filter W[ch][0][j] with left padding maps to w[k] = W[..][K-1-k]); there is
+ * no bias.  The pages use kernel 4 with dilation = the largest n-gram order.
+ * Masked positions have g = 0 (so V~ = 0 and n = 0) and still receive
+ * SiLU(c_t) from earlier positions.
+ *
+ * Before a sequence start the filter reads zeros, or, with state_d, the
+ * normalised values of the sequence's previous (kernel_size-1)*dilation
+ * positions ([P-DETAIL] §9.5: 9 for kernel 4, dilation 3).  The state of slot
+ * b is a ring: state_d[b][(p mod R)][m][i] holds n of absolute position p,
+ * R = (kernel_size-1)*dilation, and state_head_d[b] = (positions seen) mod R.
+ * A new sequence starts from a zeroed ring and head 0.  The call reads the
+ * old state, then writes the last min(R, len) values of every sequence and
+ * advances its head.  Slots must be distinct within one call.
+ *
+ *   gate_d       float32 [n_tokens][hc] (engram_gate_add with h_d = NULL)
+ *   v_d          bf16 [n_tokens][hidden] (engram_project), 16-byte aligned
+ *   h_d          bf16 [n_tokens][hc][hidden], updated in place, 16-byte aligned
+ *   mask_d       uint8 [n_tokens] or NULL
+ *   cu_seqlens_d int64 [n_seqs+1] packed sequences, or NULL: every position is
+ *                its own sequence (decode; n_seqs == n_tokens)
+ *   slots_d      int32 [n_seqs] state slot per sequence, or NULL (slot = s);
+ *                a negative slot is padding: its positions are untouched and
+ *                it keeps no state; a slot >= n_slots (with a state) sets
+ *                ENGRAM_ST_BAD_SLOT and is treated as padding
+ *   conv_w_d     float32 [kernel_size][hc][hidden], 16-byte aligned
+ *   gamma_d      float32 [hc][hidden], 16-byte aligned
+ *   state_d      float32 [n_slots][R][hc][hidden] or NULL (zeros, no state kept)
+ *   state_head_d int32 [n_slots]
+ *   workspace_d  engram_short_conv_workspace_bytes(n_tokens, hc) bytes, 256-byte aligned
+ * Requires hidden % 256 == 0, 1 <= hc <= 8, 1 <= kernel_size <= 4,
+ * dilation >= 1 and R <= 64 (ENGRAM_E_SHAPE). */
+size_t engram_short_conv_workspace_bytes(int64_t n_tokens, int32_t hc);
+int engram_short_conv_add(const float* gate_d, const uint16_t* v_d, uint16_t* h_d, const uint8_t* mask_d,
+                          int64_t n_tokens, int32_t hidden, int32_t hc, const int64_t* cu_seqlens_d,
+                          int64_t n_seqs, const int32_t* slots_d, const float* conv_w_d, const float* gamma_d,
+                          int32_t kernel_size, int32_t dilation, float eps, float* state_d,
+                          int32_t* state_head_d, int64_t n_slots, void* workspace_d, size_t workspace_bytes,
+                          int32_t* status_d, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Projection with the gate and residual fused (stage 5a-5c in one kernel)    */

@@ -93,6 +93,15 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.exp2(np.maximum(E - 1, -126) - 7.0)
 
 
+def bf16_flip(v_ref: np.ndarray, v_err: np.ndarray) -> np.ndarray:
+    """One bf16 ulp where the exact v lies within v_err of a bf16 rounding
+    midpoint (a correct fp32 v may round to the other side there), else 0."""
+    from oracle.dequant import bf16_round
+    ulp = bf16_ulp(v_ref)
+    to_midpoint = ulp / 2 - np.abs(v_ref - bf16_round(v_ref))
+    return np.where(to_midpoint <= v_err, ulp, 0.0)
+
+
 def residual_close(got: np.ndarray, ref: np.ndarray, h_in: np.ndarray, g_ref: np.ndarray,
                    v_ref: np.ndarray, v_err: np.ndarray, rtol: float = RESID_RTOL):
     """|got - ref| <= rtol * max(|ref|, |h_in|, |g v|) + g * (v_err + flip), elementwise.
@@ -106,12 +115,9 @@ def residual_close(got: np.ndarray, ref: np.ndarray, h_in: np.ndarray, g_ref: np
     away from the oracle's: flip is that ulp there and 0 elsewhere.
     Returns (ok, worst ratio of error to tolerance, strict-relative fail count).
     """
-    from oracle.dequant import bf16_round
     gv = np.abs(g_ref[:, :, None] * v_ref[:, None, :])
     scale = np.maximum(np.maximum(np.abs(ref), np.abs(h_in)), gv)
-    ulp = bf16_ulp(v_ref)
-    to_midpoint = ulp / 2 - np.abs(v_ref - bf16_round(v_ref))
-    flip = np.where(to_midpoint <= v_err, ulp, 0.0)
+    flip = bf16_flip(v_ref, v_err)
     tol = rtol * scale + np.abs(g_ref)[:, :, None] * (v_err + flip)[:, None, :] + 1e-30
     ratio = np.abs(got - ref) / tol
     strict = np.abs(got - ref) > rtol * np.abs(ref)

@@ -291,6 +291,21 @@ def layer_weights(w: Workload, n_cols: int = 24, seed: Optional[int] = None) -> 
     return LayerWeights(wkv, q_w, k_w)
 
 
+def conv_weights(kernel: int, hc: int, hidden: int, seed: int):
+    """Short-convolution inputs: filters N(0, 0.5^2) f32 [kernel][hc][hidden] and
+    RMSNorm weights U[0.5, 1.5] f32 [hc][hidden]."""
+    w = (rng_for(seed, 40).standard_normal((kernel, hc, hidden)) * 0.5).astype(np.float32)
+    return w, uniform_f32((hc, hidden), 0.5, 1.5, seed, 41)
+
+
+def gate_values(tokens: int, hc: int, seed: int, masked: Optional[np.ndarray] = None) -> np.ndarray:
+    """Gate values U[0.02, 0.98] f32 [tokens][hc], 0 at masked positions."""
+    g = uniform_f32((tokens, hc), 0.02, 0.98, seed, 42)
+    if masked is not None:
+        g[np.asarray(masked, dtype=bool)] = 0.0
+    return g
+
+
 def residual_bits(tokens: int, hc: int, hidden: int, seed: int, stream: int = 30) -> np.ndarray:
     """Residual streams h, bf16 bits [T][hc][H], N(0, 1)."""
     return normal_bf16_bits((tokens, hc, hidden), 1.0, seed, stream)
