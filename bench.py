@@ -41,6 +41,11 @@ GATHER_BYTES_PER_TOKEN = 4 + 24 * 264 + 24 * 256 * 2   # raw id + 24 rows + bf16
 KERNEL_FILES = ["project.cu", "gather.cu", "hash.cu", "engram_internal.h"]
 
 
+def CONV_BYTES_PER_TOKEN(hc: int, hidden: int) -> int:
+    """Short convolution + residual: h read and written (bf16), v and the gates read once."""
+    return 2 * hc * hidden * 2 + hidden * 2 + hc * 4
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -51,6 +56,7 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--micro-steps", type=int, default=30, help="steps of the hash+gather microbench phase")
     p.add_argument("--decode-steps", type=int, default=200, help="steps of the decode phase")
+    p.add_argument("--conv-steps", type=int, default=30, help="steps of the short-convolution layer phase")
     p.add_argument("--host-steps", type=int, default=20,
                    help="steps of the host-resident table phase (0 skips it and its pinned allocation)")
     p.add_argument("--cpu-sample", type=int, default=8192, help="tokens of the oracle CPU baseline sample")
@@ -311,6 +317,7 @@ def run_ours(args, rank, world, local):
 
     micro = microbench(args, w, inp, layer, flush, dev) if args.micro_steps > 0 else None
     dec = decode_bench(args, w, inp, layer, flush, dev) if args.decode_steps > 0 else None
+    conv = conv_bench(args, w, inp, layer, flush, dev) if args.conv_steps > 0 else None
     host = host_table_bench(args, w, inp, layer, flush, dev, statistics.mean(step_ms)) \
         if args.host_steps > 0 else None
 
@@ -324,6 +331,8 @@ def run_ours(args, rank, world, local):
         micro["peak_gbs"] = peaks["hbm_gbs"]
     if dec is not None:
         dec["wkv_frac_hbm"] = dec["wkv_gbs"] / peaks["hbm_gbs"]
+    if conv is not None:
+        conv["conv_frac_hbm"] = conv["conv_gbs"] / peaks["hbm_gbs"]
     # A timed region of 2 s or more of back-to-back steps runs under the power
     # cap like the driver's sustained GEMM loop; shorter ones compare to burst.
     sustained = timed_s >= 2.0
@@ -367,6 +376,7 @@ def run_ours(args, rank, world, local):
         "roofline_gather": roof_g,
         "microbench_hash_gather": micro,
         "decode_step": dec,
+        "short_conv_layer": conv,
         "host_table": host,
         "gpu_launches": args.steps * 4,
         "clocks": clocks,
@@ -478,6 +488,60 @@ def decode_bench(args, w, inp, layer, flush, dev):
             "hash_step_ms": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
             "gather_ms": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs),
             "project_gate_ms": proj * 1e3, "wkv_gbs": wkv_bytes / proj / 1e9}
+
+
+def conv_bench(args, w, inp, layer, flush, dev):
+    """The original Engram layer (short convolution, kernel 4, dilation 3) on the
+    same batch: hash -> gather -> projection -> gates -> convolution + residual."""
+    import torch
+    import hashed_gram_conditional_gb300 as eg
+    from workloads import conv_weights
+
+    cw, gamma = conv_weights(4, w.hc, w.hidden, w.seed)
+    cl = eg.EngramLayer(layer.layout, layer.layer, layer.table, layer.token_map, layer.wkv_packed, layer.q_w,
+                        layer.k_w, conv=eg.ShortConv(torch.from_numpy(cw).to(dev), torch.from_numpy(gamma).to(dev), 3))
+    b = inp["batch"]
+    T = len(b.raw_ids)
+    raw = torch.from_numpy(b.raw_ids).to(dev)
+    cu = torch.from_numpy(b.cu_seqlens).to(dev)
+    h = inp["bf16"](inp["h_bits"])
+    ring, head = cl.new_conv_state(w.n_seqs, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    bufs = cl._buffers(T, dev)
+
+    def run(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        eg.engram_hash(cl.layout, 0, raw, cu, cl.token_map, None, bufs["rows"], bufs["mask"], status)
+        eg.engram_gather_dequant(cl.table, cl.total_rows, bufs["rows"], bufs["e"], status)
+        eg.engram_project(bufs["e"], cl.wkv_packed, h, cl.q_w, cl.k_w, bufs["partials"], bufs["v"], status)
+        g = eg.engram_gates(bufs["partials"], T, cl.hidden, cl.hc, bufs["mask"], cl.eps, cl.clamp, cl.score_scale,
+                            bufs["gate"])
+        if ev is not None:
+            ev[1].record(stream)
+        eg.engram_short_conv_add(g, bufs["v"], h, bufs["mask"], cl.conv.w, cl.conv.gamma, 3, cl.conv.eps, cu, None,
+                                 ring, head, bufs["conv_ws"], status)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(3):
+        flush.zero_()
+        run()
+    n = args.conv_steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for k in range(n):
+        flush.zero_()
+        run(evs[k])
+    torch.cuda.synchronize()
+    step = statistics.mean(ev[0].elapsed_time(ev[2]) for ev in evs) / 1e3
+    conv_s = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs) / 1e3
+    cbytes = CONV_BYTES_PER_TOKEN(w.hc, w.hidden) * T
+    return {"workload": f"{w.name} batch, kernel 4, dilation 3, state ring kept per sequence", "steps": n,
+            "step_ms": step * 1e3, "tokens_per_s": T / step, "conv_ms": conv_s * 1e3,
+            "conv_gbs": cbytes / conv_s / 1e9, "algorithmic_bytes": cbytes, "device_status": int(status.item()),
+            "kernels": "conv_prep_kernel + conv_add_kernel + conv_state_kernel",
+            "note": "projection + gates run as two kernels here (engram_project, gates-only engram_gate_add)"}
 
 
 def host_table_bench(args, w, inp, layer, flush, dev, device_step_ms):

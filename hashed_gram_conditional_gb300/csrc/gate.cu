@@ -102,6 +102,42 @@ __global__ void __launch_bounds__(256) gate_add_kernel(
   }
 }
 
+// The gates alone (no residual): one warp per position, lanes over the
+// partials' tiles, streams in turn.
+__global__ void __launch_bounds__(256) gates_kernel(const float4* __restrict__ partials,
+                                                    const uint8_t* __restrict__ mask, int64_t n_tokens,
+                                                    int hidden, int hc, float eps, float clamp, float score_scale,
+                                                    float* __restrict__ gate_out) {
+  const int lane = threadIdx.x & 31;
+  const int ntile = hidden / 256;
+  const float inv_h = 1.0f / static_cast<float>(hidden);
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * 8;
+  for (int64_t t = blockIdx.x * 8 + (threadIdx.x >> 5); t < n_tokens; t += warps) {
+    const bool masked = (mask != nullptr) && mask[t] != 0;
+    for (int m = 0; m < hc; ++m) {
+      float dot = 0.f, kk = 0.f, hh = 0.f;
+      const float4* p = partials + (t * hc + m) * ntile;
+      for (int q = lane; q < ntile; q += 32) {
+        const float4 x = __ldg(p + q);
+        dot += x.x;
+        kk += x.y;
+        hh += x.z;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        kk += __shfl_xor_sync(0xffffffffu, kk, o);
+        hh += __shfl_xor_sync(0xffffffffu, hh, o);
+      }
+      if (lane == 0) {
+        const float sc = dot * (1.0f / sqrtf(hh * inv_h + eps)) * (1.0f / sqrtf(kk * inv_h + eps)) * score_scale;
+        const float z = copysignf(sqrtf(fmaxf(fabsf(sc), clamp)), sc);
+        gate_out[t * hc + m] = masked ? 0.0f : 1.0f / (1.0f + expf(-z));
+      }
+    }
+  }
+}
+
 }  // namespace
 }  // namespace engram
 
@@ -123,6 +159,14 @@ extern "C" int engram_gate_add(const float* partials_d, const uint16_t* v_d, uin
   int sms = 0;
   int rc = check_device(&sms);
   if (rc) return rc;
+  if (h_d == nullptr) {  // gates only
+    const int64_t cap = static_cast<int64_t>(sms) * 16;
+    const int64_t need = (n_tokens + 7) / 8;
+    gates_kernel<<<static_cast<int>(need < cap ? need : cap), 256, 0, as_stream(stream)>>>(
+        reinterpret_cast<const float4*>(partials_d), mask_d, n_tokens, hidden, hc, eps, clamp, score_scale,
+        gate_out_d);
+    return check_launch("gates_kernel");
+  }
   const int64_t cap = static_cast<int64_t>(sms) * 8;
   const int blocks = static_cast<int>(n_tokens < cap ? n_tokens : cap);
   gate_add_kernel<<<blocks, 256, 0, as_stream(stream)>>>(

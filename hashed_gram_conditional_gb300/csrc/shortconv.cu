@@ -11,24 +11,23 @@
 //       (the branch V4.1 removed) and §多模态细节 (gate 0 at image positions).
 //
 // For stream m of position t, with V~ = g * bf16(v):
-//   n_t   = gamma^(m) * V~_t / sqrt(mean(V~_t^2) + eps)
-//         = gamma^(m) * (r_t * v_t),   r_t = g / sqrt(g^2 * mean(v_t^2) + eps)
-//   c_t   = sum_k w[k] * n_{t - k*dilation}          (zeros / carried state before the start)
+//   n_t   = gamma^(m) * V~_t / sqrt(mean(V~_t^2) + eps) = gamma^(m) * x_t,
+//   x_t   = r_t * v_t,   r_t = g / sqrt(g^2 * mean(v_t^2) + eps)
+//   c_t   = sum_k (w[k] * gamma^(m)) * x_{t - k*dilation}   (zeros / carried state before the start)
 //   h_t  <- bf16(h_t + (g * v_t + SiLU(c_t)))
 //
-// Three launches: (1) one warp per position reduces mean(v^2) and writes r
-// and the position's sequence; (2) the add streams h once -- a thread owns
-// 8 channels of one stream, keeps that stream's filter taps in registers and
-// walks a run of consecutive positions, reading the tap positions' v from
-// L1/L2 (every v row serves kernel-size positions and hc streams); (3) the
-// last (kernel-1)*dilation normalised values of each sequence go to the
-// state ring, after (2) has read the old ones.
+// Three launches: (1) one warp per position reduces mean(v^2) and writes r,
+// the position's sequence and its index in it; (2) the add streams h once
+// (see conv_add_kernel); (3) the last (kernel-1)*dilation values x of each
+// sequence go to the state ring, after (2) has read the old ones.
 //
 // HBM-bound like the plain gate: per position hc*H bf16 of h read and
 // written, H bf16 of v read, the filters once per run of positions.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <atomic>
 
 #include "engram_internal.h"
 
@@ -55,11 +54,18 @@ __device__ __forceinline__ void unpack8(const uint4 x, float (&f)[8]) {
   f[6] = bf16_lo(x.w); f[7] = bf16_hi(x.w);
 }
 
-// The normalised value, one expression shared by the add and the state
-// writer so that a value read back from the state equals the in-batch one.
-__device__ __forceinline__ float normed(float gamma, float r, float v) { return gamma * (r * v); }
 
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+// x * sigmoid(x) = x / (1 + 2^(-x log2 e)) with the hardware base-2
+// exponential and reciprocal approximations (PTX ex2.approx.ftz.f32, rcp.approx.ftz.f32;
+// each about 2^-22 relative): a few ulp plus about 1.2 |x| ulp from rounding
+// the exponent's argument.  Inputs below -126/log2 e give 2^(..) = inf and
+// a result of -0, the limit of x sigmoid(x).
+__device__ __forceinline__ float silu(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return x * r;
+}
 
 struct ConvArgs {
   const float* gate;      // [T][hc]
@@ -79,7 +85,10 @@ struct ConvArgs {
   int32_t* head;          // [n_slots]
   int64_t n_slots;
   float* r;               // workspace [T][hc]
+  float* ge;              // workspace [T][hc]: the gate, 0 at masked positions
   int32_t* seq;           // workspace [T]: sequence index, -1 = padding
+  int32_t* pos;           // workspace [T]: index within the sequence, -1 = padding
+  int32_t* head0;         // workspace [T]: at a sequence's first position, its slot's ring head on entry
   int32_t* status;        // or null
 };
 
@@ -107,6 +116,7 @@ __global__ void __launch_bounds__(kThreads) conv_prep_kernel(ConvArgs a) {
     if (lane < a.hc) {
       const float g = masked ? 0.f : a.gate[t * a.hc + lane];
       a.r[t * a.hc + lane] = g / sqrtf(g * g * ms + a.eps);
+      a.ge[t * a.hc + lane] = g;
     }
     if (lane == 0) {
       int64_t s = t;
@@ -127,132 +137,294 @@ __global__ void __launch_bounds__(kThreads) conv_prep_kernel(ConvArgs a) {
         out = -1;
       }
       a.seq[t] = out;
+      const int64_t local = t - (a.cu != nullptr ? a.cu[s] : t);
+      a.pos[t] = out < 0 ? -1 : static_cast<int32_t>(local);
+      // the ring head as it was on entry, for the state writer (which
+      // advances it while other blocks still need the old value)
+      if (out >= 0 && local == 0 && a.state != nullptr) a.head0[t] = a.head[slot];
     }
   }
 }
 
-// (2) h <- bf16(h + g v + SiLU(sum_k w[k] n_{t-k*dil})).
-__global__ void __launch_bounds__(kThreads) conv_add_kernel(ConvArgs a, int tokens_per_block) {
-  const int nchunk = a.hidden / 8;
+// (2) h <- bf16(h + g v + SiLU(sum_k (w[k] gamma) x_{t-k*dil})), x_q = r_q v_q.
+//
+// A thread owns 8 channels of one stream (the filter taps, with gamma folded
+// in, stay in registers); a warp owns 256 consecutive channels of one stream,
+// so for every position its h and v are one contiguous 512-byte segment each.
+// A block walks one residue class mod dilation of a run of positions:
+// t, t+dil, t+2*dil, ...  Along the walk the taps of position t are the x of
+// the walk's previous positions, so x is computed once per position and kept
+// in a register window of three slots used round-robin (the loop is unrolled
+// three times, so the slots are fixed registers).  Positions at least
+// (K-1)*dil into their sequence take a branch-free path; the others read the
+// taps that fall before the sequence start from the state ring (or zero).
+//
+// Loads are per warp and asynchronous: lane 0 keeps the h and v segments of
+// the next kInStages-1 positions of the walk in flight as bulk copies into
+// the warp's shared-memory ring (one mbarrier per stage); results go out as
+// one coalesced 512-byte store per warp.
+constexpr int kInStages = 8;
+constexpr int kCh = 8;                    // channels per thread
+constexpr int kWarps = kThreads / 32;
+constexpr int kSegBytes = 32 * kCh * 2;   // 512
+struct WarpRing {
+  uint4 h[kInStages][32];
+  uint4 v[kInStages][32];
+  uint64_t bar[kInStages];
+};
+
+template <int K>
+__global__ void __launch_bounds__(kThreads, 2) conv_add_kernel(ConvArgs a, int walk_len) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  WarpRing& wr = reinterpret_cast<WarpRing*>(smem_raw)[warp];
+  const int nchunk = a.hidden / kCh;
   const int p = blockIdx.x * kThreads + threadIdx.x;
-  if (p >= a.hc * nchunk) return;
+  // hidden % 256 == 0, so a warp never straddles two streams and either all
+  // of its lanes have work or none has
+  if (p - lane >= a.hc * nchunk) return;
   const int m = p / nchunk, c = p - m * nchunk;
-  const int i0 = c * 8;
-  float w[kMaxK][8], gam[8];
+  const int hc = a.hc, dil = a.dil;
+  float wg[K][kCh];
+  {
+    const float4* gq = reinterpret_cast<const float4*>(a.gamma + static_cast<int64_t>(m) * a.hidden + c * kCh);
+    const float4 gx = __ldg(gq), gy = __ldg(gq + 1);
+    const float gam[8] = {gx.x, gx.y, gx.z, gx.w, gy.x, gy.y, gy.z, gy.w};
 #pragma unroll
-  for (int k = 0; k < kMaxK; ++k) {
-    if (k < a.K) {
-      const float4* wp = reinterpret_cast<const float4*>(a.w + (static_cast<int64_t>(k) * a.hc + m) * a.hidden + i0);
+    for (int k = 0; k < K; ++k) {
+      const float4* wp = reinterpret_cast<const float4*>(a.w + (static_cast<int64_t>(k) * hc + m) * a.hidden + c * kCh);
       const float4 x = __ldg(wp), y = __ldg(wp + 1);
-      w[k][0] = x.x; w[k][1] = x.y; w[k][2] = x.z; w[k][3] = x.w;
-      w[k][4] = y.x; w[k][5] = y.y; w[k][6] = y.z; w[k][7] = y.w;
+      const float wk[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int j = 0; j < kCh; ++j) wg[k][j] = wk[j] * gam[j];
+    }
+  }
+  // this block's walk: positions t0 + rho + j*dil, j < walk_len, below t1
+  const int rho = static_cast<int>(blockIdx.y % static_cast<unsigned>(dil));
+  const int64_t span = static_cast<int64_t>(walk_len) * dil;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.y / static_cast<unsigned>(dil)) * span;
+  const int64_t t1 = t0 + span < a.n_tokens ? t0 + span : a.n_tokens;
+  const int64_t first = t0 + rho;
+  const int n_pos = first < t1 ? static_cast<int>((t1 - first + dil - 1) / dil) : 0;
+  if (n_pos == 0) return;
+
+  // strides in 16-byte units along the walk
+  const int64_t hstride = static_cast<int64_t>(hc) * nchunk * dil;
+  const int64_t vstride = static_cast<int64_t>(nchunk) * dil;
+  const uint4* hsrc = a.h + (first * hc + m) * nchunk + (c - lane);  // the warp's segment at `first`
+  const uint4* vsrc = a.v + first * nchunk + (c - lane);
+  uint4* hdst = a.h + (first * hc + m) * nchunk + c;
+  const float* rp = a.r + first * hc + m;  // advanced along the walk
+  const float* gp = a.ge + first * hc + m;
+  const int32_t* pp = a.pos + first;
+  const int64_t sstride = static_cast<int64_t>(hc) * dil;  // r and ge along the walk
+
+  if (lane == 0) {
+    for (int s = 0; s < kInStages; ++s) mbar_init(smem_u32(&wr.bar[s]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  int ji = 0;           // next walk index to fetch
+  uint32_t issued = 0;  // stages with a copy in flight (lane 0)
+  auto issue = [&](int s) {
+    if (ji < n_pos) {
+      if (lane == 0) {
+        const uint32_t bar = smem_u32(&wr.bar[s]);
+        mbar_arrive_expect_tx(bar, 2 * kSegBytes);
+        bulk_g2s(smem_u32(&wr.h[s][0]), hsrc + ji * hstride, kSegBytes, bar);
+        bulk_g2s(smem_u32(&wr.v[s][0]), vsrc + ji * vstride, kSegBytes, bar);
+        issued |= 1u << s;
+      }
+      ++ji;
+    }
+  };
+  for (int s = 0; s < kInStages - 1; ++s) issue(s);
+
+  // window slot (u - k) mod 3 holds x of k steps back at unrolled step u
+  float win[3][kCh];
+#pragma unroll
+  for (int k = 1; k <= 3; ++k) {
+    const int64_t q = first - static_cast<int64_t>(k) * dil;
+    float* wdst = win[(3 - k) % 3];
+    if (k < K && q >= 0) {
+      const float rq = __ldg(a.r + q * hc + m);
+      float f[kCh];
+      unpack8(__ldg(a.v + q * nchunk + c), f);
+#pragma unroll
+      for (int j = 0; j < kCh; ++j) wdst[j] = rq * f[j];
     } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) w[k][j] = 0.f;
+      for (int j = 0; j < kCh; ++j) wdst[j] = 0.f;
     }
   }
-  {
-    const float4* gp = reinterpret_cast<const float4*>(a.gamma + static_cast<int64_t>(m) * a.hidden + i0);
-    const float4 x = __ldg(gp), y = __ldg(gp + 1);
-    gam[0] = x.x; gam[1] = x.y; gam[2] = x.z; gam[3] = x.w;
-    gam[4] = y.x; gam[5] = y.y; gam[6] = y.z; gam[7] = y.w;
-  }
-  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * tokens_per_block;
-  const int64_t t1 = t0 + tokens_per_block < a.n_tokens ? t0 + tokens_per_block : a.n_tokens;
-  for (int64_t t = t0; t < t1; ++t) {
-    const int32_t s = a.seq[t];
-    if (s < 0) continue;
-    const int64_t start = a.cu != nullptr ? a.cu[s] : t;
-    const int64_t local = t - start;
-    float acc[8];
+
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  float rt = __ldg(rp), gt = __ldg(gp);
+  int32_t lt = __ldg(pp);
+  const int64_t tail = static_cast<int64_t>(K - 1) * dil;  // positions before this take the general path
+  int j = 0;
+  while (true) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-    float vt[8];
-#pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-      if (k >= a.K) break;
-      const int64_t ql = local - static_cast<int64_t>(k) * a.dil;
-      float n[8];
-      if (ql >= 0) {
-        const int64_t q = start + ql;
-        const float rq = a.r[q * a.hc + m];
-        float f[8];
-        unpack8(__ldg(a.v + q * nchunk + c), f);
-        if (k == 0) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) vt[j] = f[j];
+    for (int u = 0; u < 3; ++u) {
+      if (j >= n_pos) goto done;
+      issue(stage == 0 ? kInStages - 1 : stage - 1);
+      {
+        const bool landed = mbar_wait_bounded(smem_u32(&wr.bar[stage]), (phase >> stage) & 1u, nullptr);
+        if (!__all_sync(0xffffffffu, landed)) {  // uniform, so no lane is left at a barrier
+          ok = false;
+          goto done;
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) n[j] = normed(gam[j], rq, f[j]);
-      } else if (a.state != nullptr) {
-        const int32_t slot = slot_of(a, s);
-        int64_t idx = (static_cast<int64_t>(a.head[slot]) + ql) % a.ring;
-        if (idx < 0) idx += a.ring;
-        const float4* sp = reinterpret_cast<const float4*>(
-            a.state + ((static_cast<int64_t>(slot) * a.ring + idx) * a.hc + m) * a.hidden + i0);
-        const float4 x = sp[0], y = sp[1];
-        n[0] = x.x; n[1] = x.y; n[2] = x.z; n[3] = x.w;
-        n[4] = y.x; n[5] = y.y; n[6] = y.z; n[7] = y.w;
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) n[j] = 0.f;
       }
+      phase ^= 1u << stage;
+      if (lane == 0) issued &= ~(1u << stage);
+      {
+        const uint4 hv = wr.h[stage][lane], vv = wr.v[stage][lane];
+        __syncwarp();  // every lane has read in-stage `stage` before lane 0 refills it
+        // next position's scalars
+        float rt_n = 0.f, gt_n = 0.f;
+        int32_t lt_n = -1;
+        rp += sstride;
+        gp += sstride;
+        pp += dil;
+        if (j + 1 < n_pos) {
+          rt_n = __ldg(rp);
+          gt_n = __ldg(gp);
+          lt_n = __ldg(pp);
+        }
+        float xt[kCh];
+        {
+          float vt[kCh];
+          unpack8(vv, vt);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = fmaf(w[k][j], n[j], acc[j]);
+          for (int q = 0; q < kCh; ++q) xt[q] = rt * vt[q];
+        }
+        if (lt >= 0) {
+          float acc[kCh];
+#pragma unroll
+          for (int q = 0; q < kCh; ++q) acc[q] = wg[0][q] * xt[q];
+          if (lt >= tail) {
+#pragma unroll
+            for (int k = 1; k < K; ++k) {
+#pragma unroll
+              for (int q = 0; q < kCh; ++q) acc[q] = fmaf(wg[k][q], win[(u - k + 3) % 3][q], acc[q]);
+            }
+          } else {
+#pragma unroll
+            for (int k = 1; k < K; ++k) {
+              const int ql = lt - k * dil;
+              if (ql >= 0) {
+#pragma unroll
+                for (int q = 0; q < kCh; ++q) acc[q] = fmaf(wg[k][q], win[(u - k + 3) % 3][q], acc[q]);
+              } else if (a.state != nullptr) {
+                const int64_t tc = first + static_cast<int64_t>(j) * dil;
+                const int64_t t_start = tc - lt;  // the sequence's first position
+                const int32_t slot = slot_of(a, a.seq[tc]);
+                int64_t idx = (static_cast<int64_t>(a.head0[t_start]) + ql) % a.ring;
+                if (idx < 0) idx += a.ring;
+                const float4* sp = reinterpret_cast<const float4*>(
+                    a.state + ((static_cast<int64_t>(slot) * a.ring + idx) * hc + m) * a.hidden + c * kCh);
+                const float4 x = sp[0], y = sp[1];
+                const float sx[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int q = 0; q < kCh; ++q) acc[q] = fmaf(wg[k][q], sx[q], acc[q]);
+              }
+            }
+          }
+          // h + (g v + SiLU(c)), a pair of channels at a time
+          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+          uint32_t ow[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float lo = bf16_lo(hw[q]) + (gt * bf16_lo(vw[q]) + silu(acc[2 * q]));
+            const float hi = bf16_hi(hw[q]) + (gt * bf16_hi(vw[q]) + silu(acc[2 * q + 1]));
+            ow[q] = pack_bf16(lo, hi);
+          }
+          *hdst = make_uint4(ow[0], ow[1], ow[2], ow[3]);  // padding positions are not written
+        }
+        hdst += hstride;
+        // the window slot of x_t is the one that held x of three steps back
+#pragma unroll
+        for (int q = 0; q < kCh; ++q) win[u][q] = xt[q];
+        rt = rt_n;
+        gt = gt_n;
+        lt = lt_n;
+      }
+      stage = stage + 1 == kInStages ? 0 : stage + 1;
+      ++j;
     }
-    const bool masked = a.mask != nullptr && a.mask[t] != 0;
-    const float g = masked ? 0.f : a.gate[t * a.hc + m];
-    uint4* hp = a.h + (t * a.hc + m) * nchunk + c;
-    const uint4 hv = *hp;
-    float hf[8];
-    unpack8(hv, hf);
-    float o[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) o[j] = hf[j] + (g * vt[j] + silu(acc[j]));
-    uint4 out;
-    out.x = pack_bf16(o[0], o[1]);
-    out.y = pack_bf16(o[2], o[3]);
-    out.z = pack_bf16(o[4], o[5]);
-    out.w = pack_bf16(o[6], o[7]);
-    *hp = out;
   }
+done:
+  if (lane == 0 && !ok) {
+    if (a.status != nullptr) atomicOr(a.status, ENGRAM_ST_TIMEOUT);
+    // let the copies still in flight land before the shared memory is released
+    for (int s = 0; s < kInStages; ++s)
+      if (issued & (1u << s)) mbar_wait_bounded(smem_u32(&wr.bar[s]), (phase >> s) & 1u, nullptr);
+  }
+  __syncwarp();
 }
 
-// (3) state ring: the last min(ring, len) normalised values of each sequence,
-// then head <- (head + len) mod ring.  One block per sequence.
+// (3) state ring: the last min(ring, len) values x of each sequence, then
+// head <- (head + len) mod ring.  One block per (sequence, kept position);
+// the entry head comes from the prep kernel's copy, so the block that
+// advances the head races with no reader.
 __global__ void __launch_bounds__(kThreads) conv_state_kernel(ConvArgs a) {
   const int64_t s = blockIdx.x;
   const int32_t slot = slot_of(a, s);
   if (slot < 0 || slot >= a.n_slots) return;
   const int64_t start = a.cu != nullptr ? a.cu[s] : s;
   const int64_t len = a.cu != nullptr ? a.cu[s + 1] - start : 1;
-  const int64_t first = len > a.ring ? len - a.ring : 0;
-  const int32_t head = a.head[slot];
+  const int64_t keep = len < a.ring ? len : a.ring;
+  if (static_cast<int64_t>(blockIdx.y) >= keep) return;
+  const int64_t local = len - keep + blockIdx.y;
+  const int32_t head = a.head0[start];
   const int nchunk = a.hidden / 8;
-  const int64_t per_pos = static_cast<int64_t>(a.hc) * nchunk;
-  const int64_t work = (len - first) * per_pos;
-  for (int64_t x = threadIdx.x; x < work; x += blockDim.x) {
-    const int64_t local = first + x / per_pos;
-    const int rem = static_cast<int>(x - (local - first) * per_pos);
-    const int m = rem / nchunk, c = rem - m * nchunk;
-    const int64_t t = start + local;
+  const int per_pos = a.hc * nchunk;
+  const int64_t t = start + local;
+  const int64_t idx = (static_cast<int64_t>(head) + local) % a.ring;
+  for (int x = threadIdx.x; x < per_pos; x += blockDim.x) {
+    const int m = x / nchunk, c = x - m * nchunk;
     const float rq = a.r[t * a.hc + m];
     float f[8];
     unpack8(__ldg(a.v + t * nchunk + c), f);
-    const float* gp = a.gamma + static_cast<int64_t>(m) * a.hidden + c * 8;
-    float n[8];
+    float n[8];  // the same product as the add's window, so state taps equal in-batch taps
 #pragma unroll
-    for (int j = 0; j < 8; ++j) n[j] = normed(__ldg(gp + j), rq, f[j]);
-    const int64_t idx = (static_cast<int64_t>(head) + local) % a.ring;
+    for (int j = 0; j < 8; ++j) n[j] = rq * f[j];
     float4* sp = reinterpret_cast<float4*>(a.state + ((static_cast<int64_t>(slot) * a.ring + idx) * a.hc + m) *
                                                          a.hidden + c * 8);
     sp[0] = make_float4(n[0], n[1], n[2], n[3]);
     sp[1] = make_float4(n[4], n[5], n[6], n[7]);
   }
-  if (threadIdx.x == 0) a.head[slot] = static_cast<int32_t>((head + len) % a.ring);
+  if (blockIdx.y == 0 && threadIdx.x == 0) a.head[slot] = static_cast<int32_t>((head + len) % a.ring);
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+template <int K>
+int launch_add(dim3 grid, int smem, cudaStream_t st, const ConvArgs& a, int walk) {
+  static std::atomic<uint64_t> attr_set{0};  // one bit per device: the shared-memory opt-in was made
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit == 0 || !(attr_set.load(std::memory_order_relaxed) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(conv_add_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    attr_set.fetch_or(bit, std::memory_order_relaxed);
+  }
+  conv_add_kernel<K><<<grid, kThreads, smem, st>>>(a, walk);
+  return check_launch("conv_add_kernel");
+}
+
+int launch_conv_add(int K, dim3 grid, int smem, cudaStream_t st, const ConvArgs& a, int walk) {
+  switch (K) {
+    case 1: return launch_add<1>(grid, smem, st, a, walk);
+    case 2: return launch_add<2>(grid, smem, st, a, walk);
+    case 3: return launch_add<3>(grid, smem, st, a, walk);
+    default: return launch_add<4>(grid, smem, st, a, walk);
+  }
+}
 
 }  // namespace
 }  // namespace engram
@@ -261,8 +433,8 @@ using namespace engram;
 
 extern "C" size_t engram_short_conv_workspace_bytes(int64_t n_tokens, int32_t hc) {
   if (n_tokens < 0 || hc < 1) return 0;
-  return round256(static_cast<size_t>(n_tokens) * hc * sizeof(float)) +
-         round256(static_cast<size_t>(n_tokens) * sizeof(int32_t));
+  return 2 * round256(static_cast<size_t>(n_tokens) * hc * sizeof(float)) +
+         3 * round256(static_cast<size_t>(n_tokens) * sizeof(int32_t));
 }
 
 extern "C" int engram_short_conv_add(const float* gate_d, const uint16_t* v_d, uint16_t* h_d,
@@ -320,8 +492,14 @@ extern "C" int engram_short_conv_add(const float* gate_d, const uint16_t* v_d, u
   a.head = state_head_d;
   a.n_slots = state_d ? n_slots : 0;
   a.r = static_cast<float*>(workspace_d);
+  a.ge = reinterpret_cast<float*>(static_cast<char*>(workspace_d) +
+                                  round256(static_cast<size_t>(n_tokens) * hc * sizeof(float)));
   a.seq = reinterpret_cast<int32_t*>(static_cast<char*>(workspace_d) +
-                                     round256(static_cast<size_t>(n_tokens) * hc * sizeof(float)));
+                                     2 * round256(static_cast<size_t>(n_tokens) * hc * sizeof(float)));
+  a.pos = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(a.seq) +
+                                     round256(static_cast<size_t>(n_tokens) * sizeof(int32_t)));
+  a.head0 = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(a.pos) +
+                                       round256(static_cast<size_t>(n_tokens) * sizeof(int32_t)));
   a.status = status_d;
   cudaStream_t st = as_stream(stream);
 
@@ -332,22 +510,24 @@ extern "C" int engram_short_conv_add(const float* gate_d, const uint16_t* v_d, u
   rc = check_launch("conv_prep_kernel");
   if (rc) return rc;
 
-  const int pairs = hc * (hidden / 8);
+  const int pairs = hc * (hidden / kCh);
   const int gx = (pairs + kThreads - 1) / kThreads;
-  int tpb = 32;  // positions per block: fewer when that leaves SMs idle
-  while (tpb > 1 && static_cast<int64_t>(gx) * ((n_tokens + tpb - 1) / tpb) < 4LL * sms) tpb >>= 1;
-  const int64_t gy = (n_tokens + tpb - 1) / tpb;
-  if (gy > 65535) {
-    tpb = static_cast<int>((n_tokens + 65534) / 65535);
-  }
-  const dim3 grid(gx, static_cast<unsigned>((n_tokens + tpb - 1) / tpb));
-  conv_add_kernel<<<grid, kThreads, 0, st>>>(a, tpb);
-  rc = check_launch("conv_add_kernel");
+  // a block walks walk_len positions of one residue class; shorter walks
+  // when the grid would leave SMs idle, longer ones to stay within grid.y
+  int walk = 32;
+  auto blocks_y = [&](int wl) {
+    return ((n_tokens + static_cast<int64_t>(wl) * dilation - 1) / (static_cast<int64_t>(wl) * dilation)) * dilation;
+  };
+  while (walk > 1 && static_cast<int64_t>(gx) * blocks_y(walk) < 4LL * sms) walk >>= 1;
+  while (blocks_y(walk) > 65535) walk <<= 1;
+  const dim3 grid(gx, static_cast<unsigned>(blocks_y(walk)));
+  const int smem = static_cast<int>(sizeof(WarpRing)) * kWarps;
+  rc = launch_conv_add(kernel_size, grid, smem, st, a, walk);
   if (rc) return rc;
 
   if (state_d != nullptr) {
     if (n_seqs > 0x7fffffff) return fail(ENGRAM_E_RANGE, "too many sequences");
-    conv_state_kernel<<<static_cast<unsigned>(n_seqs), kThreads, 0, st>>>(a);
+    conv_state_kernel<<<dim3(static_cast<unsigned>(n_seqs), static_cast<unsigned>(ring)), kThreads, 0, st>>>(a);
     rc = check_launch("conv_state_kernel");
   }
   return rc;

@@ -337,6 +337,8 @@ int engram_gate_add(const float* partials_d, const uint16_t* v_d, uint16_t* h_d,
  *   n_t = gamma[m] * V~_t / sqrt(mean_i(V~_t,i^2) + eps)         (RMSNorm)
  *   c_t = sum_{k < kernel_size} w[k][m] * n_{t - k*dilation}     (depthwise, causal)
  *   h_d[t][m][i] <- bf16_rne(h + (V~_t,i + SiLU(c_t,i)))         in fp32
+ * (gamma folded into the filter taps; SiLU with the fast exponential and
+ * division, a few ulp plus about 1.2|c| ulp)
  * w[k] multiplies the value k*dilation positions back (a PyTorch Conv1d
  * filter W[ch][0][j] with left padding maps to w[k] = W[..][K-1-k]); there is
  * no bias.  The pages use kernel 4 with dilation = the largest n-gram order.
@@ -346,7 +348,8 @@ int engram_gate_add(const float* partials_d, const uint16_t* v_d, uint16_t* h_d,
  * Before a sequence start the filter reads zeros, or, with state_d, the
  * normalised values of the sequence's previous (kernel_size-1)*dilation
  * positions ([P-DETAIL] §9.5: 9 for kernel 4, dilation 3).  The state of slot
- * b is a ring: state_d[b][(p mod R)][m][i] holds n of absolute position p,
+ * b is a ring: state_d[b][(p mod R)][m][i] holds n / gamma[m][i] (the RMS-
+ * normalised value before the RMSNorm weight) of absolute position p,
  * R = (kernel_size-1)*dilation, and state_head_d[b] = (positions seen) mod R.
  * A new sequence starts from a zeroed ring and head 0.  The call reads the
  * old state, then writes the last min(R, len) values of every sequence and
