@@ -38,7 +38,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Engram layer tokens/s (hash+gather+gate) at T=16k; gather HBM GB/s vs peak"
 GATHER_BYTES_PER_TOKEN = 4 + 24 * 264 + 24 * 256 * 2   # raw id + 24 rows + bf16 e = 18,628 B
-KERNEL_FILES = ["project.cu", "gather.cu", "hash.cu", "engram_internal.h"]
+KERNEL_FILES = ["project.cu", "gather.cu", "hash.cu", "gate.cu", "shortconv.cu", "engram_internal.h"]
 
 
 def CONV_BYTES_PER_TOKEN(hc: int, hidden: int) -> int:
@@ -325,6 +325,7 @@ def run_ours(args, rank, world, local):
         return None
 
     peaks, peak_src = load_peaks()
+    traffic = profiled_traffic()
     timed_s = wall1 - wall0
     if micro is not None:
         micro["frac"] = micro["gather_gbs"] / peaks["hbm_gbs"]
@@ -333,6 +334,7 @@ def run_ours(args, rank, world, local):
         dec["wkv_frac_hbm"] = dec["wkv_gbs"] / peaks["hbm_gbs"]
     if conv is not None:
         conv["conv_frac_hbm"] = conv["conv_gbs"] / peaks["hbm_gbs"]
+        conv["traffic_conv_add"] = traffic.get("conv_add_kernel")
     # A timed region of 2 s or more of back-to-back steps runs under the power
     # cap like the driver's sustained GEMM loop; shorter ones compare to burst.
     sustained = timed_s >= 2.0
@@ -340,7 +342,6 @@ def run_ours(args, rank, world, local):
     flops = 2.0 * T * 6144 * (w.hc + 1) * w.hidden
     proj_s = statistics.mean(stage["project_gate"]) / 1e3
     gat_s = statistics.mean(stage["gather"]) / 1e3
-    traffic = profiled_traffic()
     roof = {"bound": "tensor",
             "kernel": "project2_kernel<fused> (CTA-pair tcgen05 wkv GEMM, gate and residual in the epilogue)",
             "achieved": flops / proj_s / 1e12, "peak": tf_peak, "unit": "TFLOP/s",
