@@ -105,6 +105,8 @@ _SIGS = {
     "engram_dequant_rows": [_P, _I64, _I64, _I32, _P, _P, _P],
     "engram_host_gather": [_P, _I64, _P, _I64, _P, _I32, _P],
     "engram_host_gather_async": [_P, _I64, _P, _I64, _P, _I32, _P, _P],
+    "engram_hash_gather": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _I64, _P, _P, _P, _P,
+                           _P],
     "engram_short_conv_add": [_P, _P, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _I32, _I32, _F32, _P, _P,
                               _I64, _P, ctypes.c_size_t, _P, _P],
 }
@@ -357,6 +359,40 @@ def engram_gather_dequant(table: torch.Tensor, total_rows: int, row_ids: torch.T
     _check(L.engram_gather_dequant(_ptr(table), total_rows, table.numel(), _ptr(row_ids), T, C, _ptr(e),
                                    _ptr(status), _stream(dev)), "engram_gather_dequant")
     return e
+
+
+def engram_hash_gather(layout: Layout, layer: int, raw_ids: torch.Tensor, cu_seqlens: torch.Tensor,
+                       token_map: torch.Tensor, table: torch.Tensor, hist: Optional[torch.Tensor] = None,
+                       e: Optional[torch.Tensor] = None, mask: Optional[torch.Tensor] = None,
+                       row_ids: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """Hash + gather + dequantise in one kernel; returns (e bf16 [T][n_cols*256], mask uint8 [T]).
+    row_ids (int32 [T][n_cols]) is filled only when given; hist is advanced in place."""
+    L = _load()
+    dev = raw_ids.device
+    T = raw_ids.numel()
+    C = layout.n_cols
+    _need(raw_ids, "raw_ids", torch.int32)
+    _need(cu_seqlens, "cu_seqlens", torch.int64, dev)
+    _need(token_map, "token_map", torch.int32, dev)
+    if table.is_cuda:
+        _need(table, "table", torch.uint8, dev)
+    elif not (table.dtype == torch.uint8 and table.is_pinned() and table.is_contiguous()):
+        raise ValueError("a host table must be a contiguous pinned uint8 tensor (read over NVLink-C2C)")
+    n_seqs = cu_seqlens.numel() - 1
+    if hist is not None:
+        _need(hist, "hist", torch.int32, dev, n_seqs * (layout.max_ngram - 1))
+    if e is None:
+        e = torch.empty((T, C * HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    if mask is None:
+        mask = torch.empty(T, dtype=torch.uint8, device=dev)
+    _need(e, "e", torch.bfloat16, dev, T * C * HEAD_DIM)
+    _need(mask, "mask", torch.uint8, dev, T)
+    if row_ids is not None:
+        _need(row_ids, "row_ids", torch.int32, dev, T * C)
+    _check(L.engram_hash_gather(layout.ref, layer, _ptr(raw_ids), T, _ptr(cu_seqlens), n_seqs, _ptr(token_map),
+                                token_map.numel(), _ptr(hist), _ptr(table), table.numel(), _ptr(e), _ptr(mask),
+                                _ptr(row_ids), _ptr(status), _stream(dev)), "engram_hash_gather")
+    return e, mask
 
 
 def engram_dequant_rows(rows: torch.Tensor, n_cols: int, e: Optional[torch.Tensor] = None,
@@ -672,9 +708,8 @@ class EngramLayer:
         layer with the short convolution (None: zeros before every sequence)."""
         T = raw_ids.numel()
         b = self._buffers(T, raw_ids.device)
-        engram_hash(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, hist, b["rows"], b["mask"],
-                    status)
-        engram_gather_dequant(self.table, self.total_rows, b["rows"], b["e"], status)
+        engram_hash_gather(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, self.table, hist, b["e"],
+                           b["mask"], b["rows"], status)
         self._gate(b, h, status, gate_out, cu_seqlens=cu_seqlens, conv_state=conv_state)
         return b
 

@@ -26,6 +26,7 @@
 #include <cstdlib>
 
 #include "engram_internal.h"
+#include "hash_device.cuh"
 
 namespace engram {
 namespace {
@@ -199,11 +200,45 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Where the row ids of a position come from: read from memory (or the
+// identity t * n_cols + j for contiguous rows) ...
+struct IdRows {
+  const int32_t* rows;
+  __device__ __forceinline__ int32_t operator()(int64_t t, uint32_t lane, int n_cols) const {
+    if (lane >= static_cast<uint32_t>(n_cols)) return -1;
+    return rows != nullptr ? __ldg(rows + t * n_cols + lane) : static_cast<int32_t>(t * n_cols + lane);
+  }
+};
+
+// ... or computed in the warp from the position's token window (the fused
+// hash + gather: the row ids need not round-trip through memory; they and
+// the mask are still written when asked for).
+struct HashedRows {
+  hashdev::HashConsts c;
+  const int32_t* raw;
+  const int64_t* cu;
+  int32_t n_seqs;
+  const int32_t* tmap;
+  const int32_t* hist;
+  int32_t* rows_out;  // or null
+  uint8_t* mask;
+  int32_t* status;
+  __device__ __forceinline__ int32_t operator()(int64_t t, uint32_t lane, int n_cols) const {
+    const int32_t slot = hashdev::prefill_slot(c, t, raw, cu, n_seqs, tmap, hist, status);
+    int32_t row;
+    const bool dead = hashdev::window_rows(slot, c, &row);
+    if (rows_out != nullptr && lane < static_cast<uint32_t>(n_cols)) rows_out[t * n_cols + lane] = row;
+    if (lane == 0) mask[t] = dead ? 1 : 0;
+    return row;
+  }
+};
+
 // Same pipeline as gather_dequant_kernel, but each row window moves as 17
 // 16-byte cp.async copies spread over the warp's lanes (a flat list of
 // n_cols * 17 pieces per position) instead of one bulk copy per row: many
 // small requests go through the LSU rather than the TMA unit.
-__global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArgs a) {
+template <class RowSource>
+__global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArgs a, RowSource src) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int w = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
@@ -225,10 +260,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArg
   const int pieces = n_cols * 17;
 
   auto issue = [&](int64_t t, int s) {
-    int32_t r = -1;
+    const int32_t r = src(t, lane, n_cols);  // warp-collective
     bool valid = false;
     if (lane < static_cast<uint32_t>(n_cols)) {
-      r = a.rows != nullptr ? __ldg(a.rows + t * n_cols + lane) : static_cast<int32_t>(t * n_cols + lane);
       valid = r >= 0 && static_cast<int64_t>(r) < a.total_rows;
       if (!valid && a.status) atomicOr(a.status, static_cast<int>(ENGRAM_ST_BAD_ROW));
     }
@@ -347,6 +381,36 @@ bool use_ldgsts() {
 
 using namespace engram;
 
+namespace engram {
+namespace {
+
+// Pipeline depth and shared memory of the gather kernels for n_cols rows per
+// position; launches the cp.async kernel with the given row source.
+int gather_config(int n_cols, int* stages, size_t* smem) {
+  const int smem_max = 227 * 1024;
+  const int per_stage = n_cols * kSlot + 16;  // slots + mbarrier + two masks
+  int s = smem_max / (kWarps * per_stage);
+  if (s > 4) s = 4;
+  if (s < 1) return fail(ENGRAM_E_SHAPE, "n_cols %d does not fit shared memory", n_cols);
+  *stages = s;
+  *smem = static_cast<size_t>(kWarps) * s * per_stage;
+  return ENGRAM_OK;
+}
+
+template <class RowSource>
+int launch_ldgsts(const GatherArgs& a, const RowSource& src, size_t smem, int sms, cudaStream_t st) {
+  cudaError_t err = cudaFuncSetAttribute(gather_ldgsts_kernel<RowSource>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(gather): %s", cudaGetErrorString(err));
+  const int64_t want = (a.n_tokens + kWarps - 1) / kWarps;
+  const int blocks = static_cast<int>(want < sms ? want : sms);
+  gather_ldgsts_kernel<RowSource><<<blocks, kWarps * 32, smem, st>>>(a, src);
+  return check_launch("gather_ldgsts_kernel");
+}
+
+}  // namespace
+}  // namespace engram
+
 extern "C" int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows,
                                      int64_t table_bytes, const int32_t* row_ids_d,
                                      int64_t n_tokens, int32_t n_cols, uint16_t* e_d,
@@ -362,25 +426,53 @@ extern "C" int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows,
   int sms = 0;
   int rc = check_device(&sms);
   if (rc) return rc;
-  const int smem_max = 227 * 1024;
-  const int per_stage = n_cols * kSlot + 16;  // slots + mbarrier + two masks
-  int stages = smem_max / (kWarps * per_stage);
-  if (stages > 4) stages = 4;
-  if (stages < 1) return fail(ENGRAM_E_SHAPE, "n_cols %d does not fit shared memory", n_cols);
-  const size_t smem = static_cast<size_t>(kWarps) * stages * per_stage;
-  cudaError_t err = cudaFuncSetAttribute(use_ldgsts() ? gather_ldgsts_kernel : gather_dequant_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+  int stages = 0;
+  size_t smem = 0;
+  if ((rc = gather_config(n_cols, &stages, &smem))) return rc;
+  GatherArgs a{table_d, total_rows, table_bytes, row_ids_d, n_tokens, n_cols, stages, e_d, status_d};
+  if (use_ldgsts()) return launch_ldgsts(a, IdRows{row_ids_d}, smem, sms, as_stream(stream));
+  cudaError_t err = cudaFuncSetAttribute(gather_dequant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
   if (err != cudaSuccess)
     return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(gather): %s", cudaGetErrorString(err));
-  GatherArgs a{table_d, total_rows, table_bytes, row_ids_d, n_tokens, n_cols, stages, e_d, status_d};
   const int64_t want = (n_tokens + kWarps - 1) / kWarps;
   const int blocks = static_cast<int>(want < sms ? want : sms);
-  if (use_ldgsts()) {
-    gather_ldgsts_kernel<<<blocks, kWarps * 32, smem, as_stream(stream)>>>(a);
-    return check_launch("gather_ldgsts_kernel");
-  }
   gather_dequant_kernel<<<blocks, kWarps * 32, smem, as_stream(stream)>>>(a);
   return check_launch("gather_dequant_kernel");
+}
+
+extern "C" int engram_hash_gather(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
+                                  int64_t n_tokens, const int64_t* cu_seqlens_d, int32_t n_seqs,
+                                  const int32_t* token_map_d, int64_t vocab_raw, int32_t* hist_d,
+                                  const uint8_t* table_d, int64_t table_bytes, uint16_t* e_d, uint8_t* mask_d,
+                                  int32_t* row_ids_d, int32_t* status_d, void* stream) {
+  hashdev::HashConsts c;
+  int rc = hashdev::make_consts(layout, layer, vocab_raw, &c);
+  if (rc) return rc;
+  const int64_t total_rows = layout->total_rows[layer];
+  if (n_tokens < 0 || n_seqs < 1) return fail(ENGRAM_E_INVALID, "n_tokens < 0 or n_seqs < 1");
+  if (table_bytes < total_rows * kRowBytes)
+    return fail(ENGRAM_E_SHAPE, "table_bytes %lld < total_rows * 264", (long long)table_bytes);
+  if (n_tokens == 0 && hist_d == nullptr) return ENGRAM_OK;
+  if (!cu_seqlens_d || !token_map_d || (n_tokens > 0 && (!raw_ids_d || !table_d || !e_d || !mask_d)))
+    return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (n_tokens > 0 && (!aligned(table_d, 16) || !aligned(e_d, 16)))
+    return fail(ENGRAM_E_ALIGN, "table and e must be 16-byte aligned");
+  int sms = 0;
+  if ((rc = check_device(&sms))) return rc;
+  cudaStream_t st = as_stream(stream);
+  if (n_tokens > 0) {
+    int stages = 0;
+    size_t smem = 0;
+    if ((rc = gather_config(c.n_cols, &stages, &smem))) return rc;
+    GatherArgs a{table_d, total_rows, table_bytes, nullptr, n_tokens, c.n_cols, stages, e_d, status_d};
+    HashedRows src{c, raw_ids_d, cu_seqlens_d, n_seqs, token_map_d, hist_d, row_ids_d, mask_d, status_d};
+    if ((rc = launch_ldgsts(a, src, smem, sms, st))) return rc;
+  }
+  // the history advances after every position has read the old one
+  if (hist_d != nullptr)
+    return hashdev::launch_hist_commit(c, raw_ids_d, cu_seqlens_d, n_seqs, token_map_d, hist_d, status_d, st);
+  return ENGRAM_OK;
 }
 
 extern "C" int engram_dequant_rows(const uint8_t* rows_d, int64_t n_rows, int64_t rows_bytes, int32_t n_cols,

@@ -15,156 +15,21 @@
 #include <stdint.h>
 
 #include "engram_internal.h"
+#include "hash_device.cuh"
 
 namespace engram {
+using namespace hashdev;
 namespace {
-
-constexpr int kDead = ENGRAM_DEAD;
-
-struct HashConsts {
-  uint64_t mult[ENGRAM_MAX_NGRAM];
-  uint64_t recip[ENGRAM_MAX_COLS];
-  uint32_t prime[ENGRAM_MAX_COLS];
-  uint32_t offset[ENGRAM_MAX_COLS];
-  int32_t n_cols;
-  int32_t n_heads;
-  int32_t max_ngram;
-  int32_t pad_id;
-  int64_t vocab;      // V (compressed)
-  int64_t vocab_raw;  // V_raw
-};
-
-int make_consts(const engram_layout* L, int layer, int64_t vocab_raw, HashConsts* c) {
-  if (L == nullptr) return fail(ENGRAM_E_INVALID, "null layout");
-  if (layer < 0 || layer >= L->n_layers)
-    return fail(ENGRAM_E_INVALID, "layer %d not in [0, %d)", layer, L->n_layers);
-  if (L->n_cols < 1 || L->n_cols > ENGRAM_MAX_COLS || L->max_ngram < 2 ||
-      L->max_ngram > ENGRAM_MAX_NGRAM || L->n_cols != (L->max_ngram - 1) * L->n_heads)
-    return fail(ENGRAM_E_SHAPE, "layout has inconsistent column counts");
-  if (vocab_raw < 1 || vocab_raw > INT32_MAX) return fail(ENGRAM_E_INVALID, "bad vocab_raw");
-  for (int j = 0; j < L->n_cols; ++j) {
-    int64_t p = L->primes[layer][j];
-    int64_t o = L->offsets[layer][j];
-    if (p < 2 || p >= (int64_t(1) << 31) || o < 0 || o + p > (int64_t(1) << 31))
-      return fail(ENGRAM_E_RANGE, "column %d prime/offset out of the int32 row range", j);
-    c->prime[j] = static_cast<uint32_t>(p);
-    c->offset[j] = static_cast<uint32_t>(o);
-    c->recip[j] = ~0ull / static_cast<uint64_t>(p);  // recomputed: never trust a stale field
-  }
-  for (int i = 0; i < L->max_ngram; ++i) c->mult[i] = static_cast<uint64_t>(L->multipliers[layer][i]);
-  c->n_cols = L->n_cols;
-  c->n_heads = L->n_heads;
-  c->max_ngram = L->max_ngram;
-  c->pad_id = L->pad_id;
-  c->vocab = L->vocab_compressed;
-  c->vocab_raw = vocab_raw;
-  return ENGRAM_OK;
-}
-
-// x mod p for any 64-bit x, with r = floor((2^64-1)/p) precomputed (Barrett
-// reduction, Barrett 1986).  q = floor(x r / 2^64) is floor(x/p) or one less,
-// so a single conditional subtraction finishes.
-__device__ __forceinline__ uint32_t mod_prime(uint64_t x, uint32_t p, uint64_t r) {
-  uint64_t q = __umul64hi(x, r);
-  uint64_t rem = x - q * static_cast<uint64_t>(p);
-  if (rem >= p) rem -= p;
-  return static_cast<uint32_t>(rem);
-}
-
-// Compressed id of one raw id, DEAD for an image position; an invalid raw id
-// or map value reports ENGRAM_ST_BAD_TOKEN and becomes DEAD (masked).
-__device__ __forceinline__ int32_t compress_id(int32_t raw, const int32_t* __restrict__ tmap,
-                                               const HashConsts& c, int32_t* status) {
-  if (raw == kDead) return kDead;
-  if (raw < 0 || static_cast<int64_t>(raw) >= c.vocab_raw) {
-    if (status) atomicOr(status, static_cast<int>(ENGRAM_ST_BAD_TOKEN));
-    return kDead;
-  }
-  int32_t x = __ldg(tmap + raw);
-  if (x < 0 || static_cast<int64_t>(x) >= c.vocab) {
-    if (status) atomicOr(status, static_cast<int>(ENGRAM_ST_BAD_TOKEN));
-    return kDead;
-  }
-  return x;
-}
-
-// A history entry must be DEAD or a compressed id.
-__device__ __forceinline__ int32_t check_hist(int32_t x, const HashConsts& c, int32_t* status) {
-  if (x == kDead) return kDead;
-  if (x < 0 || static_cast<int64_t>(x) >= c.vocab) {
-    if (status) atomicOr(status, static_cast<int>(ENGRAM_ST_BAD_TOKEN));
-    return kDead;
-  }
-  return x;
-}
-
-// Given the window slot held by lane i < max_ngram (slot i = x'_{t-i}),
-// applies the DEAD cascade, forms the mixes and writes the row ids of one
-// position.  All 32 lanes call it.
-__device__ __forceinline__ void hash_window(int32_t my_slot, const HashConsts& c,
-                                            int32_t* __restrict__ rows_out, uint8_t* mask_out,
-                                            bool force_mask) {
-  const uint32_t lane = lane_id();
-  // [P-V41] image tokens / [P-LMNT] §多模态细节: looking back, the first DEAD
-  // slot and every slot farther back count as pad.
-  uint64_t g[ENGRAM_MAX_NGRAM];
-  bool dead_seen = false;
-  bool self_dead = false;
-#pragma unroll
-  for (int i = 0; i < ENGRAM_MAX_NGRAM; ++i) {
-    int32_t v = __shfl_sync(0xffffffffu, my_slot, i);
-    if (i < c.max_ngram) {
-      if (v == kDead) {
-        dead_seen = true;
-        if (i == 0) self_dead = true;
-      }
-      g[i] = static_cast<uint64_t>(dead_seen ? c.pad_id : v);
-    } else {
-      g[i] = 0;
-    }
-  }
-  if (lane < static_cast<uint32_t>(c.n_cols)) {
-    // [P-V41] eq. (H): mix_n = XOR_{i<n} x'_{t-i} * m_i; column j is order
-    // n = 2 + j / n_heads ([P-DS4] step 3: row = mix mod p + offset).
-    const int n = 2 + static_cast<int>(lane) / c.n_heads;
-    uint64_t mix = 0;
-#pragma unroll
-    for (int i = 0; i < ENGRAM_MAX_NGRAM; ++i)
-      if (i < n) mix ^= g[i] * c.mult[i];
-    const uint32_t z = mod_prime(mix, c.prime[lane], c.recip[lane]);
-    rows_out[lane] = static_cast<int32_t>(z + c.offset[lane]);
-  }
-  if (lane == 0) *mask_out = (self_dead || force_mask) ? 1 : 0;
-}
 
 __global__ void __launch_bounds__(256) hash_prefill_kernel(
     HashConsts c, const int32_t* __restrict__ raw, int64_t n_tokens,
     const int64_t* __restrict__ cu, int32_t n_seqs, const int32_t* __restrict__ tmap,
     const int32_t* __restrict__ hist, int32_t* __restrict__ rows, uint8_t* __restrict__ mask,
     int32_t* status) {
-  const uint32_t lane = lane_id();
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-  const int depth = c.max_ngram - 1;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
        t < n_tokens; t += warps) {
-    // sequence of position t: largest s with cu[s] <= t
-    int lo = 0, hi = n_seqs - 1;
-    while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
-    }
-    const int64_t start = __ldg(cu + lo);
-    int32_t slot = c.pad_id;
-    if (lane < static_cast<uint32_t>(c.max_ngram)) {
-      const int64_t src = t - static_cast<int64_t>(lane);
-      if (src >= start) {
-        slot = compress_id(__ldg(raw + src), tmap, c, status);
-      } else if (hist != nullptr) {
-        // before the chunk start: carried history, most recent first
-        const int64_t hidx = static_cast<int64_t>(lane) - 1 - (t - start);
-        slot = check_hist(__ldg(hist + static_cast<int64_t>(lo) * depth + hidx), c, status);
-      }
-    }
+    const int32_t slot = prefill_slot(c, t, raw, cu, n_seqs, tmap, hist, status);
     hash_window(slot, c, rows + t * c.n_cols, mask + t, false);
   }
 }
@@ -183,27 +48,10 @@ __global__ void __launch_bounds__(256) hash_all_layers_kernel(
     int32_t n_seqs, const int32_t* __restrict__ tmap, const int32_t* __restrict__ hist,
     int32_t* __restrict__ rows, uint8_t* __restrict__ mask, int32_t* status) {
   const HashConsts& c = ca.l[0];
-  const uint32_t lane = lane_id();
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-  const int depth = c.max_ngram - 1;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; t < n_tokens;
        t += warps) {
-    int lo = 0, hi = n_seqs - 1;
-    while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
-    }
-    const int64_t start = __ldg(cu + lo);
-    int32_t slot = c.pad_id;
-    if (lane < static_cast<uint32_t>(c.max_ngram)) {
-      const int64_t src = t - static_cast<int64_t>(lane);
-      if (src >= start) {
-        slot = compress_id(__ldg(raw + src), tmap, c, status);
-      } else if (hist != nullptr) {
-        const int64_t hidx = static_cast<int64_t>(lane) - 1 - (t - start);
-        slot = check_hist(__ldg(hist + static_cast<int64_t>(lo) * depth + hidx), c, status);
-      }
-    }
+    const int32_t slot = prefill_slot(c, t, raw, cu, n_seqs, tmap, hist, status);
     for (int li = 0; li < ca.n_layers; ++li)
       hash_window(slot, ca.l[li], rows + (static_cast<int64_t>(li) * n_tokens + t) * c.n_cols, mask + t, false);
   }
@@ -285,6 +133,13 @@ __global__ void selftest_mod_kernel(HashConsts c, const uint64_t* __restrict__ x
 }
 
 }  // namespace
+
+int hashdev::launch_hist_commit(const HashConsts& c, const int32_t* raw, const int64_t* cu, int32_t n_seqs,
+                                const int32_t* tmap, int32_t* hist, int32_t* status, cudaStream_t st) {
+  hash_commit_kernel<<<(n_seqs + 127) / 128, 128, 0, st>>>(c, raw, cu, n_seqs, tmap, hist, status);
+  return check_launch("hash_commit_kernel");
+}
+
 }  // namespace engram
 
 using namespace engram;

@@ -223,6 +223,24 @@ int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows, int64_t ta
                           const int32_t* row_ids_d, int64_t n_tokens, int32_t n_cols,
                           uint16_t* e_d, int32_t* status_d, void* stream);
 
+/* Stages 1-4 fused: the prefill hash of engram_hash and the gather of
+ * engram_gather_dequant in one kernel.  The warp that gathers a position's
+ * rows computes their ids from the position's token window, so the ids need
+ * not round-trip through memory ([P-O1] §2.4: the rows depend only on the
+ * token ids).  Arguments as in engram_hash and engram_gather_dequant, with
+ * the table of layer `layer` (total_rows from the layout):
+ *   table_d      uint8 [total_rows][264], 16-byte aligned; table_bytes >= total_rows * 264
+ *   e_d          bf16 [n_tokens][n_cols*256] out, 16-byte aligned
+ *   mask_d       uint8 [n_tokens] out (1 = DEAD position)
+ *   row_ids_d    int32 [n_tokens][n_cols] out, or NULL (not written)
+ *   hist_d       int32 [n_seqs][max_ngram-1] in/out carried history, or NULL
+ * The history is advanced by a second launch after every position has read
+ * it.  Status bits as for the two calls it fuses. */
+int engram_hash_gather(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d, int64_t n_tokens,
+                       const int64_t* cu_seqlens_d, int32_t n_seqs, const int32_t* token_map_d, int64_t vocab_raw,
+                       int32_t* hist_d, const uint8_t* table_d, int64_t table_bytes, uint16_t* e_d,
+                       uint8_t* mask_d, int32_t* row_ids_d, int32_t* status_d, void* stream);
+
 /* Dequantise rows that already sit contiguously in device memory (e.g. after
  * a host-side gather and one DMA): e_d[i/n_cols][256*(i%n_cols) + c] from
  * row i of rows_d, for i < n_rows (a multiple of n_cols).  Same arithmetic as
