@@ -41,6 +41,11 @@ GATHER_BYTES_PER_TOKEN = 4 + 24 * 264 + 24 * 256 * 2   # raw id + 24 rows + bf16
 KERNEL_FILES = ["project.cu", "gather.cu", "hash.cu", "gate.cu", "shortconv.cu", "engram_internal.h"]
 
 
+def GATE_BYTES_PER_TOKEN(hc: int, hidden: int) -> int:
+    """Gate + residual add: h read and written (bf16), v read, the partial sums read, the mask."""
+    return 2 * hc * hidden * 2 + hidden * 2 + hc * (hidden // 256) * 16 + 1
+
+
 def CONV_BYTES_PER_TOKEN(hc: int, hidden: int) -> int:
     """Short convolution + residual: h read and written (bf16), v and the gates read once."""
     return 2 * hc * hidden * 2 + hidden * 2 + hc * 4
@@ -57,6 +62,8 @@ def parse():
     p.add_argument("--micro-steps", type=int, default=30, help="steps of the hash+gather microbench phase")
     p.add_argument("--decode-steps", type=int, default=200, help="steps of the decode phase")
     p.add_argument("--conv-steps", type=int, default=30, help="steps of the short-convolution layer phase")
+    p.add_argument("--fullscale-passes", type=int, default=2,
+                   help="timed passes over the 131,072-token full-scale sequence (101 GB table; 0 skips it)")
     p.add_argument("--host-steps", type=int, default=20,
                    help="steps of the host-resident table phase (0 skips it and its pinned allocation)")
     p.add_argument("--cpu-sample", type=int, default=8192, help="tokens of the oracle CPU baseline sample")
@@ -234,16 +241,14 @@ def run_ours(args, rank, world, local):
         # one pass of the whole layer; events between the stage launches when timing
         if ev is not None:
             ev[0].record(stream)
-        eg.engram_hash(layer.layout, 0, raw, cu, layer.token_map, hist, b_["rows"], b_["mask"], status)
+        eg.engram_hash_gather(layer.layout, 0, raw, cu, layer.token_map, layer.table, hist, b_["e"], b_["mask"],
+                              None, status)
         if ev is not None:
             ev[1].record(stream)
-        eg.engram_gather_dequant(layer.table, layer.total_rows, b_["rows"], b_["e"], status)
-        if ev is not None:
-            ev[2].record(stream)
         eg.engram_project_gate(b_["e"], layer.wkv_packed, h, layer.q_w, layer.k_w, b_["mask"], layer.eps,
                                layer.clamp, layer.score_scale, None, b_["work"], status)
         if ev is not None:
-            ev[3].record(stream)
+            ev[2].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -252,7 +257,7 @@ def run_ours(args, rank, world, local):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during warm-up")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     props = torch.cuda.get_device_properties(dev)
     gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) is not None else str(local)
     sampler = ClockSampler(gpu_id)
@@ -275,9 +280,9 @@ def run_ours(args, rank, world, local):
     def ms(k, i, j):
         return events[k][i].elapsed_time(events[k][j])
 
-    step_ms = [ms(k, 0, 3) for k in range(args.steps)]
+    step_ms = [ms(k, 0, 2) for k in range(args.steps)]
     stage = {name: [ms(k, i, i + 1) for k in range(args.steps)]
-             for i, name in enumerate(["hash", "gather", "project_gate"])}
+             for i, name in enumerate(["hash_gather", "project_gate"])}
     total_s = reduce_max(sum(step_ms) / 1e3, world, dev)
 
     # ---- end to end: host buffers through the public layer API.  Each step
@@ -289,11 +294,13 @@ def run_ours(args, rank, world, local):
     if args.e2e_steps > 0:
         e2e = e2e_pipeline(args, b, h0, layer, hist, status, dev, world)
 
+    hgg = hash_gather_gate_bench(args, w, inp, layer, flush, dev) if args.micro_steps > 0 else None
     micro = microbench(args, w, inp, layer, flush, dev) if args.micro_steps > 0 else None
     dec = decode_bench(args, w, inp, layer, flush, dev) if args.decode_steps > 0 else None
     conv = conv_bench(args, w, inp, layer, flush, dev) if args.conv_steps > 0 else None
     host = host_table_bench(args, w, inp, layer, flush, dev, statistics.mean(step_ms)) \
         if args.host_steps > 0 else None
+    full = fullscale_bench(args, inp, layer, dev) if args.fullscale_passes > 0 else None
 
     if rank != 0:
         return None
@@ -304,6 +311,12 @@ def run_ours(args, rank, world, local):
     if micro is not None:
         micro["frac"] = micro["gather_gbs"] / peaks["hbm_gbs"]
         micro["peak_gbs"] = peaks["hbm_gbs"]
+        micro["uniform_control"]["frac"] = micro["uniform_control"]["gather_gbs"] / peaks["hbm_gbs"]
+    if hgg is not None:
+        hgg["gate_frac_hbm"] = hgg["gate_gbs"] / peaks["hbm_gbs"]
+        hgg["hash_gather_frac_hbm"] = hgg["hash_gather_gbs"] / peaks["hbm_gbs"]
+    if full is not None and "hash_gather_gbs" in full:
+        full["hash_gather_frac_hbm"] = full["hash_gather_gbs"] / peaks["hbm_gbs"]
     if dec is not None:
         dec["wkv_frac_hbm"] = dec["wkv_gbs"] / peaks["hbm_gbs"]
     if conv is not None:
@@ -315,7 +328,7 @@ def run_ours(args, rank, world, local):
     tf_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     flops = 2.0 * T * 6144 * (w.hc + 1) * w.hidden
     proj_s = statistics.mean(stage["project_gate"]) / 1e3
-    gat_s = statistics.mean(stage["gather"]) / 1e3
+    gat_s = statistics.mean(stage["hash_gather"]) / 1e3
     roof = {"bound": "tensor",
             "kernel": "project2_kernel<fused> (CTA-pair tcgen05 wkv GEMM, gate and residual in the epilogue)",
             "achieved": flops / proj_s / 1e12, "peak": tf_peak, "unit": "TFLOP/s",
@@ -324,9 +337,9 @@ def run_ours(args, rank, world, local):
             "algorithmic_per_launch": f"{flops:.4g} FLOP (2*T*6144*{(w.hc + 1) * w.hidden}, T={T})",
             "peak_source": f"{peak_src} bf16_tflops{'_sustained' if sustained else ''}"}
     gbytes = GATHER_BYTES_PER_TOKEN * T
-    gather_kernel = "gather_dequant_kernel" if os.environ.get("ENGRAM_GATHER", "").startswith("b") \
-        else "gather_ldgsts_kernel"
-    roof_g = {"bound": "hbm", "kernel": gather_kernel, "achieved": gbytes / gat_s / 1e9,
+    gather_kernel = "gather_ldgsts_kernel"
+    roof_g = {"bound": "hbm", "kernel": "gather_ldgsts_kernel<HashedRows> (hash fused into the gather) + the history "
+                                        "commit", "achieved": gbytes / gat_s / 1e9,
               "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbytes / gat_s / 1e9 / peaks["hbm_gbs"],
               "traffic": traffic.get(gather_kernel),
               "algorithmic_per_launch": f"{gbytes} B ({GATHER_BYTES_PER_TOKEN} B/token, T={T})",
@@ -349,11 +362,13 @@ def run_ours(args, rank, world, local):
         "stages_ms": {k: statistics.mean(v) for k, v in stage.items()},
         "roofline": roof,
         "roofline_gather": roof_g,
+        "hash_gather_gate": hgg,
         "microbench_hash_gather": micro,
         "decode_step": dec,
         "short_conv_layer": conv,
+        "fullscale": full,
         "host_table": host,
-        "gpu_launches": args.steps * 4,
+        "gpu_launches": args.steps * 3,
         "clocks": clocks,
         "e2e": e2e,
         "wall_s_timed": wall1 - wall0,
@@ -422,6 +437,117 @@ def e2e_pipeline(args, b, h0, layer, hist, status, dev, world):
                    "move while step k computes"}
 
 
+def hash_gather_gate_bench(args, w, inp, layer, flush, dev):
+    """The layer without the wkv GEMM (the metric's hash + gather + gate): the
+    fused hash + gather, then the gate and residual add from partial sums and
+    v produced once, outside the timed region, by the projection."""
+    import torch
+    import hashed_gram_conditional_gb300 as eg
+
+    b = inp["batch"]
+    T = len(b.raw_ids)
+    raw = torch.from_numpy(b.raw_ids).to(dev)
+    cu = torch.from_numpy(b.cu_seqlens).to(dev)
+    h = inp["bf16"](inp["h_bits"])
+    e, mask = eg.engram_hash_gather(layer.layout, 0, raw, cu, layer.token_map, layer.table)
+    partials, v = eg.engram_project(e, layer.wkv_packed, h, layer.q_w, layer.k_w)
+    stream = torch.cuda.current_stream(dev)
+
+    def run(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        eg.engram_hash_gather(layer.layout, 0, raw, cu, layer.token_map, layer.table, None, e, mask)
+        if ev is not None:
+            ev[1].record(stream)
+        eg.engram_gate_add(partials, v, h, mask, layer.eps, layer.clamp, layer.score_scale)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(3):
+        flush.zero_()
+        run()
+    n = args.micro_steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for k in range(n):
+        flush.zero_()
+        run(evs[k])
+    torch.cuda.synchronize()
+    step = statistics.mean(ev[0].elapsed_time(ev[2]) for ev in evs) / 1e3
+    hg = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs) / 1e3
+    gate = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs) / 1e3
+    gb = GATE_BYTES_PER_TOKEN(w.hc, w.hidden) * T
+    return {"workload": f"{w.name} batch ({T} tokens), L2 flushed before every step", "steps": n,
+            "tokens_per_s": T / step, "ms_per_step": step * 1e3, "hash_gather_ms": hg * 1e3, "gate_ms": gate * 1e3,
+            "hash_gather_gbs": GATHER_BYTES_PER_TOKEN * T / hg / 1e9, "gate_gbs": gb / gate / 1e9,
+            "gate_algorithmic_bytes": gb, "kernels": "gather_ldgsts_kernel<HashedRows> + gate_add_kernel"}
+
+
+def fullscale_bench(args, inp, layer, dev):
+    """The full-scale configuration: a 384,006,168-row (101.4 GB) table from
+    base 16,000,000 and one 131,072-token sequence prefilled in 8 chunks of
+    16,384 with the history carried; the same projection weights."""
+    import torch
+    import hashed_gram_conditional_gb300 as eg
+    from workloads import WORKLOADS, prefill_batch, token_map
+
+    wf = WORKLOADS["fullscale"]
+    tm = token_map(wf.v_raw, wf.v, wf.seed)
+    lay = eg.build_layout(wf.v, wf.base_rows, [wf.layer_id], pad_id=int(tm[0]), expected_vocab=wf.v)
+    total = lay.total_rows(0)
+    free, _ = torch.cuda.mem_get_info(dev)
+    if free < total * eg.ROW_BYTES + (6 << 30):
+        return {"skipped": f"needs {total * eg.ROW_BYTES / 1e9:.1f} GB free, {free / 1e9:.1f} GB available"}
+    table = torch.empty(total * eg.ROW_BYTES, dtype=torch.uint8, device=dev)
+    eg.engram_fill_synthetic_table(table, total, wf.seed)
+    fl = eg.EngramLayer(lay, 0, table, torch.from_numpy(tm).to(dev), layer.wkv_packed, layer.q_w, layer.k_w)
+    b = prefill_batch(wf)
+    T = len(b.raw_ids)
+    C = T // wf.chunks
+    raw = torch.from_numpy(b.raw_ids).to(dev)
+    cu = torch.tensor([0, C], dtype=torch.int64, device=dev)
+    h = inp["bf16"](inp["h_bits"][:C])
+    hist = torch.full((1, 3), lay.pad_id, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    buf = fl._buffers(C, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one_pass(evs=None):
+        hist.fill_(lay.pad_id)
+        for c in range(wf.chunks):
+            if evs is not None:
+                evs[c][0].record(stream)
+            eg.engram_hash_gather(lay, 0, raw[c * C:(c + 1) * C], cu, fl.token_map, table, hist, buf["e"],
+                                  buf["mask"], None, status)
+            if evs is not None:
+                evs[c][1].record(stream)
+            eg.engram_project_gate(buf["e"], fl.wkv_packed, h, fl.q_w, fl.k_w, buf["mask"], fl.eps, fl.clamp,
+                                   fl.score_scale, None, buf["work"], status)
+            if evs is not None:
+                evs[c][2].record(stream)
+
+    one_pass()
+    torch.cuda.synchronize()
+    res = []
+    for _ in range(args.fullscale_passes):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(wf.chunks)]
+        one_pass(evs)
+        torch.cuda.synchronize()
+        res.append(evs)
+    tot = sum(ev[c][0].elapsed_time(ev[c][2]) for ev in res for c in range(wf.chunks)) / 1e3
+    hg = sum(ev[c][0].elapsed_time(ev[c][1]) for ev in res for c in range(wf.chunks)) / 1e3
+    n_tok = T * args.fullscale_passes
+    out = {"workload": f"fullscale: 1 x {T} Zipf(1.1) tokens in {wf.chunks} chunks of {C}, history carried, "
+                       f"{total * eg.ROW_BYTES / 1e9:.1f} GB table (primes above {wf.base_rows})",
+           "passes": args.fullscale_passes, "tokens_per_s": n_tok / tot, "ms_per_chunk": tot / (wf.chunks *
+                                                                                                 args.fullscale_passes) * 1e3,
+           "hash_gather_ms_per_chunk": hg / (wf.chunks * args.fullscale_passes) * 1e3,
+           "hash_gather_gbs": GATHER_BYTES_PER_TOKEN * n_tok / hg / 1e9, "device_status": int(status.item()),
+           "note": "chunks run back to back (no L2 flush; the table is 101 GB, so rows come from HBM)"}
+    del fl, table
+    torch.cuda.empty_cache()
+    return out
+
+
 def microbench(args, w, inp, layer, flush, dev):
     """Hash + gather only on the 65,536-token microbench workload (same table)."""
     import torch
@@ -461,9 +587,23 @@ def microbench(args, w, inp, layer, flush, dev):
     step = statistics.mean(ev[0].elapsed_time(ev[2]) for ev in evs) / 1e3
     gat = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs) / 1e3
     gbytes = GATHER_BYTES_PER_TOKEN * T
+    # control: uniformly random tokens (no Zipf reuse of hot rows in L2)
+    g = np.random.default_rng(wm.seed + 77)
+    raw = torch.from_numpy(g.integers(0, wm.v_raw, size=T).astype(np.int32)).to(dev)
+    for _ in range(3):
+        flush.zero_()
+        run()
+    evu = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.micro_steps)]
+    for k in range(args.micro_steps):
+        flush.zero_()
+        run(evu[k])
+    torch.cuda.synchronize()
+    gat_u = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evu) / 1e3
     return {"workload": f"microbench: 1 x {T} Zipf(1.1) tokens, same 12.67 GB table", "steps": args.micro_steps,
             "hash_gather_tokens_per_s": T / step, "hash_ms": (step - gat) * 1e3, "gather_ms": gat * 1e3,
-            "gather_gbs": gbytes / gat / 1e9, "algorithmic_bytes": gbytes}
+            "gather_gbs": gbytes / gat / 1e9, "algorithmic_bytes": gbytes,
+            "uniform_control": {"tokens": "uniform over the raw vocabulary", "gather_ms": gat_u * 1e3,
+                                "gather_gbs": gbytes / gat_u / 1e9}}
 
 
 def decode_bench(args, w, inp, layer, flush, dev):
