@@ -10,9 +10,10 @@
 //           (the gate runs in fp32)
 //
 // HBM-bound: per position it reads hc*H bf16 of h and H bf16 of v and writes
-// hc*H bf16 of h.  One CTA handles one position at a time; warp 0 reduces the
-// partial sums in a fixed order (deterministic), then all threads stream the
-// row with 16-byte vectors, reusing each v vector for every stream.
+// hc*H bf16 of h.  A CTA handles 8 positions at a time: each warp reduces one
+// position's partial sums in a fixed order (deterministic), then all threads
+// stream the 8 rows with 16-byte vectors, reusing each v vector for every
+// stream.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -36,74 +37,97 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t h, float g, uint32_t v) 
   return pack_bf16(bf16_lo(h) + g * bf16_lo(v), bf16_hi(h) + g * bf16_hi(v));
 }
 
+// The gate of position t, stream m, from the projection's partial sums
+// (reduced over the tiles by the warp's lanes, then across lanes); lane 0
+// holds the result.
+__device__ __forceinline__ float warp_gate(const float4* __restrict__ partials, int64_t t, int m, int hc, int ntile,
+                                           float inv_h, float eps, float clamp, float score_scale) {
+  const int lane = threadIdx.x & 31;
+  float dot = 0.f, kk = 0.f, hh = 0.f;
+  const float4* p = partials + (t * hc + m) * ntile;
+  for (int q = lane; q < ntile; q += 32) {
+    const float4 x = __ldg(p + q);
+    dot += x.x;
+    kk += x.y;
+    hh += x.z;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    kk += __shfl_xor_sync(0xffffffffu, kk, o);
+    hh += __shfl_xor_sync(0xffffffffu, hh, o);
+  }
+  // s = dot * rstd(h) * rstd(k) * scale; gate = sigmoid(signed sqrt(s))
+  const float sc = dot * (1.0f / sqrtf(hh * inv_h + eps)) * (1.0f / sqrtf(kk * inv_h + eps)) * score_scale;
+  const float z = copysignf(sqrtf(fmaxf(fabsf(sc), clamp)), sc);
+  return 1.0f / (1.0f + expf(-z));
+}
+
+// A CTA takes P <= 8 positions at a time (P is chosen so that small batches
+// still spread over the SMs): warp w < P finishes the gates of position w,
+// then all 256 threads stream the P positions' rows (v once, every stream of
+// h read and written) with 16-byte vectors.
+constexpr int kPosPerCta = 8;
+
 __global__ void __launch_bounds__(256) gate_add_kernel(
     const float4* __restrict__ partials, const uint4* __restrict__ v, uint4* h,
     const uint8_t* __restrict__ mask, int64_t n_tokens, int hidden, int hc, float eps,
-    float clamp, float score_scale, float* __restrict__ gate_out) {
-  __shared__ float gs[kMaxHc];
+    float clamp, float score_scale, float* __restrict__ gate_out, int pos_per_cta) {
+  __shared__ float gs[kPosPerCta][kMaxHc];
+  __shared__ uint8_t live[kPosPerCta];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntile = hidden / 256;
   const int nvec = hidden / 8;  // 16-byte vectors per stream row
   const float inv_h = 1.0f / static_cast<float>(hidden);
-  for (int64_t t = blockIdx.x; t < n_tokens; t += gridDim.x) {
-    const bool masked = (mask != nullptr) && mask[t] != 0;
-    if (masked) {
-      // [P-DS4] step 4: the masked branch returns; the gate is 0.
-      if (gate_out != nullptr && threadIdx.x < hc) gate_out[t * hc + threadIdx.x] = 0.0f;
-      continue;
-    }
-    if (threadIdx.x < 32) {
-      const uint32_t lane = threadIdx.x;
+  const int P = pos_per_cta;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * P; base < n_tokens;
+       base += static_cast<int64_t>(gridDim.x) * P) {
+    const int64_t t = base + warp;
+    if (warp < P && t < n_tokens) {
+      // [P-DS4] step 4: a masked position returns untouched; its gate is 0.
+      const bool masked = (mask != nullptr) && mask[t] != 0;
       for (int m = 0; m < hc; ++m) {
-        float dot = 0.f, kk = 0.f, hh = 0.f;
-        const float4* p = partials + (t * hc + m) * ntile;
-        for (int q = lane; q < ntile; q += 32) {
-          const float4 x = p[q];
-          dot += x.x;
-          kk += x.y;
-          hh += x.z;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          dot += __shfl_xor_sync(0xffffffffu, dot, o);
-          kk += __shfl_xor_sync(0xffffffffu, kk, o);
-          hh += __shfl_xor_sync(0xffffffffu, hh, o);
-        }
+        const float g = masked ? 0.f : warp_gate(partials, t, m, hc, ntile, inv_h, eps, clamp, score_scale);
         if (lane == 0) {
-          // s = dot * rstd(h) * rstd(k) * scale; gate = sigmoid(signed sqrt(s))
-          const float s = dot * (1.0f / sqrtf(hh * inv_h + eps)) * (1.0f / sqrtf(kk * inv_h + eps)) *
-                          score_scale;
-          const float z = copysignf(sqrtf(fmaxf(fabsf(s), clamp)), s);
-          const float g = 1.0f / (1.0f + expf(-z));
-          gs[m] = g;
+          gs[warp][m] = g;
           if (gate_out != nullptr) gate_out[t * hc + m] = g;
         }
       }
+      if (lane == 0) live[warp] = masked ? 0 : 1;
+    } else if (warp < P && lane == 0) {
+      live[warp] = 0;
     }
     __syncthreads();
-    float g[kMaxHc];
+    if (h != nullptr) {  // no h: gates only
+      const int work = P * nvec;
+      for (int i = threadIdx.x; i < work; i += blockDim.x) {
+        const int p = i / nvec, j = i - p * nvec;
+        if (!live[p]) continue;
+        const int64_t tp = base + p;
+        const uint4 vv = v[tp * nvec + j];
+        uint4* ht = h + tp * static_cast<int64_t>(hc) * nvec + j;
+        uint4 hv[kMaxHc];
 #pragma unroll
-    for (int m = 0; m < kMaxHc; ++m) g[m] = (m < hc) ? gs[m] : 0.f;
-    const uint4* vt = v + t * nvec;
-    uint4* ht = h + t * static_cast<int64_t>(hc) * nvec;
-    for (int i = threadIdx.x; h != nullptr && i < nvec; i += blockDim.x) {  // no h: gates only
-      const uint4 vv = vt[i];
+        for (int m = 0; m < kMaxHc; ++m)
+          if (m < hc) hv[m] = ht[m * nvec];
 #pragma unroll
-      for (int m = 0; m < kMaxHc; ++m) {
-        if (m >= hc) break;
-        uint4 hv = ht[m * nvec + i];
-        hv.x = fma_bf16x2(hv.x, g[m], vv.x);
-        hv.y = fma_bf16x2(hv.y, g[m], vv.y);
-        hv.z = fma_bf16x2(hv.z, g[m], vv.z);
-        hv.w = fma_bf16x2(hv.w, g[m], vv.w);
-        ht[m * nvec + i] = hv;
+        for (int m = 0; m < kMaxHc; ++m) {
+          if (m >= hc) break;
+          const float g = gs[p][m];
+          uint4 o;
+          o.x = fma_bf16x2(hv[m].x, g, vv.x);
+          o.y = fma_bf16x2(hv[m].y, g, vv.y);
+          o.z = fma_bf16x2(hv[m].z, g, vv.z);
+          o.w = fma_bf16x2(hv[m].w, g, vv.w);
+          ht[m * nvec] = o;
+        }
       }
     }
-    __syncthreads();  // gs is rewritten for the next position
+    __syncthreads();  // gs and live are rewritten for the next 8 positions
   }
 }
 
-// The gates alone (no residual): one warp per position, lanes over the
-// partials' tiles, streams in turn.
+// The gates alone (no residual): one warp per position.
 __global__ void __launch_bounds__(256) gates_kernel(const float4* __restrict__ partials,
                                                     const uint8_t* __restrict__ mask, int64_t n_tokens,
                                                     int hidden, int hc, float eps, float clamp, float score_scale,
@@ -115,25 +139,8 @@ __global__ void __launch_bounds__(256) gates_kernel(const float4* __restrict__ p
   for (int64_t t = blockIdx.x * 8 + (threadIdx.x >> 5); t < n_tokens; t += warps) {
     const bool masked = (mask != nullptr) && mask[t] != 0;
     for (int m = 0; m < hc; ++m) {
-      float dot = 0.f, kk = 0.f, hh = 0.f;
-      const float4* p = partials + (t * hc + m) * ntile;
-      for (int q = lane; q < ntile; q += 32) {
-        const float4 x = __ldg(p + q);
-        dot += x.x;
-        kk += x.y;
-        hh += x.z;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        kk += __shfl_xor_sync(0xffffffffu, kk, o);
-        hh += __shfl_xor_sync(0xffffffffu, hh, o);
-      }
-      if (lane == 0) {
-        const float sc = dot * (1.0f / sqrtf(hh * inv_h + eps)) * (1.0f / sqrtf(kk * inv_h + eps)) * score_scale;
-        const float z = copysignf(sqrtf(fmaxf(fabsf(sc), clamp)), sc);
-        gate_out[t * hc + m] = masked ? 0.0f : 1.0f / (1.0f + expf(-z));
-      }
+      const float g = masked ? 0.f : warp_gate(partials, t, m, hc, ntile, inv_h, eps, clamp, score_scale);
+      if (lane == 0) gate_out[t * hc + m] = g;
     }
   }
 }
@@ -167,11 +174,15 @@ extern "C" int engram_gate_add(const float* partials_d, const uint16_t* v_d, uin
         gate_out_d);
     return check_launch("gates_kernel");
   }
+  // positions per CTA: 8 when there are enough positions for 4 CTAs per SM
+  int P = kPosPerCta;
+  while (P > 1 && (n_tokens + P - 1) / P < 4LL * sms) P >>= 1;
   const int64_t cap = static_cast<int64_t>(sms) * 8;
-  const int blocks = static_cast<int>(n_tokens < cap ? n_tokens : cap);
+  const int64_t need = (n_tokens + P - 1) / P;
+  const int blocks = static_cast<int>(need < cap ? need : cap);
   gate_add_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
       reinterpret_cast<const float4*>(partials_d), reinterpret_cast<const uint4*>(v_d),
       reinterpret_cast<uint4*>(h_d), mask_d, n_tokens, hidden, hc, eps, clamp, score_scale,
-      gate_out_d);
+      gate_out_d, P);
   return check_launch("gate_add_kernel");
 }
