@@ -38,7 +38,21 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Engram layer tokens/s (hash+gather+gate) at T=16k; gather HBM GB/s vs peak"
 GATHER_BYTES_PER_TOKEN = 4 + 24 * 264 + 24 * 256 * 2   # raw id + 24 rows + bf16 e = 18,628 B
-KERNEL_FILES = ["project.cu", "gather.cu", "hash.cu", "gate.cu", "shortconv.cu", "engram_internal.h"]
+# the sources each profiled kernel is built from: a traffic figure is used
+# only while the hash of its kernel's sources matches the one it was taken with
+KERNEL_SOURCES = {
+    "project2_kernel": ["project.cu", "engram_internal.h"],
+    "project2_kernel_unfused": ["project.cu", "engram_internal.h"],
+    "gather_ldgsts_kernel": ["gather.cu", "hash_device.cuh", "engram_internal.h"],
+    "gather_ldgsts_kernel_ids": ["gather.cu", "hash_device.cuh", "engram_internal.h"],
+    "hash_prefill_kernel": ["hash.cu", "hash_device.cuh", "engram_internal.h"],
+    "hash_commit_kernel": ["hash.cu", "hash_device.cuh", "engram_internal.h"],
+    "gates_kernel": ["gate.cu", "engram_internal.h"],
+    "gate_add_kernel": ["gate.cu", "engram_internal.h"],
+    "conv_prep_kernel": ["shortconv.cu", "engram_internal.h"],
+    "conv_add_kernel": ["shortconv.cu", "engram_internal.h"],
+    "conv_state_kernel": ["shortconv.cu", "engram_internal.h"],
+}
 
 
 def GATE_BYTES_PER_TOKEN(hc: int, hidden: int) -> int:
@@ -87,24 +101,32 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_hash():
+def sources_hash(files, read=None) -> str:
+    """Hash of the given kernel sources (read(name) -> bytes; the working tree by default)."""
     h = hashlib.sha256()
-    for f in KERNEL_FILES:
-        with open(os.path.join(ROOT, "hashed_gram_conditional_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for f in files:
+        if read is None:
+            with open(os.path.join(ROOT, "hashed_gram_conditional_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+        else:
+            h.update(read(f))
     return h.hexdigest()[:16]
 
 
 def profiled_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if it matches the kernels."""
+    """Per-launch DRAM bytes from the committed ncu summary, for the kernels
+    whose sources still hash to the values the counters were taken with."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return {}
     with open(path) as f:
         d = json.load(f)
-    if d.get("kernel_hash") != kernel_hash():
-        return {}
-    return d.get("per_launch_bytes", {})
+    out = {}
+    for name, entry in d.get("kernels", {}).items():
+        files = KERNEL_SOURCES.get(name)
+        if files is not None and entry.get("sources_hash") == sources_hash(files):
+            out[name] = entry["bytes_per_launch"]
+    return out
 
 
 class ClockSampler:
