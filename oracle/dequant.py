@@ -11,6 +11,14 @@ Sources:
       outputs bf16.
   [P-V41] §"门控" (e_t is the 6144-dim lookup result): the 24 rows are
       concatenated in column order.
+  [P-O1] §三 / SGLang notes: the wkv projection of the released model runs
+      on block-FP8 weights.
+
+Readings (weights):
+  * Block-FP8 wkv is taken in the same E4M3 x E8M0-per-32 family as the
+    rows, blocked along the contraction axis k (dequant_mx_weights); its
+    values are exact in fp64, so the FP8 projection's oracle is the same fp64
+    GEMM on these values.
 
 Readings:
   * E4M3 is the OCP FP8 E4M3 format (bias 7, no infinities, 0x7F/0xFF are
@@ -85,6 +93,15 @@ def dequant_rows(rows: np.ndarray) -> np.ndarray:
     w = e4m3_value(rows[:, :HEAD_DIM])
     s = e8m0_value(rows[:, HEAD_DIM:HEAD_DIM + HEAD_DIM // BLOCK])
     return bf16_round(w * np.repeat(s, BLOCK, axis=1))
+
+
+def dequant_mx_weights(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Block-FP8 weights to float64: w[k][n] = E4M3(codes[k][n]) * 2^(scales[k // 32][n] - 127),
+    the same E4M3 x E8M0-per-32 family as the table rows, blocked along k (the
+    contraction axis of kv = e @ wkv).  Exact; no rounding."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint8)
+    return e4m3_value(codes) * e8m0_value(np.repeat(scales, BLOCK, axis=0))
 
 
 def gather_dequant(row_ids: np.ndarray, table_rows) -> np.ndarray:

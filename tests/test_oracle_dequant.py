@@ -91,3 +91,14 @@ def test_synthetic_rows_have_no_nan_and_scales_in_range():
     assert len(np.unique(r[:, 256:])) == 11
     v = D.dequant_rows(r)
     assert np.isfinite(v).all()
+
+
+def test_dequant_mx_weights_blocks_along_k():
+    """Row k of column n takes scale row k // 32 of that column."""
+    from oracle.dequant import dequant_mx_weights
+    codes = np.full((64, 2), 0x38, dtype=np.uint8)          # E4M3 1.0
+    codes[31, 1] = 0x7E                                       # 448
+    scales = np.array([[127, 130], [120, 125]], dtype=np.uint8)
+    w = dequant_mx_weights(codes, scales)
+    assert w[0, 0] == 1.0 and w[31, 0] == 1.0 and w[32, 0] == 2.0 ** -7 and w[63, 0] == 2.0 ** -7
+    assert w[31, 1] == 448.0 * 8 and w[32, 1] == 0.25 and w[0, 1] == 8.0

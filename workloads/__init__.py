@@ -306,6 +306,19 @@ def gate_values(tokens: int, hc: int, seed: int, masked: Optional[np.ndarray] = 
     return g
 
 
+def mxfp8_weights(k: int, n: int, seed: int):
+    """A wkv matrix in the block-FP8 checkpoint form: E4M3 codes uint8 [k][n]
+    (uniform bytes, the NaN codes 0x7F / 0xFF replaced by byte ^ 1) and one
+    E8M0 scale per 32 consecutive rows of each column, uint8 [k/32][n],
+    uniform over [114, 118] (factors 2^-13 .. 2^-9)."""
+    g = rng_for(seed, 50)
+    w = g.integers(0, 256, size=(k, n), dtype=np.int64).astype(np.uint8)
+    nan = (w & 0x7F) == 0x7F
+    w[nan] ^= 1
+    sf = (114 + rng_for(seed, 51).integers(0, 5, size=(k // 32, n))).astype(np.uint8)
+    return w, sf
+
+
 def residual_bits(tokens: int, hc: int, hidden: int, seed: int, stream: int = 30) -> np.ndarray:
     """Residual streams h, bf16 bits [T][hc][H], N(0, 1)."""
     return normal_bf16_bits((tokens, hc, hidden), 1.0, seed, stream)
