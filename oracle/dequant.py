@@ -11,8 +11,8 @@ Sources:
       outputs bf16.
   [P-V41] §"门控" (e_t is the 6144-dim lookup result): the 24 rows are
       concatenated in column order.
-  [P-O1] §三 / SGLang notes: the wkv projection of the released model runs
-      on block-FP8 weights.
+  [P-O1] §2.3: the projection weights of the released model are block-FP8,
+      and the table payload is E4M3 with E8M0 block scales.
 
 Readings (weights):
   * Block-FP8 wkv is taken in the same E4M3 x E8M0-per-32 family as the
