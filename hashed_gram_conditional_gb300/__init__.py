@@ -107,6 +107,13 @@ _SIGS = {
     "engram_host_gather_async": [_P, _I64, _P, _I64, _P, _I32, _P, _P],
     "engram_hash_gather": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _I64, _P, _P, _P, _P,
                            _P],
+    "engram_gather_fp8": [_P, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _P],
+    "engram_hash_gather_fp8": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _I64, _P, _P,
+                               _P, _P, _P, _P],
+    "engram_pack_wkv_fp8": [_P, _P, _I64, _I64, _P, _P, _P],
+    "engram_project_fp8": [_P, _P, _I64, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P],
+    "engram_project_gate_fp8": [_P, _P, _I64, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P, _F32, _F32, _F32, _P, _P,
+                                ctypes.c_size_t, _P, _P],
     "engram_short_conv_add": [_P, _P, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _I32, _I32, _F32, _P, _P,
                               _I64, _P, ctypes.c_size_t, _P, _P],
 }
@@ -393,6 +400,127 @@ def engram_hash_gather(layout: Layout, layer: int, raw_ids: torch.Tensor, cu_seq
                                 token_map.numel(), _ptr(hist), _ptr(table), table.numel(), _ptr(e), _ptr(mask),
                                 _ptr(row_ids), _ptr(status), _stream(dev)), "engram_hash_gather")
     return e, mask
+
+
+def engram_gather_fp8(table: torch.Tensor, total_rows: int, row_ids: torch.Tensor,
+                      e8: Optional[torch.Tensor] = None, sf: Optional[torch.Tensor] = None,
+                      status: Optional[torch.Tensor] = None):
+    """Gather without dequantising: (e8 uint8 [T][n_cols*256], sf int32 [n_cols*2][T] words of 4 E8M0 scales)."""
+    L = _load()
+    dev = row_ids.device
+    _need(table, "table", torch.uint8, dev)
+    _need(row_ids, "row_ids", torch.int32)
+    T, C = row_ids.shape
+    if e8 is None:
+        e8 = torch.empty((T, C * HEAD_DIM), dtype=torch.uint8, device=dev)
+    if sf is None:
+        sf = torch.empty((2 * C, T), dtype=torch.int32, device=dev)
+    _need(e8, "e8", torch.uint8, dev, T * C * HEAD_DIM)
+    _need(sf, "sf", torch.int32, dev, 2 * C * T)
+    _check(L.engram_gather_fp8(_ptr(table), total_rows, table.numel(), _ptr(row_ids), T, C, _ptr(e8), _ptr(sf),
+                               _ptr(status), _stream(dev)), "engram_gather_fp8")
+    return e8, sf
+
+
+def engram_hash_gather_fp8(layout: Layout, layer: int, raw_ids: torch.Tensor, cu_seqlens: torch.Tensor,
+                           token_map: torch.Tensor, table: torch.Tensor, hist: Optional[torch.Tensor] = None,
+                           e8: Optional[torch.Tensor] = None, sf: Optional[torch.Tensor] = None,
+                           mask: Optional[torch.Tensor] = None, row_ids: Optional[torch.Tensor] = None,
+                           status: Optional[torch.Tensor] = None):
+    """Hash + gather, FP8 outputs; returns (e8, sf, mask)."""
+    L = _load()
+    dev = raw_ids.device
+    T = raw_ids.numel()
+    C = layout.n_cols
+    _need(raw_ids, "raw_ids", torch.int32)
+    _need(cu_seqlens, "cu_seqlens", torch.int64, dev)
+    _need(token_map, "token_map", torch.int32, dev)
+    _need(table, "table", torch.uint8, dev)
+    n_seqs = cu_seqlens.numel() - 1
+    if hist is not None:
+        _need(hist, "hist", torch.int32, dev, n_seqs * (layout.max_ngram - 1))
+    if e8 is None:
+        e8 = torch.empty((T, C * HEAD_DIM), dtype=torch.uint8, device=dev)
+    if sf is None:
+        sf = torch.empty((2 * C, T), dtype=torch.int32, device=dev)
+    if mask is None:
+        mask = torch.empty(T, dtype=torch.uint8, device=dev)
+    _need(e8, "e8", torch.uint8, dev, T * C * HEAD_DIM)
+    _need(sf, "sf", torch.int32, dev, 2 * C * T)
+    _need(mask, "mask", torch.uint8, dev, T)
+    if row_ids is not None:
+        _need(row_ids, "row_ids", torch.int32, dev, T * C)
+    _check(L.engram_hash_gather_fp8(layout.ref, layer, _ptr(raw_ids), T, _ptr(cu_seqlens), n_seqs, _ptr(token_map),
+                                    token_map.numel(), _ptr(hist), _ptr(table), table.numel(), _ptr(e8), _ptr(sf),
+                                    _ptr(mask), _ptr(row_ids), _ptr(status), _stream(dev)), "engram_hash_gather_fp8")
+    return e8, sf, mask
+
+
+def engram_pack_wkv_fp8(w8: torch.Tensor, sf: torch.Tensor):
+    """Block-FP8 wkv (codes uint8 [K][N], scales uint8 [K/32][N]) -> (packed codes, packed scale words)."""
+    L = _load()
+    dev = w8.device
+    K, N = w8.shape
+    _need(w8, "w8", torch.uint8, dev)
+    _need(sf, "sf", torch.uint8, dev, (K // 32) * N)
+    w8p = torch.empty(K * N, dtype=torch.uint8, device=dev)
+    sfp = torch.empty((K // 128, N), dtype=torch.int32, device=dev)
+    _check(L.engram_pack_wkv_fp8(_ptr(w8), _ptr(sf), K, N, _ptr(w8p), _ptr(sfp), _stream(dev)),
+           "engram_pack_wkv_fp8")
+    return w8p, sfp
+
+
+def engram_project_fp8(e8: torch.Tensor, sfa: torch.Tensor, w8p: torch.Tensor, sfb: torch.Tensor, h: torch.Tensor,
+                       q_w: torch.Tensor, k_w: torch.Tensor, partials: Optional[torch.Tensor] = None,
+                       v: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """engram_project on FP8 operands; returns (partials, v)."""
+    L = _load()
+    dev = e8.device
+    _need(e8, "e8", torch.uint8)
+    T, K = e8.shape
+    _need(h, "h", torch.bfloat16, dev)
+    _, hc, H = h.shape
+    _need(sfa, "sfa", torch.int32, dev, (K // 128) * T)
+    _need(w8p, "w8p", torch.uint8, dev, K * (hc + 1) * H)
+    _need(sfb, "sfb", torch.int32, dev, (K // 128) * (hc + 1) * H)
+    if partials is None:
+        partials = torch.empty(partials_shape(T, H, hc), dtype=torch.float32, device=dev)
+    if v is None:
+        v = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    _need(partials, "partials", torch.float32, dev, T * hc * (H // 256) * 4)
+    _need(v, "v", torch.bfloat16, dev, T * H)
+    _check(L.engram_project_fp8(_ptr(e8), _ptr(sfa), T, K, _ptr(w8p), _ptr(sfb), H, hc, _ptr(h), _ptr(q_w), _ptr(k_w),
+                                _ptr(partials), _ptr(v), _ptr(status), _stream(dev)), "engram_project_fp8")
+    return partials, v
+
+
+def engram_project_gate_fp8(e8: torch.Tensor, sfa: torch.Tensor, w8p: torch.Tensor, sfb: torch.Tensor,
+                            h: torch.Tensor, q_w: torch.Tensor, k_w: torch.Tensor, mask: Optional[torch.Tensor],
+                            eps: float = 1e-6, clamp: float = 1e-6, score_scale: Optional[float] = None,
+                            gate_out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                            status: Optional[torch.Tensor] = None):
+    """engram_project_gate on FP8 operands: h updated in place; returns gate_out (or None)."""
+    L = _load()
+    dev = e8.device
+    _need(e8, "e8", torch.uint8)
+    T, K = e8.shape
+    _need(h, "h", torch.bfloat16, dev)
+    _, hc, H = h.shape
+    _need(sfa, "sfa", torch.int32, dev, (K // 128) * T)
+    _need(w8p, "w8p", torch.uint8, dev, K * (hc + 1) * H)
+    _need(sfb, "sfb", torch.int32, dev, (K // 128) * (hc + 1) * H)
+    if mask is not None:
+        _need(mask, "mask", torch.uint8, dev, T)
+    if gate_out is not None:
+        _need(gate_out, "gate_out", torch.float32, dev, T * hc)
+    if workspace is None:
+        workspace = project_gate_workspace(T, H, hc, dev)
+    if score_scale is None:
+        score_scale = H ** -0.5
+    _check(L.engram_project_gate_fp8(_ptr(e8), _ptr(sfa), T, K, _ptr(w8p), _ptr(sfb), H, hc, _ptr(h), _ptr(q_w),
+                                     _ptr(k_w), _ptr(mask), eps, clamp, score_scale, _ptr(gate_out), _ptr(workspace),
+                                     workspace.numel(), _ptr(status), _stream(dev)), "engram_project_gate_fp8")
+    return gate_out
 
 
 def engram_dequant_rows(rows: torch.Tensor, n_cols: int, e: Optional[torch.Tensor] = None,

@@ -233,12 +233,60 @@ struct HashedRows {
   }
 };
 
+// What a warp writes for a position once its rows sit in shared memory
+// (row j at sb + j * 272 + 8 if odd): dequantised bf16 rows ...
+struct Bf16Out {
+  uint16_t* e;  // [T][n_cols * 256]
+  __device__ __forceinline__ void operator()(const uint8_t* sb, uint32_t odd, uint32_t vm, int64_t t, int n_cols,
+                                             uint32_t lane) const {
+    uint16_t* out = e + t * static_cast<int64_t>(n_cols) * ENGRAM_HEAD_DIM;
+#pragma unroll 4
+    for (int j = 0; j < n_cols; ++j) {
+      const uint8_t* row = sb + j * kSlot + (((odd >> j) & 1u) ? 8 : 0);
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if ((vm >> j) & 1u) {
+        const uint2 wv = *reinterpret_cast<const uint2*>(row + lane * 8);
+        const uint32_t sbyte = row[256 + (lane >> 2)];
+        o = dequant8(wv, sbyte);
+      }
+      *reinterpret_cast<uint4*>(out + j * ENGRAM_HEAD_DIM + lane * 8) = o;
+    }
+  }
+};
+
+// ... or the rows as they are, for the block-scaled FP8 projection: the E4M3
+// bytes concatenated, e8[t][256 j + c], and the E8M0 scales grouped by
+// 128-element k-block, sf[(2 j + b / 4) * T + t] byte b % 4 (so the four
+// scales of one k-block of consecutive positions are contiguous).  A bad row
+// becomes zero bytes with scale 127 (the value 0).
+struct Fp8Out {
+  uint8_t* e8;    // [T][n_cols * 256]
+  uint32_t* sf;   // [n_cols * 2][T] words of four E8M0 bytes
+  int64_t n_tokens;
+  __device__ __forceinline__ void operator()(const uint8_t* sb, uint32_t odd, uint32_t vm, int64_t t, int n_cols,
+                                             uint32_t lane) const {
+    uint8_t* out = e8 + t * static_cast<int64_t>(n_cols) * ENGRAM_HEAD_DIM;
+#pragma unroll 4
+    for (int j = 0; j < n_cols; ++j) {
+      const uint8_t* row = sb + j * kSlot + (((odd >> j) & 1u) ? 8 : 0);
+      const uint2 wv = ((vm >> j) & 1u) ? *reinterpret_cast<const uint2*>(row + lane * 8) : make_uint2(0u, 0u);
+      *reinterpret_cast<uint2*>(out + j * ENGRAM_HEAD_DIM + lane * 8) = wv;
+    }
+    if (lane < static_cast<uint32_t>(n_cols)) {
+      const uint8_t* row = sb + lane * kSlot + (((odd >> lane) & 1u) ? 8 : 0);
+      const uint2 sc = ((vm >> lane) & 1u) ? *reinterpret_cast<const uint2*>(row + 256) : make_uint2(0x7f7f7f7fu, 0x7f7f7f7fu);
+      sf[(2 * static_cast<int64_t>(lane)) * n_tokens + t] = sc.x;
+      sf[(2 * static_cast<int64_t>(lane) + 1) * n_tokens + t] = sc.y;
+    }
+  }
+};
+
 // Same pipeline as gather_dequant_kernel, but each row window moves as 17
 // 16-byte cp.async copies spread over the warp's lanes (a flat list of
 // n_cols * 17 pieces per position) instead of one bulk copy per row: many
 // small requests go through the LSU rather than the TMA unit.
-template <class RowSource>
-__global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArgs a, RowSource src) {
+template <class RowSource, class Out>
+__global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArgs a, RowSource src, Out store) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int w = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
@@ -308,21 +356,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArg
       timed_out = true;
       break;
     }
-    const uint32_t odd = masks[2 * s];
-    const uint32_t vm = masks[2 * s + 1];
-    const uint8_t* sb = wbuf + static_cast<size_t>(s) * stage_bytes;
-    uint16_t* out = a.e + t * static_cast<int64_t>(n_cols) * ENGRAM_HEAD_DIM;
-#pragma unroll 4
-    for (int j = 0; j < n_cols; ++j) {
-      const uint8_t* row = sb + j * kSlot + (((odd >> j) & 1u) ? 8 : 0);
-      uint4 o = make_uint4(0u, 0u, 0u, 0u);
-      if ((vm >> j) & 1u) {
-        const uint2 wv = *reinterpret_cast<const uint2*>(row + lane * 8);
-        const uint32_t sbyte = row[256 + (lane >> 2)];
-        o = dequant8(wv, sbyte);
-      }
-      *reinterpret_cast<uint4*>(out + j * ENGRAM_HEAD_DIM + lane * 8) = o;
-    }
+    store(wbuf + static_cast<size_t>(s) * stage_bytes, masks[2 * s], masks[2 * s + 1], t, n_cols, lane);
     __syncwarp();
     const int64_t t2 = t + static_cast<int64_t>(S) * nw;
     if (t2 < a.n_tokens) issue(t2, s);
@@ -397,14 +431,14 @@ int gather_config(int n_cols, int* stages, size_t* smem) {
   return ENGRAM_OK;
 }
 
-template <class RowSource>
-int launch_ldgsts(const GatherArgs& a, const RowSource& src, size_t smem, int sms, cudaStream_t st) {
-  cudaError_t err = cudaFuncSetAttribute(gather_ldgsts_kernel<RowSource>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024);
+template <class RowSource, class Out>
+int launch_ldgsts(const GatherArgs& a, const RowSource& src, const Out& out, size_t smem, int sms, cudaStream_t st) {
+  cudaError_t err = cudaFuncSetAttribute(gather_ldgsts_kernel<RowSource, Out>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(gather): %s", cudaGetErrorString(err));
   const int64_t want = (a.n_tokens + kWarps - 1) / kWarps;
   const int blocks = static_cast<int>(want < sms ? want : sms);
-  gather_ldgsts_kernel<RowSource><<<blocks, kWarps * 32, smem, st>>>(a, src);
+  gather_ldgsts_kernel<RowSource, Out><<<blocks, kWarps * 32, smem, st>>>(a, src, out);
   return check_launch("gather_ldgsts_kernel");
 }
 
@@ -430,7 +464,7 @@ extern "C" int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows,
   size_t smem = 0;
   if ((rc = gather_config(n_cols, &stages, &smem))) return rc;
   GatherArgs a{table_d, total_rows, table_bytes, row_ids_d, n_tokens, n_cols, stages, e_d, status_d};
-  if (use_ldgsts()) return launch_ldgsts(a, IdRows{row_ids_d}, smem, sms, as_stream(stream));
+  if (use_ldgsts()) return launch_ldgsts(a, IdRows{row_ids_d}, Bf16Out{e_d}, smem, sms, as_stream(stream));
   cudaError_t err = cudaFuncSetAttribute(gather_dequant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
   if (err != cudaSuccess)
@@ -467,9 +501,63 @@ extern "C" int engram_hash_gather(const engram_layout* layout, int32_t layer, co
     if ((rc = gather_config(c.n_cols, &stages, &smem))) return rc;
     GatherArgs a{table_d, total_rows, table_bytes, nullptr, n_tokens, c.n_cols, stages, e_d, status_d};
     HashedRows src{c, raw_ids_d, cu_seqlens_d, n_seqs, token_map_d, hist_d, row_ids_d, mask_d, status_d};
-    if ((rc = launch_ldgsts(a, src, smem, sms, st))) return rc;
+    if ((rc = launch_ldgsts(a, src, Bf16Out{e_d}, smem, sms, st))) return rc;
   }
   // the history advances after every position has read the old one
+  if (hist_d != nullptr)
+    return hashdev::launch_hist_commit(c, raw_ids_d, cu_seqlens_d, n_seqs, token_map_d, hist_d, status_d, st);
+  return ENGRAM_OK;
+}
+
+extern "C" int engram_gather_fp8(const uint8_t* table_d, int64_t total_rows, int64_t table_bytes,
+                                 const int32_t* row_ids_d, int64_t n_tokens, int32_t n_cols, uint8_t* e8_d,
+                                 uint32_t* sf_d, int32_t* status_d, void* stream) {
+  if (n_tokens < 0 || total_rows < 0) return fail(ENGRAM_E_INVALID, "negative size");
+  if (n_cols < 1 || n_cols > ENGRAM_MAX_COLS) return fail(ENGRAM_E_SHAPE, "n_cols %d", n_cols);
+  if (table_bytes < total_rows * kRowBytes)
+    return fail(ENGRAM_E_SHAPE, "table_bytes %lld < total_rows * 264", (long long)table_bytes);
+  if (n_tokens == 0) return ENGRAM_OK;
+  if (!table_d || !e8_d || !sf_d || !row_ids_d) return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (!aligned(table_d, 16) || !aligned(e8_d, 16) || !aligned(sf_d, 4))
+    return fail(ENGRAM_E_ALIGN, "table and e8 must be 16-byte and sf 4-byte aligned");
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  int stages = 0;
+  size_t smem = 0;
+  if ((rc = gather_config(n_cols, &stages, &smem))) return rc;
+  GatherArgs a{table_d, total_rows, table_bytes, row_ids_d, n_tokens, n_cols, stages, nullptr, status_d};
+  return launch_ldgsts(a, IdRows{row_ids_d}, Fp8Out{e8_d, sf_d, n_tokens}, smem, sms, as_stream(stream));
+}
+
+extern "C" int engram_hash_gather_fp8(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
+                                      int64_t n_tokens, const int64_t* cu_seqlens_d, int32_t n_seqs,
+                                      const int32_t* token_map_d, int64_t vocab_raw, int32_t* hist_d,
+                                      const uint8_t* table_d, int64_t table_bytes, uint8_t* e8_d, uint32_t* sf_d,
+                                      uint8_t* mask_d, int32_t* row_ids_d, int32_t* status_d, void* stream) {
+  hashdev::HashConsts c;
+  int rc = hashdev::make_consts(layout, layer, vocab_raw, &c);
+  if (rc) return rc;
+  const int64_t total_rows = layout->total_rows[layer];
+  if (n_tokens < 0 || n_seqs < 1) return fail(ENGRAM_E_INVALID, "n_tokens < 0 or n_seqs < 1");
+  if (table_bytes < total_rows * kRowBytes)
+    return fail(ENGRAM_E_SHAPE, "table_bytes %lld < total_rows * 264", (long long)table_bytes);
+  if (n_tokens == 0 && hist_d == nullptr) return ENGRAM_OK;
+  if (!cu_seqlens_d || !token_map_d || (n_tokens > 0 && (!raw_ids_d || !table_d || !e8_d || !sf_d || !mask_d)))
+    return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (n_tokens > 0 && (!aligned(table_d, 16) || !aligned(e8_d, 16) || !aligned(sf_d, 4)))
+    return fail(ENGRAM_E_ALIGN, "table and e8 must be 16-byte and sf 4-byte aligned");
+  int sms = 0;
+  if ((rc = check_device(&sms))) return rc;
+  cudaStream_t st = as_stream(stream);
+  if (n_tokens > 0) {
+    int stages = 0;
+    size_t smem = 0;
+    if ((rc = gather_config(c.n_cols, &stages, &smem))) return rc;
+    GatherArgs a{table_d, total_rows, table_bytes, nullptr, n_tokens, c.n_cols, stages, nullptr, status_d};
+    HashedRows src{c, raw_ids_d, cu_seqlens_d, n_seqs, token_map_d, hist_d, row_ids_d, mask_d, status_d};
+    if ((rc = launch_ldgsts(a, src, Fp8Out{e8_d, sf_d, n_tokens}, smem, sms, st))) return rc;
+  }
   if (hist_d != nullptr)
     return hashdev::launch_hist_commit(c, raw_ids_d, cu_seqlens_d, n_seqs, token_map_d, hist_d, status_d, st);
   return ENGRAM_OK;

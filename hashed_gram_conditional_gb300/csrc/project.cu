@@ -812,6 +812,275 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Block-scaled FP8 projection ([P-O1] §2.3: the released model's projection
+// weights are block-FP8 and the table payload is E4M3 with E8M0 scales per
+// 32 elements).  The gathered rows enter the tensor cores as they are stored
+// (tcgen05.mma kind::mxf8f6f4, E4M3 x E4M3 with an E8M0 scale per 32 elements
+// of k on both operands, fp32 accumulation), so there is no bf16 e at all.
+//
+// One CTA per 128 x 256 tile (two N = 128 MMAs per k-step), k-blocks of 128
+// bytes (four K = 32 steps), 4 stages of 48 KB.  The scale factors do not go
+// through TMA: four "scale" warps (one per TMEM lane quarter) read each
+// k-block's scales from global memory and write them to a per-stage TMEM slot
+// with tcgen05.st in the layout the MMA reads -- lane L, column c, byte k
+// holds the scale of row (L mod 32) + 32 c for k-step k, replicated in every
+// lane quarter (established on GB300 by a standalone probe).  The slot of a
+// stage is rewritten only after the MMAs that read it have completed (the
+// stage's "empty" barrier).  TMEM: the 256-column accumulator plus 4 x 12
+// scale columns, so the accumulator is single-buffered and the epilogue does
+// not overlap the next tile's main loop.  Epilogues are the bf16 kernels'.
+constexpr int BK8 = 128;  // bytes = elements per k-block
+constexpr int STAGES8 = 4;
+constexpr int A8_BYTES = BM * BK8;
+constexpr int B8_BYTES = BN * BK8;
+constexpr int STAGE8_BYTES = A8_BYTES + B8_BYTES;
+constexpr int kThreads8 = 320;  // producer, MMA, 4 epilogue, 4 scale warps
+constexpr int kSfCols = 12;     // per stage: A (4), B rows 0..127 (4), B rows 128..255 (4)
+constexpr int kSfBase = BN;     // scale slots after the accumulator
+constexpr int TMEM8_COLS = 512;
+
+struct __align__(8) Ctl8 {
+  uint64_t sf_full[STAGES8];
+};
+
+// kind::mxf8f6f4 instruction descriptor: A and B E4M3, K-major, N = 128,
+// M = 128, E8M0 scales, both scale-factor ids = the k-step (byte of the
+// scale column); the accumulator is fp32.
+__device__ __forceinline__ uint32_t idesc8(uint32_t sf_id) {
+  return (sf_id << 4) | ((128u >> 3) << 17) | (1u << 23) | ((static_cast<uint32_t>(BM) >> 4) << 24) | (sf_id << 29);
+}
+
+__device__ __forceinline__ void tc_mma8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.block32 [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
+// sfa: [K/128][M] words (four E8M0 bytes: the k-block's four 32-element
+// scales of a row); sfb: [K/128][N] words likewise for the rows of wkv^T.
+template <bool kFuse>
+__global__ void __launch_bounds__(kThreads8, 1)
+    project8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ProjArgs a,
+                    const uint32_t* __restrict__ sfa, const uint32_t* __restrict__ sfb) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + STAGES8 * A8_BYTES;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + STAGES8 * STAGE8_BYTES);
+  Ctl8* ctl8 = reinterpret_cast<Ctl8*>(ctl + 1);
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const int nkb = a.K / BK8;
+  const int64_t N = static_cast<int64_t>(a.hc + 1) * a.H;
+  volatile int* abort_flag = &ctl->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES8; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl8->sf_full[s]), 4);
+    }
+    mbar_init(smem_u32(&ctl->tfull[0]), 1);
+    mbar_init(smem_u32(&ctl->tempty[0]), 4);
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(TMEM8_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (operands)
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, a.mt, a.nt, kGroupM, mb, nb);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES8;
+          const uint32_t ph = (it / STAGES8) & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag)) {
+            if (!*abort_flag) raise_abort(ctl, a);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(fb, STAGE8_BYTES);
+          tma_load_2d(smem_u32(smA + s * A8_BYTES), &tmA, kb * BK8, mb * BM, fb);
+          tma_load_4d(smem_u32(smB + s * B8_BYTES), &tmB, kb, nb * (BN / 128), fb);
+        }
+      }
+      for (int j = (it > STAGES8 ? it - STAGES8 : 0); j < it; ++j)
+        mbar_wait_bounded(smem_u32(&ctl->full[j % STAGES8]), (j / STAGES8) & 1, nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x, ++local) {
+        if (!mbar_wait_bounded(smem_u32(&ctl->tempty[0]), (local & 1) ^ 1, abort_flag)) {
+          if (!*abort_flag) raise_abort(ctl, a);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES8;
+          const uint32_t ph = (it / STAGES8) & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag) ||
+              !mbar_wait_bounded(smem_u32(&ctl8->sf_full[s]), ph, abort_flag)) {
+            if (!*abort_flag) raise_abort(ctl, a);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smA + s * A8_BYTES);
+          const uint32_t b0 = smem_u32(smB + s * B8_BYTES);
+          const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + s * kSfCols);
+#pragma unroll
+          for (int k = 0; k < BK8 / 32; ++k) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              tc_mma8(tmem_base + static_cast<uint32_t>(hh * 128), sw128_desc(a0 + k * 32),
+                      sw128_desc(b0 + hh * (128 * BK8) + k * 32), idesc8(static_cast<uint32_t>(k)), sf,
+                      sf + 4u + 4u * static_cast<uint32_t>(hh), (kb | k) != 0 ? 1u : 0u);
+            }
+          }
+          tc_commit(smem_u32(&ctl->empty[s]));
+        }
+        if (ok) tc_commit(smem_u32(&ctl->tfull[0]));
+      }
+      tc_commit(smem_u32(&ctl->drain));
+      mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr);
+    }
+  } else if (warp < 6) {
+    // ---------------- epilogue (warps 2..5)
+    const int q = warp & 3;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++local) {
+      int mb, nb;
+      tile_coords(tile, a.mt, a.nt, kGroupM, mb, nb);
+      const EpiTile et = epi_tile(a, nb);
+      epilogue_stage(a, ctl, q, lane, et);
+      if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), local & 1, abort_flag)) {
+        if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      if (!epilogue_tile<kFuse>(a, ctl, q, lane, taddr, mb, et, abort_flag)) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[0]));
+    }
+  } else {
+    // ---------------- scale warps (6..9): one per TMEM lane quarter
+    const uint32_t q = static_cast<uint32_t>(warp & 3);
+    const uint32_t lane_off = (q * 32u) << 16;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, a.mt, a.nt, kGroupM, mb, nb);
+      const int64_t m0 = static_cast<int64_t>(mb) * BM;
+      const int64_t n0 = static_cast<int64_t>(nb) * BN;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % STAGES8;
+        const uint32_t ph = (it / STAGES8) & 1;
+        // this k-block's scales, replicated layout: column c holds row lane + 32 c
+        uint32_t ra[4], rb0[4], rb1[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int64_t row = m0 + lane + 32 * c;
+          ra[c] = row < a.M ? __ldg(sfa + static_cast<int64_t>(kb) * a.M + row) : 0x7f7f7f7fu;
+          rb0[c] = __ldg(sfb + static_cast<int64_t>(kb) * N + n0 + lane + 32 * c);
+          rb1[c] = __ldg(sfb + static_cast<int64_t>(kb) * N + n0 + 128 + lane + 32 * c);
+        }
+        bool free_slot = true;
+        if (lane == 0) free_slot = mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag);
+        free_slot = __shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0) != 0;
+        if (!free_slot) {
+          if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sf = tmem_base + lane_off + static_cast<uint32_t>(kSfBase + s * kSfCols);
+        tc_st4(sf, ra);
+        tc_st4(sf + 4u, rb0);
+        tc_st4(sf + 8u, rb1);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl8->sf_full[s]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM8_COLS)
+                 : "memory");
+  }
+}
+
+// Block-FP8 wkv into the operand layouts of project8_kernel: codes [K][N]
+// (kv = e @ wkv) -> [N/128][K/128][128][128] bytes, so each 128 x 128-byte
+// tile of wkv^T is 16 KB contiguous; scales [K/32][N] -> [K/128][N] words,
+// byte j of word (kb, n) = scale of rows kb*128 + 32 j .. +31 of column n.
+__global__ void pack_wkv8_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ sf, int64_t K,
+                                 int64_t N, uint8_t* __restrict__ wt, uint32_t* __restrict__ sft) {
+  __shared__ uint8_t tile[32][33];
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 32, k0 = static_cast<int64_t>(blockIdx.y) * 32;
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int64_t k = k0 + r, n = n0 + threadIdx.x;
+    tile[r][threadIdx.x] = (k < K && n < N) ? w[k * N + n] : 0;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int64_t n = n0 + r, k = k0 + threadIdx.x;
+    if (n < N && k < K)
+      wt[(((n / 128) * (K / 128) + k / 128) * 128 + n % 128) * 128 + k % 128] = tile[threadIdx.x][r];
+  }
+  // scale words: the blocks with threadIdx.y == 0 of the first k-row of every 128 k
+  if (blockIdx.y % 4 == 0 && threadIdx.y == 0) {
+    const int64_t n = n0 + threadIdx.x, kb = k0 / 128;
+    if (n < N && kb < K / 128) {
+      uint32_t word = 0;
+      for (int j = 0; j < 4; ++j) word |= static_cast<uint32_t>(sf[(kb * 4 + j) * N + n]) << (8 * j);
+      sft[kb * N + n] = word;
+    }
+  }
+}
+
 // wkv [K][N] -> tiled K-major operand layout [N/128][K/64][128][64]: the
 // 128 x 64 tile (rows n, columns k) of every k-block is 16 KB contiguous and a
 // 128-row block of wkv^T is one contiguous 1.5 MB run, so operand loads stream
@@ -886,6 +1155,39 @@ int make_tmap_wkv(CUtensorMap* tm, const void* base, uint64_t N, uint64_t K, uin
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ENGRAM_E_CUDA, "cuTensorMapEncodeTiled(wkv) failed (%d)", static_cast<int>(r));
+  return ENGRAM_OK;
+}
+
+// 2-D byte tensor [rows][cols] (E4M3 e), box = box_rows x 128 bytes, 128-byte swizzle.
+int make_tmap8(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc;
+  int rc = get_encode_fn(&enc);
+  if (rc) return rc;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK8), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ENGRAM_E_CUDA, "cuTensorMapEncodeTiled(e8) failed (%d)", static_cast<int>(r));
+  return ENGRAM_OK;
+}
+
+// Packed FP8 wkv as a 4-D byte tensor {128, 128, K/128, N/128}; a box covers
+// one k-block of `nblocks` consecutive 128-row blocks.
+int make_tmap_wkv8(CUtensorMap* tm, const void* base, uint64_t N, uint64_t K, uint32_t nblocks) {
+  EncodeTiledFn enc;
+  int rc = get_encode_fn(&enc);
+  if (rc) return rc;
+  const cuuint64_t dims[4] = {128, 128, K / 128, N / 128};
+  const cuuint64_t strides[3] = {128, 128 * 128, (K / 128) * 128 * 128};
+  const cuuint32_t box[4] = {128, 128, 1, nblocks};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ENGRAM_E_CUDA, "cuTensorMapEncodeTiled(wkv8) failed (%d)", static_cast<int>(r));
   return ENGRAM_OK;
 }
 
@@ -1006,6 +1308,84 @@ int launch(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB
   return check_launch("project kernel");
 }
 
+// Argument checks and set-up of the FP8 entry points (single-CTA tiles).
+int prepare8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K, const uint8_t* w8_d,
+             const uint32_t* sfb_d, int32_t hidden, int32_t hc, const uint16_t* h_d, const float* q_w_d,
+             const float* k_w_d, float* partials_d, int32_t* status_d, ProjArgs* a, CUtensorMap* tmA,
+             CUtensorMap* tmB) {
+  if (n_tokens < 0) return fail(ENGRAM_E_INVALID, "n_tokens < 0");
+  if (K < BK8 || K % BK8 != 0 || K > (int64_t(1) << 20))
+    return fail(ENGRAM_E_SHAPE, "K %lld must be a positive multiple of 128", (long long)K);
+  if (hidden < BN || hidden % BN != 0) return fail(ENGRAM_E_SHAPE, "hidden %d must be a multiple of 256", hidden);
+  if (hc < 1 || hc > kMaxHc) return fail(ENGRAM_E_SHAPE, "hc %d not in [1, %d]", hc, kMaxHc);
+  if (n_tokens == 0) return ENGRAM_OK;
+  if (n_tokens > (int64_t(1) << 31) - 2 * BM) return fail(ENGRAM_E_SHAPE, "too many tokens");
+  if (!e8_d || !sfa_d || !w8_d || !sfb_d || !h_d || !q_w_d || !k_w_d || !partials_d)
+    return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (!aligned(e8_d, 16) || !aligned(w8_d, 16) || !aligned(h_d, 16) || !aligned(partials_d, 16) ||
+      !aligned(sfa_d, 4) || !aligned(sfb_d, 4))
+    return fail(ENGRAM_E_ALIGN, "e8, wkv8, h and partials must be 16-byte aligned, the scales 4-byte");
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  const int64_t N = static_cast<int64_t>(hc + 1) * hidden;
+  if ((rc = make_tmap8(tmA, e8_d, static_cast<uint64_t>(n_tokens), static_cast<uint64_t>(K), BM))) return rc;
+  if ((rc = make_tmap_wkv8(tmB, w8_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 2))) return rc;
+  *a = ProjArgs{};
+  a->M = n_tokens;
+  a->K = static_cast<int32_t>(K);
+  a->H = hidden;
+  a->hc = hc;
+  a->mt = static_cast<int32_t>((n_tokens + BM - 1) / BM);
+  a->mt2 = static_cast<int32_t>((n_tokens + 2 * BM - 1) / (2 * BM));
+  a->nt = static_cast<int32_t>(N / BN);
+  const int64_t tiles = static_cast<int64_t>(a->mt) * a->nt;
+  if (tiles > INT32_MAX) return fail(ENGRAM_E_SHAPE, "too many tiles");
+  a->num_tiles = static_cast<int32_t>(tiles);
+  a->h = const_cast<uint16_t*>(h_d);
+  a->q_w = q_w_d;
+  a->k_w = k_w_d;
+  a->partials = reinterpret_cast<float4*>(partials_d);
+  a->status = status_d;
+  return ENGRAM_OK;
+}
+
+size_t project8_smem_bytes() { return 1024 + STAGES8 * STAGE8_BYTES + sizeof(SmemCtl) + sizeof(Ctl8); }
+
+int launch8(bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB, const ProjArgs& a, const uint32_t* sfa,
+            const uint32_t* sfb, cudaStream_t st) {
+  const void* fn = fused ? reinterpret_cast<const void*>(&project8_kernel<true>)
+                         : reinterpret_cast<const void*>(&project8_kernel<false>);
+  const size_t smem = project8_smem_bytes();
+  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(project8): %s", cudaGetErrorString(err));
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads8);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  int nattr = 0;
+  if (fused && use_cooperative()) {
+    attr[nattr].id = cudaLaunchAttributeCooperative;
+    attr[nattr].val.cooperative = 1;
+    ++nattr;
+  }
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads8, smem);
+  if (err != cudaSuccess || per_sm < 1)
+    return fail(ENGRAM_E_CUDA, "no resident CTA for the FP8 projection: %s", cudaGetErrorString(err));
+  const int units = sms * per_sm;
+  cfg.gridDim = dim3(a.num_tiles < units ? a.num_tiles : units);
+  cfg.attrs = attr;
+  cfg.numAttrs = nattr;
+  err = fused ? cudaLaunchKernelEx(&cfg, project8_kernel<true>, tmA, tmB, a, sfa, sfb)
+              : cudaLaunchKernelEx(&cfg, project8_kernel<false>, tmA, tmB, a, sfa, sfb);
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "project8 kernel launch: %s", cudaGetErrorString(err));
+  return check_launch("project8 kernel");
+}
+
 }  // namespace
 }  // namespace engram
 
@@ -1124,4 +1504,76 @@ extern "C" int engram_project_gate(const uint16_t* e_d, int64_t n_tokens, int64_
   cudaError_t err = cudaMemsetAsync(a.cnt, 0, ws.counter_words * sizeof(int32_t), st);
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaMemsetAsync(counters): %s", cudaGetErrorString(err));
   return launch(pair, true, tmA, tmB, a, st);
+}
+
+extern "C" int engram_pack_wkv_fp8(const uint8_t* w8_d, const uint8_t* sf_d, int64_t K, int64_t N,
+                                   uint8_t* w8_packed_d, uint32_t* sf_packed_d, void* stream) {
+  if (K < 1 || N < 1) return fail(ENGRAM_E_INVALID, "K and N must be positive");
+  if (K % 128 != 0 || N % 128 != 0) return fail(ENGRAM_E_SHAPE, "K and N must be multiples of 128");
+  if (!w8_d || !sf_d || !w8_packed_d || !sf_packed_d) return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (!aligned(sf_packed_d, 4)) return fail(ENGRAM_E_ALIGN, "packed scales must be 4-byte aligned");
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  const int64_t gx = (N + 31) / 32, gy = (K + 31) / 32;
+  if (gy > 65535) return fail(ENGRAM_E_SHAPE, "K too large");
+  pack_wkv8_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), dim3(32, 8), 0,
+                     as_stream(stream)>>>(w8_d, sf_d, K, N, w8_packed_d, sf_packed_d);
+  return check_launch("pack_wkv8_kernel");
+}
+
+extern "C" int engram_project_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K,
+                                  const uint8_t* w8_packed_d, const uint32_t* sfb_d, int32_t hidden, int32_t hc,
+                                  const uint16_t* h_d, const float* q_w_d, const float* k_w_d, float* partials_d,
+                                  uint16_t* v_d, int32_t* status_d, void* stream) {
+  if (!v_d && n_tokens > 0) return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (v_d && !aligned(v_d, 16)) return fail(ENGRAM_E_ALIGN, "v must be 16-byte aligned");
+  ProjArgs a;
+  CUtensorMap tmA, tmB;
+  int rc = prepare8(e8_d, sfa_d, n_tokens, K, w8_packed_d, sfb_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d,
+                    status_d, &a, &tmA, &tmB);
+  if (rc || n_tokens == 0) return rc;
+  a.v = v_d;
+  return launch8(false, tmA, tmB, a, sfa_d, sfb_d, as_stream(stream));
+}
+
+extern "C" int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K,
+                                       const uint8_t* w8_packed_d, const uint32_t* sfb_d, int32_t hidden, int32_t hc,
+                                       uint16_t* h_d, const float* q_w_d, const float* k_w_d, const uint8_t* mask_d,
+                                       float eps, float clamp, float score_scale, float* gate_out_d,
+                                       void* workspace_d, size_t workspace_bytes, int32_t* status_d, void* stream) {
+  if (n_tokens > 0 && workspace_d == nullptr) return fail(ENGRAM_E_INVALID, "null workspace");
+  if (workspace_d && !aligned(workspace_d, 256)) return fail(ENGRAM_E_ALIGN, "workspace must be 256-byte aligned");
+  const size_t need = engram_project_gate_workspace_bytes(n_tokens, hidden, hc);
+  if (n_tokens > 0 && workspace_bytes < need)
+    return fail(ENGRAM_E_SHAPE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  const FusedWs ws = fused_ws(n_tokens, hidden, hc);
+  unsigned char* base = static_cast<unsigned char*>(workspace_d);
+  if (n_tokens > 0 && n_tokens <= kTwoKernelMaxTokens) {
+    float* partials_d = reinterpret_cast<float*>(base);
+    uint16_t* v_d = reinterpret_cast<uint16_t*>(base + ws.v_off);
+    int rc = engram_project_fp8(e8_d, sfa_d, n_tokens, K, w8_packed_d, sfb_d, hidden, hc, h_d, q_w_d, k_w_d,
+                                partials_d, v_d, status_d, stream);
+    if (rc) return rc;
+    return engram_gate_add(partials_d, v_d, h_d, mask_d, n_tokens, hidden, hc, eps, clamp, score_scale, gate_out_d,
+                           stream);
+  }
+  ProjArgs a;
+  CUtensorMap tmA, tmB;
+  int rc = prepare8(e8_d, sfa_d, n_tokens, K, w8_packed_d, sfb_d, hidden, hc, h_d, q_w_d, k_w_d,
+                    static_cast<float*>(workspace_d), status_d, &a, &tmA, &tmB);
+  if (rc || n_tokens == 0) return rc;
+  const int mt_ws = 2 * a.mt2;
+  a.cnt = reinterpret_cast<int32_t*>(base + ws.counters_off);
+  a.ready = a.cnt + static_cast<size_t>(mt_ws) * hc * 4;
+  a.abort_g = a.ready + mt_ws;
+  a.gates = reinterpret_cast<float*>(base + ws.gates_off);
+  a.mask = mask_d;
+  a.gate_out = gate_out_d;
+  a.eps = eps;
+  a.clamp = clamp;
+  a.score_scale = score_scale;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t err = cudaMemsetAsync(a.cnt, 0, ws.counter_words * sizeof(int32_t), st);
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaMemsetAsync(counters): %s", cudaGetErrorString(err));
+  return launch8(true, tmA, tmB, a, sfa_d, sfb_d, st);
 }

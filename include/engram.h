@@ -241,6 +241,27 @@ int engram_hash_gather(const engram_layout* layout, int32_t layer, const int32_t
                        int32_t* hist_d, const uint8_t* table_d, int64_t table_bytes, uint16_t* e_d,
                        uint8_t* mask_d, int32_t* row_ids_d, int32_t* status_d, void* stream);
 
+/* The gather for the block-scaled FP8 projection: the rows are copied as
+ * stored instead of dequantised ([P-O1] §2.3: E4M3 payload with E8M0 scales
+ * per 32 elements).  For position t and column j:
+ *   e8_d[t][256 j + c]          = weight byte c of row row_ids_d[t][j]
+ *   sf_d[(2 j + b / 4) * n_tokens + t], byte b % 4 = scale byte b of that row
+ * i.e. the scales are grouped per 128-element k-block, one 32-bit word of four
+ * E8M0 scales per (k-block, position).  A row id outside [0, total_rows) sets
+ * ENGRAM_ST_BAD_ROW and gives zero bytes with scales 127 (the value 0).
+ *   e8_d  uint8 [n_tokens][n_cols*256], 16-byte aligned
+ *   sf_d  uint32 [n_cols*2][n_tokens], 4-byte aligned */
+int engram_gather_fp8(const uint8_t* table_d, int64_t total_rows, int64_t table_bytes, const int32_t* row_ids_d,
+                      int64_t n_tokens, int32_t n_cols, uint8_t* e8_d, uint32_t* sf_d, int32_t* status_d,
+                      void* stream);
+
+/* engram_hash_gather with the FP8 outputs of engram_gather_fp8. */
+int engram_hash_gather_fp8(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d, int64_t n_tokens,
+                           const int64_t* cu_seqlens_d, int32_t n_seqs, const int32_t* token_map_d,
+                           int64_t vocab_raw, int32_t* hist_d, const uint8_t* table_d, int64_t table_bytes,
+                           uint8_t* e8_d, uint32_t* sf_d, uint8_t* mask_d, int32_t* row_ids_d, int32_t* status_d,
+                           void* stream);
+
 /* Dequantise rows that already sit contiguously in device memory (e.g. after
  * a host-side gather and one DMA): e_d[i/n_cols][256*(i%n_cols) + c] from
  * row i of rows_d, for i < n_rows (a multiple of n_cols).  Same arithmetic as
@@ -317,6 +338,40 @@ int engram_project(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint1
                    int32_t hidden, int32_t hc, const uint16_t* h_d, const float* q_w_d,
                    const float* k_w_d, float* partials_d, uint16_t* v_d, int32_t* status_d,
                    void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Block-scaled FP8 projection (stage 5a on block-FP8 weights)               */
+/* ------------------------------------------------------------------------ */
+
+/* [P-O1] §2.3: the released model's projection weights are block-FP8.  Here
+ * wkv is E4M3 codes w8_d uint8 [K][N] (kv = e @ wkv) with one E8M0 scale per
+ * 32 consecutive rows of k in each column, sf_d uint8 [K/32][N]; value
+ * E4M3(w) * 2^(s - 127).  engram_pack_wkv_fp8 repacks them once into the
+ * operand layouts of the FP8 projection: w8_packed_d uint8, K*N bytes, tiles
+ * [N/128][K/128][128][128] (element (k, n) at ((n/128 * K/128 + k/128) * 128
+ * + n%128) * 128 + k%128); sf_packed_d uint32 [K/128][N], byte j of word
+ * (kb, n) = the scale of rows kb*128 + 32 j .. +31.  K and N multiples of 128. */
+int engram_pack_wkv_fp8(const uint8_t* w8_d, const uint8_t* sf_d, int64_t K, int64_t N, uint8_t* w8_packed_d,
+                        uint32_t* sf_packed_d, void* stream);
+
+/* engram_project on FP8 operands: e in the engram_gather_fp8 form (e8_d uint8
+ * [n_tokens][K], sfa_d uint32 [K/128][n_tokens]) and the packed FP8 wkv.  The
+ * tensor cores take the E4M3 values with their E8M0 scales (tcgen05.mma
+ * kind::mxf8f6f4, block size 32) and accumulate in fp32; the outputs
+ * (partials_d, v_d) are those of engram_project.  K % 128 == 0; other
+ * requirements as for engram_project.  A bounded on-chip wait that runs out
+ * sets ENGRAM_ST_TIMEOUT. */
+int engram_project_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K,
+                       const uint8_t* w8_packed_d, const uint32_t* sfb_d, int32_t hidden, int32_t hc,
+                       const uint16_t* h_d, const float* q_w_d, const float* k_w_d, float* partials_d,
+                       uint16_t* v_d, int32_t* status_d, void* stream);
+
+/* engram_project_gate on FP8 operands (same workspace, engram_project_gate_workspace_bytes). */
+int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K,
+                            const uint8_t* w8_packed_d, const uint32_t* sfb_d, int32_t hidden, int32_t hc,
+                            uint16_t* h_d, const float* q_w_d, const float* k_w_d, const uint8_t* mask_d, float eps,
+                            float clamp, float score_scale, float* gate_out_d, void* workspace_d,
+                            size_t workspace_bytes, int32_t* status_d, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Gate + residual add (stage 5b/5c)                                          */
