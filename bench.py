@@ -76,6 +76,7 @@ def parse():
     p.add_argument("--micro-steps", type=int, default=30, help="steps of the hash+gather microbench phase")
     p.add_argument("--decode-steps", type=int, default=200, help="steps of the decode phase")
     p.add_argument("--conv-steps", type=int, default=30, help="steps of the short-convolution layer phase")
+    p.add_argument("--fp8-steps", type=int, default=200, help="steps of the block-FP8 projection layer phase")
     p.add_argument("--fullscale-passes", type=int, default=2,
                    help="timed passes over the 131,072-token full-scale sequence (101 GB table; 0 skips it)")
     p.add_argument("--host-steps", type=int, default=20,
@@ -320,6 +321,7 @@ def run_ours(args, rank, world, local):
     micro = microbench(args, w, inp, layer, flush, dev) if args.micro_steps > 0 else None
     dec = decode_bench(args, w, inp, layer, flush, dev) if args.decode_steps > 0 else None
     conv = conv_bench(args, w, inp, layer, flush, dev) if args.conv_steps > 0 else None
+    fp8 = fp8_bench(args, w, inp, layer, flush, dev) if args.fp8_steps > 0 else None
     host = host_table_bench(args, w, inp, layer, flush, dev, statistics.mean(step_ms)) \
         if args.host_steps > 0 else None
     full = fullscale_bench(args, inp, layer, dev) if args.fullscale_passes > 0 else None
@@ -341,6 +343,15 @@ def run_ours(args, rank, world, local):
         full["hash_gather_frac_hbm"] = full["hash_gather_gbs"] / peaks["hbm_gbs"]
     if dec is not None:
         dec["wkv_frac_hbm"] = dec["wkv_gbs"] / peaks["hbm_gbs"]
+    if fp8 is not None:
+        # fp8 dense tensor peak: the measured bf16 figure times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+        fp8_sust = fp8["timed_s"] >= 2.0
+        pk = 2.0 * (peaks["bf16_tflops_sustained"] if fp8_sust else peaks["bf16_tflops"])
+        fp8["roofline"] = {"bound": "tensor", "kernel": "project8_kernel<fused> (tcgen05 kind::mxf8f6f4)",
+                           "achieved": fp8["project_tflops"], "peak": pk, "unit": "TFLOP/s",
+                           "frac": fp8["project_tflops"] / pk,
+                           "peak_source": f"{peak_src} bf16_tflops{'_sustained' if fp8_sust else ''} x 2 "
+                                          "(nominal fp8 / bf16 dense ratio)"}
     if conv is not None:
         conv["conv_frac_hbm"] = conv["conv_gbs"] / peaks["hbm_gbs"]
         conv["traffic_conv_add"] = traffic.get("conv_add_kernel")
@@ -388,6 +399,7 @@ def run_ours(args, rank, world, local):
         "microbench_hash_gather": micro,
         "decode_step": dec,
         "short_conv_layer": conv,
+        "fp8_layer": fp8,
         "fullscale": full,
         "host_table": host,
         "gpu_launches": args.steps * 3,
@@ -683,6 +695,65 @@ def decode_bench(args, w, inp, layer, flush, dev):
             "hash_step_ms": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
             "gather_ms": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs),
             "project_gate_ms": proj * 1e3, "wkv_gbs": wkv_bytes / proj / 1e9}
+
+
+def fp8_bench(args, w, inp, layer, flush, dev):
+    """The layer with block-FP8 weights: the fused hash + gather copying the
+    rows as stored (E4M3 + E8M0) and the block-scaled tensor-core projection
+    with the gate and residual, on the same batch and table."""
+    import torch
+    import hashed_gram_conditional_gb300 as eg
+    from workloads import mxfp8_weights
+
+    K, N = 24 * 256, (w.hc + 1) * w.hidden
+    w8, sf = mxfp8_weights(K, N, w.seed)
+    w8p, sfb = eg.engram_pack_wkv_fp8(torch.from_numpy(w8).to(dev), torch.from_numpy(sf).to(dev))
+    b = inp["batch"]
+    T = len(b.raw_ids)
+    raw = torch.from_numpy(b.raw_ids).to(dev)
+    cu = torch.from_numpy(b.cu_seqlens).to(dev)
+    h = inp["bf16"](inp["h_bits"])
+    hist = torch.full((w.n_seqs, 3), layer.layout.pad_id, dtype=torch.int32, device=dev)
+    e8 = torch.empty((T, K), dtype=torch.uint8, device=dev)
+    sfa = torch.empty((2 * 24, T), dtype=torch.int32, device=dev)
+    mask = torch.empty(T, dtype=torch.uint8, device=dev)
+    work = eg.project_gate_workspace(T, w.hidden, w.hc, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def run(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        eg.engram_hash_gather_fp8(layer.layout, 0, raw, cu, layer.token_map, layer.table, hist, e8, sfa, mask, None,
+                                  status)
+        if ev is not None:
+            ev[1].record(stream)
+        eg.engram_project_gate_fp8(e8, sfa, w8p, sfb, h, layer.q_w, layer.k_w, mask, layer.eps, layer.clamp,
+                                   layer.score_scale, None, work, status)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(5):
+        flush.zero_()
+        run()
+    n = args.fp8_steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(n):
+        flush.zero_()
+        run(evs[k])
+    torch.cuda.synchronize()
+    timed = time.perf_counter() - t0
+    step = statistics.mean(ev[0].elapsed_time(ev[2]) for ev in evs) / 1e3
+    proj = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs) / 1e3
+    hg = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs) / 1e3
+    flops = 2.0 * T * K * N
+    return {"workload": f"{w.name} batch ({T} tokens), block-FP8 wkv (E4M3, E8M0 per 32 of k), L2 flushed",
+            "steps": n, "step_ms": step * 1e3, "tokens_per_s": T / step, "hash_gather_ms": hg * 1e3,
+            "project_gate_ms": proj * 1e3, "project_tflops": flops / proj / 1e12, "timed_s": timed,
+            "hash_gather_bytes_per_token": 4 + 24 * 264 + 24 * 256 + 24 * 8,
+            "device_status": int(status.item())}
 
 
 def conv_bench(args, w, inp, layer, flush, dev):

@@ -819,13 +819,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (tcgen05.mma kind::mxf8f6f4, E4M3 x E4M3 with an E8M0 scale per 32 elements
 // of k on both operands, fp32 accumulation), so there is no bf16 e at all.
 //
-// One CTA per 128 x 256 tile (two N = 128 MMAs per k-step), k-blocks of 128
-// bytes (four K = 32 steps), 4 stages of 48 KB.  The scale factors do not go
+// One CTA per 128 x 256 tile (one M = 128, N = 256 MMA per K = 32 step),
+// k-blocks of 128 bytes (four steps), 4 stages of 48 KB.  The scale factors do not go
 // through TMA: four "scale" warps (one per TMEM lane quarter) read each
 // k-block's scales from global memory and write them to a per-stage TMEM slot
 // with tcgen05.st in the layout the MMA reads -- lane L, column c, byte k
-// holds the scale of row (L mod 32) + 32 c for k-step k, replicated in every
-// lane quarter (established on GB300 by a standalone probe).  The slot of a
+// holds the scale of row (L mod 32) + 32 c for k-step k (c < 4 for the 128
+// rows of A, c < 8 for the 256 rows of B), replicated in every lane quarter
+// (established on GB300 by a standalone probe).  The slot of a
 // stage is rewritten only after the MMAs that read it have completed (the
 // stage's "empty" barrier).  TMEM: the 256-column accumulator plus 4 x 12
 // scale columns, so the accumulator is single-buffered and the epilogue does
@@ -836,7 +837,7 @@ constexpr int A8_BYTES = BM * BK8;
 constexpr int B8_BYTES = BN * BK8;
 constexpr int STAGE8_BYTES = A8_BYTES + B8_BYTES;
 constexpr int kThreads8 = 320;  // producer, MMA, 4 epilogue, 4 scale warps
-constexpr int kSfCols = 12;     // per stage: A (4), B rows 0..127 (4), B rows 128..255 (4)
+constexpr int kSfCols = 12;     // per stage: A (4 columns), B (8 columns)
 constexpr int kSfBase = BN;     // scale slots after the accumulator
 constexpr int TMEM8_COLS = 512;
 
@@ -844,11 +845,12 @@ struct __align__(8) Ctl8 {
   uint64_t sf_full[STAGES8];
 };
 
-// kind::mxf8f6f4 instruction descriptor: A and B E4M3, K-major, N = 128,
+// kind::mxf8f6f4 instruction descriptor: A and B E4M3, K-major, N = 256,
 // M = 128, E8M0 scales, both scale-factor ids = the k-step (byte of the
 // scale column); the accumulator is fp32.
 __device__ __forceinline__ uint32_t idesc8(uint32_t sf_id) {
-  return (sf_id << 4) | ((128u >> 3) << 17) | (1u << 23) | ((static_cast<uint32_t>(BM) >> 4) << 24) | (sf_id << 29);
+  return (sf_id << 4) | ((static_cast<uint32_t>(BN) >> 3) << 17) | (1u << 23) |
+         ((static_cast<uint32_t>(BM) >> 4) << 24) | (sf_id << 29);
 }
 
 __device__ __forceinline__ void tc_mma8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -963,14 +965,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
           const uint32_t b0 = smem_u32(smB + s * B8_BYTES);
           const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + s * kSfCols);
 #pragma unroll
-          for (int k = 0; k < BK8 / 32; ++k) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              tc_mma8(tmem_base + static_cast<uint32_t>(hh * 128), sw128_desc(a0 + k * 32),
-                      sw128_desc(b0 + hh * (128 * BK8) + k * 32), idesc8(static_cast<uint32_t>(k)), sf,
-                      sf + 4u + 4u * static_cast<uint32_t>(hh), (kb | k) != 0 ? 1u : 0u);
-            }
-          }
+          for (int k = 0; k < BK8 / 32; ++k)
+            tc_mma8(tmem_base, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc8(static_cast<uint32_t>(k)), sf,
+                    sf + 4u, (kb | k) != 0 ? 1u : 0u);
           tc_commit(smem_u32(&ctl->empty[s]));
         }
         if (ok) tc_commit(smem_u32(&ctl->tfull[0]));
@@ -999,28 +996,45 @@ __global__ void __launch_bounds__(kThreads8, 1)
       if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[0]));
     }
   } else {
-    // ---------------- scale warps (6..9): one per TMEM lane quarter
+    // ---------------- scale warps (6..9): one per TMEM lane quarter.  The
+    // scales of the next kSfAhead k-blocks are in flight in registers while
+    // the current one is written, so the global-memory latency stays off the
+    // MMA's critical path.
+    constexpr int kSfAhead = 4;
     const uint32_t q = static_cast<uint32_t>(warp & 3);
     const uint32_t lane_off = (q * 32u) << 16;
-    int it = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+    const int my_tiles = blockIdx.x < a.num_tiles ? (a.num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    const int total = my_tiles * nkb;
+    // this k-block's scales, replicated layout: column c holds row lane + 32 c
+    auto load = [&](int it, uint32_t (&r)[12]) {
+      const int tile = static_cast<int>(blockIdx.x) + (it / nkb) * static_cast<int>(gridDim.x);
+      const int kb = it % nkb;
       int mb, nb;
       tile_coords(tile, a.mt, a.nt, kGroupM, mb, nb);
       const int64_t m0 = static_cast<int64_t>(mb) * BM;
       const int64_t n0 = static_cast<int64_t>(nb) * BN;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
+      const uint32_t* pa = sfa + static_cast<int64_t>(kb) * a.M;
+      const uint32_t* pb = sfb + static_cast<int64_t>(kb) * N + n0 + lane;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int64_t row = m0 + lane + 32 * c;
+        r[c] = row < a.M ? __ldg(pa + row) : 0x7f7f7f7fu;
+        r[4 + c] = __ldg(pb + 32 * c);
+        r[8 + c] = __ldg(pb + 128 + 32 * c);
+      }
+    };
+    uint32_t ring[kSfAhead][12];
+#pragma unroll
+    for (int u = 0; u < kSfAhead; ++u)
+      if (u < total) load(u, ring[u]);
+    bool ok = true;
+    for (int base = 0; ok && base < total; base += kSfAhead) {
+#pragma unroll
+      for (int u = 0; u < kSfAhead; ++u) {
+        const int it = base + u;
+        if (it >= total) break;
         const int s = it % STAGES8;
         const uint32_t ph = (it / STAGES8) & 1;
-        // this k-block's scales, replicated layout: column c holds row lane + 32 c
-        uint32_t ra[4], rb0[4], rb1[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int64_t row = m0 + lane + 32 * c;
-          ra[c] = row < a.M ? __ldg(sfa + static_cast<int64_t>(kb) * a.M + row) : 0x7f7f7f7fu;
-          rb0[c] = __ldg(sfb + static_cast<int64_t>(kb) * N + n0 + lane + 32 * c);
-          rb1[c] = __ldg(sfb + static_cast<int64_t>(kb) * N + n0 + 128 + lane + 32 * c);
-        }
         bool free_slot = true;
         if (lane == 0) free_slot = mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag);
         free_slot = __shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0) != 0;
@@ -1031,6 +1045,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
         }
         tc_fence_after();
         const uint32_t sf = tmem_base + lane_off + static_cast<uint32_t>(kSfBase + s * kSfCols);
+        const uint32_t ra[4] = {ring[u][0], ring[u][1], ring[u][2], ring[u][3]};
+        const uint32_t rb0[4] = {ring[u][4], ring[u][5], ring[u][6], ring[u][7]};
+        const uint32_t rb1[4] = {ring[u][8], ring[u][9], ring[u][10], ring[u][11]};
         tc_st4(sf, ra);
         tc_st4(sf + 4u, rb0);
         tc_st4(sf + 8u, rb1);
@@ -1038,6 +1055,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl8->sf_full[s]));
+        if (it + kSfAhead < total) load(it + kSfAhead, ring[u]);
       }
     }
   }
