@@ -227,6 +227,12 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
       : "memory");
 }
 
+// Arrive on a barrier at a cluster address with the default (CTA-scope)
+// release: for signals whose data is ordered by other means (tcgen05 fences).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
@@ -1070,6 +1076,252 @@ __global__ void __launch_bounds__(kThreads8, 1)
   }
 }
 
+// CTA-pair form of the FP8 projection: clusters of 2 CTAs, the even CTA
+// issuing tcgen05.mma.cta_group::2.kind::mxf8f6f4 (M = 256, N = 256).  Each
+// CTA streams its 128 e rows and its half of the pair's 256 wkv rows per
+// k-block (6 stages of 32 KB, completion on the even CTA's barrier), so each
+// SM moves half the wkv bytes of project8_kernel through shared memory.  Each
+// CTA's TMEM holds the scales of its own 128 rows of A (4 columns) and of all
+// 256 rows of B (8 columns), in the layout of project8_kernel (established by
+// a standalone probe on GB300); the scale warps of both CTAs arrive on the
+// even CTA's sf_full barrier (count 8).  Accumulator single-buffered.
+constexpr int STAGES82 = 6;
+constexpr int B82_BYTES = (BN / 2) * BK8;
+constexpr int STAGE82_BYTES = A8_BYTES + B82_BYTES;
+
+struct __align__(8) Ctl82 {
+  uint64_t sf_full[STAGES82];
+};
+
+__device__ __forceinline__ void tc_mma8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.block32 [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// M = 256 for the pair.
+__device__ __forceinline__ uint32_t idesc82(uint32_t sf_id) {
+  return (sf_id << 4) | ((static_cast<uint32_t>(BN) >> 3) << 17) | (1u << 23) |
+         ((static_cast<uint32_t>(2 * BM) >> 4) << 24) | (sf_id << 29);
+}
+
+template <bool kFuse>
+__global__ void __launch_bounds__(kThreads8, 1)
+    project82_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ProjArgs a,
+                     const uint32_t* __restrict__ sfa, const uint32_t* __restrict__ sfb) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + STAGES82 * A8_BYTES;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + STAGES82 * STAGE82_BYTES);
+  Ctl82* ctl8 = reinterpret_cast<Ctl82*>(ctl + 1);
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t rank = cluster_rank();
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int nkb = a.K / BK8;
+  const int64_t N = static_cast<int64_t>(a.hc + 1) * a.H;
+  volatile int* abort_flag = &ctl->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES82; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl8->sf_full[s]), 8);
+    }
+    mbar_init(smem_u32(&ctl->tfull[0]), 1);
+    mbar_init(smem_u32(&ctl->tempty[0]), 8);
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(TMEM8_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs)
+      int it = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < a.num_tiles; tile += npairs) {
+        int mb2, nb;
+        tile_coords(tile, a.mt2, a.nt, kGroupM2, mb2, nb);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES82;
+          const uint32_t ph = (it / STAGES82) & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag)) {
+            if (!*abort_flag) raise_abort(ctl, a);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * STAGE82_BYTES);
+          const uint32_t leader_fb = map_to_cta(fb, 0);
+          tma_load_2d_pair(smem_u32(smA + s * A8_BYTES), &tmA, kb * BK8, mb2 * (2 * BM) + static_cast<int>(rank) * BM,
+                           leader_fb);
+          tma_load_4d_pair(smem_u32(smB + s * B82_BYTES), &tmB, kb, nb * (BN / 128) + static_cast<int>(rank),
+                           leader_fb);
+        }
+      }
+      if (rank == 0) {
+        for (int j = (it > STAGES82 ? it - STAGES82 : 0); j < it; ++j)
+          mbar_wait_bounded(smem_u32(&ctl->full[j % STAGES82]), (j / STAGES82) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA only)
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < a.num_tiles; tile += npairs, ++local) {
+        if (!mbar_wait_bounded(smem_u32(&ctl->tempty[0]), (local & 1) ^ 1, abort_flag)) {
+          if (!*abort_flag) raise_abort(ctl, a);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES82;
+          const uint32_t ph = (it / STAGES82) & 1;
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag) ||
+              !mbar_wait_bounded(smem_u32(&ctl8->sf_full[s]), ph, abort_flag)) {
+            if (!*abort_flag) raise_abort(ctl, a);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smA + s * A8_BYTES);
+          const uint32_t b0 = smem_u32(smB + s * B82_BYTES);
+          const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + s * kSfCols);
+#pragma unroll
+          for (int k = 0; k < BK8 / 32; ++k)
+            tc_mma8_pair(tmem_base, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc82(static_cast<uint32_t>(k)),
+                         sf, sf + 4u, (kb | k) != 0 ? 1u : 0u);
+          tc_commit_pair(smem_u32(&ctl->empty[s]));
+        }
+        if (ok) tc_commit_pair(smem_u32(&ctl->tfull[0]));
+      }
+      tc_commit_pair(smem_u32(&ctl->drain));
+      mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr);
+    }
+  } else if (warp < 6) {
+    // ---------------- epilogue (warps 2..5 of both CTAs; each its own 128 rows)
+    const int q = warp & 3;
+    const uint32_t leader_tempty = map_to_cta(smem_u32(&ctl->tempty[0]), 0);
+    int local = 0;
+    for (int tile = pair; tile < a.num_tiles; tile += npairs, ++local) {
+      int mb2, nb;
+      tile_coords(tile, a.mt2, a.nt, kGroupM2, mb2, nb);
+      const int mb = mb2 * 2 + static_cast<int>(rank);
+      const EpiTile et = epi_tile(a, nb);
+      epilogue_stage(a, ctl, q, lane, et);
+      if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), local & 1, abort_flag)) {
+        if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      if (!epilogue_tile<kFuse>(a, ctl, q, lane, taddr, mb, et, abort_flag)) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_tempty);
+    }
+  } else {
+    // ---------------- scale warps (6..9 of both CTAs): this CTA's 128 rows of
+    // A and all 256 rows of B, kSfAhead k-blocks in flight in registers
+    constexpr int kSfAhead = 4;
+    const uint32_t q = static_cast<uint32_t>(warp & 3);
+    const uint32_t lane_off = (q * 32u) << 16;
+    const uint32_t leader_sf = map_to_cta(smem_u32(&ctl8->sf_full[0]), 0);
+    const int my_tiles = pair < a.num_tiles ? (a.num_tiles - 1 - pair) / npairs + 1 : 0;
+    const int total = my_tiles * nkb;
+    auto load = [&](int it, uint32_t (&r)[12]) {
+      const int tile = pair + (it / nkb) * npairs;
+      const int kb = it % nkb;
+      int mb2, nb;
+      tile_coords(tile, a.mt2, a.nt, kGroupM2, mb2, nb);
+      const int64_t m0 = static_cast<int64_t>(mb2) * (2 * BM) + static_cast<int64_t>(rank) * BM;
+      const int64_t n0 = static_cast<int64_t>(nb) * BN;
+      const uint32_t* pa = sfa + static_cast<int64_t>(kb) * a.M;
+      const uint32_t* pb = sfb + static_cast<int64_t>(kb) * N + n0 + lane;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int64_t row = m0 + lane + 32 * c;
+        r[c] = row < a.M ? __ldg(pa + row) : 0x7f7f7f7fu;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) r[4 + c] = __ldg(pb + 32 * c);
+    };
+    uint32_t ring[kSfAhead][12];
+#pragma unroll
+    for (int u = 0; u < kSfAhead; ++u)
+      if (u < total) load(u, ring[u]);
+    bool ok = true;
+    for (int base = 0; ok && base < total; base += kSfAhead) {
+#pragma unroll
+      for (int u = 0; u < kSfAhead; ++u) {
+        const int it = base + u;
+        if (it >= total) break;
+        const int s = it % STAGES82;
+        const uint32_t ph = (it / STAGES82) & 1;
+        bool free_slot = true;
+        if (lane == 0) free_slot = mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag);
+        free_slot = __shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0) != 0;
+        if (!free_slot) {
+          if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sf = tmem_base + lane_off + static_cast<uint32_t>(kSfBase + s * kSfCols);
+        const uint32_t ra[4] = {ring[u][0], ring[u][1], ring[u][2], ring[u][3]};
+        const uint32_t rb0[4] = {ring[u][4], ring[u][5], ring[u][6], ring[u][7]};
+        const uint32_t rb1[4] = {ring[u][8], ring[u][9], ring[u][10], ring[u][11]};
+        tc_st4(sf, ra);
+        tc_st4(sf + 4u, rb0);
+        tc_st4(sf + 8u, rb1);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        // the TMEM writes are ordered by wait::st and the tcgen05 fence; the
+        // arrive needs no cluster-scope memory fence of its own
+        if (lane == 0) mbar_arrive_remote(leader_sf + static_cast<uint32_t>(s * 8));
+        if (it + kSfAhead < total) load(it + kSfAhead, ring[u]);
+      }
+    }
+  }
+
+  // No CTA leaves while its partner may still signal its barriers or read its
+  // shared memory; then both free their TMEM.
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM8_COLS)
+                 : "memory");
+  }
+}
+
 // Block-FP8 wkv into the operand layouts of project8_kernel: codes [K][N]
 // (kv = e @ wkv) -> [N/128][K/128][128][128] bytes, so each 128 x 128-byte
 // tile of wkv^T is 16 KB contiguous; scales [K/32][N] -> [K/128][N] words,
@@ -1326,10 +1578,22 @@ int launch(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB
   return check_launch("project kernel");
 }
 
-// Argument checks and set-up of the FP8 entry points (single-CTA tiles).
+// The single-CTA FP8 kernel is the default: under the GB300 power cap it runs
+// the layer slightly faster than the CTA pair (3.12 vs 3.21 ms on 16,384
+// tokens), as both keep a single accumulator buffer.  ENGRAM_FP8_PAIR=1
+// selects the pair.
+bool use_fp8_pair() {
+  static const bool v = [] {
+    const char* e = std::getenv("ENGRAM_FP8_PAIR");
+    return e != nullptr && e[0] == '1';
+  }();
+  return v;
+}
+
+// Argument checks and set-up of the FP8 entry points.
 int prepare8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K, const uint8_t* w8_d,
              const uint32_t* sfb_d, int32_t hidden, int32_t hc, const uint16_t* h_d, const float* q_w_d,
-             const float* k_w_d, float* partials_d, int32_t* status_d, ProjArgs* a, CUtensorMap* tmA,
+             const float* k_w_d, float* partials_d, int32_t* status_d, bool pair, ProjArgs* a, CUtensorMap* tmA,
              CUtensorMap* tmB) {
   if (n_tokens < 0) return fail(ENGRAM_E_INVALID, "n_tokens < 0");
   if (K < BK8 || K % BK8 != 0 || K > (int64_t(1) << 20))
@@ -1347,7 +1611,7 @@ int prepare8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64
   if (rc) return rc;
   const int64_t N = static_cast<int64_t>(hc + 1) * hidden;
   if ((rc = make_tmap8(tmA, e8_d, static_cast<uint64_t>(n_tokens), static_cast<uint64_t>(K), BM))) return rc;
-  if ((rc = make_tmap_wkv8(tmB, w8_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 2))) return rc;
+  if ((rc = make_tmap_wkv8(tmB, w8_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), pair ? 1 : 2))) return rc;
   *a = ProjArgs{};
   a->M = n_tokens;
   a->K = static_cast<int32_t>(K);
@@ -1356,7 +1620,7 @@ int prepare8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64
   a->mt = static_cast<int32_t>((n_tokens + BM - 1) / BM);
   a->mt2 = static_cast<int32_t>((n_tokens + 2 * BM - 1) / (2 * BM));
   a->nt = static_cast<int32_t>(N / BN);
-  const int64_t tiles = static_cast<int64_t>(a->mt) * a->nt;
+  const int64_t tiles = static_cast<int64_t>(pair ? a->mt2 : a->mt) * a->nt;
   if (tiles > INT32_MAX) return fail(ENGRAM_E_SHAPE, "too many tiles");
   a->num_tiles = static_cast<int32_t>(tiles);
   a->h = const_cast<uint16_t*>(h_d);
@@ -1367,13 +1631,18 @@ int prepare8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64
   return ENGRAM_OK;
 }
 
-size_t project8_smem_bytes() { return 1024 + STAGES8 * STAGE8_BYTES + sizeof(SmemCtl) + sizeof(Ctl8); }
+size_t project8_smem_bytes(bool pair) {
+  return pair ? 1024 + STAGES82 * STAGE82_BYTES + sizeof(SmemCtl) + sizeof(Ctl82)
+              : 1024 + STAGES8 * STAGE8_BYTES + sizeof(SmemCtl) + sizeof(Ctl8);
+}
 
-int launch8(bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB, const ProjArgs& a, const uint32_t* sfa,
-            const uint32_t* sfb, cudaStream_t st) {
-  const void* fn = fused ? reinterpret_cast<const void*>(&project8_kernel<true>)
-                         : reinterpret_cast<const void*>(&project8_kernel<false>);
-  const size_t smem = project8_smem_bytes();
+int launch8(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB, const ProjArgs& a,
+            const uint32_t* sfa, const uint32_t* sfb, cudaStream_t st) {
+  const void* fn = pair ? (fused ? reinterpret_cast<const void*>(&project82_kernel<true>)
+                                 : reinterpret_cast<const void*>(&project82_kernel<false>))
+                        : (fused ? reinterpret_cast<const void*>(&project8_kernel<true>)
+                                 : reinterpret_cast<const void*>(&project8_kernel<false>));
+  const size_t smem = project8_smem_bytes(pair);
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(project8): %s", cudaGetErrorString(err));
   int sms = 0;
@@ -1383,23 +1652,43 @@ int launch8(bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB, const Pr
   cfg.blockDim = dim3(kThreads8);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int nattr = 0;
+  int units = 0;  // CTAs (single) or CTA pairs that can be resident at once
+  if (pair) {
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = 2;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+    cfg.gridDim = dim3(2 * (sms / 2));
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    err = cudaOccupancyMaxActiveClusters(&units, fn, &cfg);
+    if (err != cudaSuccess || units < 1)
+      return fail(ENGRAM_E_CUDA, "no resident CTA pair for the FP8 projection: %s", cudaGetErrorString(err));
+  } else {
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads8, smem);
+    if (err != cudaSuccess || per_sm < 1)
+      return fail(ENGRAM_E_CUDA, "no resident CTA for the FP8 projection: %s", cudaGetErrorString(err));
+    units = sms * per_sm;
+  }
   if (fused && use_cooperative()) {
     attr[nattr].id = cudaLaunchAttributeCooperative;
     attr[nattr].val.cooperative = 1;
     ++nattr;
   }
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads8, smem);
-  if (err != cudaSuccess || per_sm < 1)
-    return fail(ENGRAM_E_CUDA, "no resident CTA for the FP8 projection: %s", cudaGetErrorString(err));
-  const int units = sms * per_sm;
-  cfg.gridDim = dim3(a.num_tiles < units ? a.num_tiles : units);
+  const int n = a.num_tiles < units ? a.num_tiles : units;
+  cfg.gridDim = dim3(pair ? 2 * n : n);
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
-  err = fused ? cudaLaunchKernelEx(&cfg, project8_kernel<true>, tmA, tmB, a, sfa, sfb)
-              : cudaLaunchKernelEx(&cfg, project8_kernel<false>, tmA, tmB, a, sfa, sfb);
+  if (pair)
+    err = fused ? cudaLaunchKernelEx(&cfg, project82_kernel<true>, tmA, tmB, a, sfa, sfb)
+                : cudaLaunchKernelEx(&cfg, project82_kernel<false>, tmA, tmB, a, sfa, sfb);
+  else
+    err = fused ? cudaLaunchKernelEx(&cfg, project8_kernel<true>, tmA, tmB, a, sfa, sfb)
+                : cudaLaunchKernelEx(&cfg, project8_kernel<false>, tmA, tmB, a, sfa, sfb);
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "project8 kernel launch: %s", cudaGetErrorString(err));
   return check_launch("project8 kernel");
 }
@@ -1547,11 +1836,12 @@ extern "C" int engram_project_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, in
   if (v_d && !aligned(v_d, 16)) return fail(ENGRAM_E_ALIGN, "v must be 16-byte aligned");
   ProjArgs a;
   CUtensorMap tmA, tmB;
+  const bool pair = use_fp8_pair();
   int rc = prepare8(e8_d, sfa_d, n_tokens, K, w8_packed_d, sfb_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d,
-                    status_d, &a, &tmA, &tmB);
+                    status_d, pair, &a, &tmA, &tmB);
   if (rc || n_tokens == 0) return rc;
   a.v = v_d;
-  return launch8(false, tmA, tmB, a, sfa_d, sfb_d, as_stream(stream));
+  return launch8(pair, false, tmA, tmB, a, sfa_d, sfb_d, as_stream(stream));
 }
 
 extern "C" int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K,
@@ -1577,8 +1867,9 @@ extern "C" int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_
   }
   ProjArgs a;
   CUtensorMap tmA, tmB;
+  const bool pair = use_fp8_pair();
   int rc = prepare8(e8_d, sfa_d, n_tokens, K, w8_packed_d, sfb_d, hidden, hc, h_d, q_w_d, k_w_d,
-                    static_cast<float*>(workspace_d), status_d, &a, &tmA, &tmB);
+                    static_cast<float*>(workspace_d), status_d, pair, &a, &tmA, &tmB);
   if (rc || n_tokens == 0) return rc;
   const int mt_ws = 2 * a.mt2;
   a.cnt = reinterpret_cast<int32_t*>(base + ws.counters_off);
@@ -1593,5 +1884,5 @@ extern "C" int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_
   cudaStream_t st = as_stream(stream);
   cudaError_t err = cudaMemsetAsync(a.cnt, 0, ws.counter_words * sizeof(int32_t), st);
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaMemsetAsync(counters): %s", cudaGetErrorString(err));
-  return launch8(true, tmA, tmB, a, sfa_d, sfb_d, st);
+  return launch8(pair, true, tmA, tmB, a, sfa_d, sfb_d, st);
 }

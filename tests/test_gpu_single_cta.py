@@ -1,5 +1,6 @@
-"""The single-CTA projection kernels (selected with ENGRAM_SINGLE_CTA_MMA=1)
-pass the same projection parity tests as the default CTA-pair kernels.
+"""The alternative projection kernels pass the same parity tests as the
+defaults: the single-CTA bf16 kernels (ENGRAM_SINGLE_CTA_MMA=1) and the
+CTA-pair block-FP8 kernels (ENGRAM_FP8_PAIR=1).
 
 The selection is read once per process, so the tests run in a child process.
 """
@@ -19,5 +20,14 @@ def test_single_cta_kernels_pass_projection_parity():
     here = os.path.dirname(os.path.abspath(__file__))
     env = dict(os.environ, ENGRAM_SINGLE_CTA_MMA="1")
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_project.py"), "-m", "gpu", "-q",
+                        "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+
+
+def test_fp8_pair_kernels_pass_fp8_parity():
+    require_gpu()
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, ENGRAM_FP8_PAIR="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_fp8.py"), "-m", "gpu", "-q",
                         "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
