@@ -106,3 +106,52 @@ def test_host_side_argument_checks(lib):
     lay = eg.build_layout(1000, 4099, [1])
     assert lib.engram_hash(lay.ref, 3, P(16), 4, P(16), 1, P(16), 1300, None, P(16), P(16), None, None) == -1
     assert lib.engram_project_partials_bytes(16384, 5120, 4) == 16384 * 4 * 20 * 16
+
+
+def test_host_side_argument_checks_of_the_wider_path(lib):
+    """The FP8, fused hash + gather, short-convolution and host-gather entry
+    points reject bad shapes and pointers before touching a device."""
+    P = ctypes.c_void_p
+    E_INVALID, E_SHAPE, E_ALIGN = -1, -3, -4
+    lay = eg.build_layout(1000, 4099, [1])
+    # FP8 packing: K and N multiples of 128; nothing to do for empty batches
+    assert lib.engram_pack_wkv_fp8(P(16), P(16), 100, 256, P(16), P(16), None) == E_SHAPE
+    assert lib.engram_pack_wkv_fp8(P(16), P(16), 256, 100, P(16), P(16), None) == E_SHAPE
+    assert lib.engram_pack_wkv_fp8(None, P(16), 256, 256, P(16), P(16), None) == E_INVALID
+    # FP8 projection: K % 128, hidden % 256, hc range
+    args = (P(16), P(16), 128, 6100, P(16), P(16), 256, 4, P(16), P(16), P(16), P(16), P(16), None, None)
+    assert lib.engram_project_fp8(*args) == E_SHAPE
+    args = (P(16), P(16), 128, 6144, P(16), P(16), 200, 4, P(16), P(16), P(16), P(16), P(16), None, None)
+    assert lib.engram_project_fp8(*args) == E_SHAPE
+    args = (P(16), P(16), 128, 6144, P(16), P(16), 256, 9, P(16), P(16), P(16), P(16), P(16), None, None)
+    assert lib.engram_project_fp8(*args) == E_SHAPE
+    assert lib.engram_project_fp8(P(16), P(16), 0, 6144, P(16), P(16), 256, 4, P(16), P(16), P(16), P(16),
+                                  P(16), None, None) == 0
+    # FP8 gather: n_cols, table size, alignment
+    assert lib.engram_gather_fp8(P(16), 10, 10 * 264, P(16), 4, 0, P(16), P(16), None, None) == E_SHAPE
+    assert lib.engram_gather_fp8(P(16), 10, 10 * 264 - 1, P(16), 4, 24, P(16), P(16), None, None) == E_SHAPE
+    assert lib.engram_gather_fp8(P(17), 10, 10 * 264, P(16), 4, 24, P(16), P(16), None, None) == E_ALIGN
+    # fused hash + gather: layer range, sequence count, table size
+    assert lib.engram_hash_gather(lay.ref, 3, P(16), 4, P(16), 1, P(16), 1300, None, P(16), 10 ** 9, P(16), P(16),
+                                  None, None, None) == E_INVALID
+    assert lib.engram_hash_gather(lay.ref, 0, P(16), 4, P(16), 0, P(16), 1300, None, P(16), 10 ** 9, P(16), P(16),
+                                  None, None, None) == E_INVALID
+    assert lib.engram_hash_gather(lay.ref, 0, P(16), 4, P(16), 1, P(16), 1300, None, P(16), 264, P(16), P(16),
+                                  None, None, None) == E_SHAPE
+    assert lib.engram_hash_gather_fp8(lay.ref, 0, P(16), 4, P(16), 1, P(16), 1300, None, P(16), 264, P(16), P(16),
+                                      P(16), None, None, None) == E_SHAPE
+    # short convolution: kernel size, dilation, ring length, shapes
+    conv = lambda K, dil, hidden=256, hc=4, n_seqs=4, cu=None: lib.engram_short_conv_add(  # noqa: E731
+        P(16), P(16), P(16), None, 4, hidden, hc, cu, n_seqs, None, P(16), P(16), K, dil, 1e-6, None, None, 0,
+        P(256), 1 << 20, None, None)
+    assert conv(5, 3) == E_SHAPE
+    assert conv(0, 3) == E_SHAPE
+    assert conv(4, 0) == E_SHAPE
+    assert conv(4, 30) == E_SHAPE                 # (K-1)*dilation = 90 > 64
+    assert conv(4, 3, hidden=200) == E_SHAPE
+    assert conv(4, 3, hc=9) == E_SHAPE
+    assert conv(4, 3, n_seqs=3) == E_SHAPE        # without cu_seqlens every position is a sequence
+    assert lib.engram_short_conv_workspace_bytes(1000, 4) == 2 * 16128 + 3 * 4096
+    # host gather: sizes and pointers
+    assert lib.engram_host_gather(None, 10, None, 5, None, 0, None) == E_INVALID
+    assert lib.engram_host_gather(None, -1, None, 0, None, 0, None) == E_INVALID
