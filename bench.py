@@ -317,14 +317,18 @@ def run_ours(args, rank, world, local):
     if args.e2e_steps > 0:
         e2e = e2e_pipeline(args, b, h0, layer, hist, status, dev, world)
 
-    hgg = hash_gather_gate_bench(args, w, inp, layer, flush, dev) if args.micro_steps > 0 else None
-    micro = microbench(args, w, inp, layer, flush, dev) if args.micro_steps > 0 else None
-    dec = decode_bench(args, w, inp, layer, flush, dev) if args.decode_steps > 0 else None
-    conv = conv_bench(args, w, inp, layer, flush, dev) if args.conv_steps > 0 else None
-    fp8 = fp8_bench(args, w, inp, layer, flush, dev) if args.fp8_steps > 0 else None
+    # side phases, reported next to the headline at N = 1 only (under
+    # torchrun every rank would otherwise pin host memory and allocate the
+    # full-scale table at once)
+    side = world == 1
+    hgg = hash_gather_gate_bench(args, w, inp, layer, flush, dev) if side and args.micro_steps > 0 else None
+    micro = microbench(args, w, inp, layer, flush, dev) if side and args.micro_steps > 0 else None
+    dec = decode_bench(args, w, inp, layer, flush, dev) if side and args.decode_steps > 0 else None
+    conv = conv_bench(args, w, inp, layer, flush, dev) if side and args.conv_steps > 0 else None
+    fp8 = fp8_bench(args, w, inp, layer, flush, dev) if side and args.fp8_steps > 0 else None
     host = host_table_bench(args, w, inp, layer, flush, dev, statistics.mean(step_ms)) \
-        if args.host_steps > 0 else None
-    full = fullscale_bench(args, inp, layer, dev) if args.fullscale_passes > 0 else None
+        if side and args.host_steps > 0 else None
+    full = fullscale_bench(args, inp, layer, dev) if side and args.fullscale_passes > 0 else None
 
     if rank != 0:
         return None
