@@ -1465,14 +1465,19 @@ size_t project_smem_bytes(bool pair) {
   return 1024 + (pair ? STAGES2 * STAGE2_BYTES : STAGES * STAGE_BYTES) + sizeof(SmemCtl);
 }
 
-// The CTA-pair kernel is the default; ENGRAM_SINGLE_CTA_MMA=1 selects the
-// single-CTA kernel (for comparisons).
-bool use_pair_kernel() {
-  static const bool pair = [] {
+// The CTA-pair kernel is the default from 129 tokens on.  A batch of at most
+// 128 tokens (one 128-row block) runs the single-CTA kernel: the pair's second
+// CTA would hold no rows, and as 128 x 256 tiles the column tiles fill the SMs
+// in one wave where the pairs need two (GB300, hidden 5120, 128 tokens, L2
+// flushed: 72 us single-CTA vs 87 us pair).  ENGRAM_SINGLE_CTA_MMA=1 selects
+// the single-CTA kernel and =0 the pair at every size (for comparisons).
+bool use_pair_kernel(int64_t n_tokens) {
+  static const int forced = [] {
     const char* v = std::getenv("ENGRAM_SINGLE_CTA_MMA");
-    return !(v != nullptr && v[0] == '1');
+    return v == nullptr ? -1 : (v[0] == '1' ? 1 : 0);
   }();
-  return pair;
+  if (forced >= 0) return forced == 0;
+  return n_tokens > BM;
 }
 
 // Shared argument checks and set-up of both projection entry points.
@@ -1724,7 +1729,7 @@ extern "C" int engram_project(const uint16_t* e_d, int64_t n_tokens, int64_t K,
                               float* partials_d, uint16_t* v_d, int32_t* status_d, void* stream) {
   if (!v_d && n_tokens > 0) return fail(ENGRAM_E_INVALID, "null device pointer");
   if (v_d && !aligned(v_d, 16)) return fail(ENGRAM_E_ALIGN, "v must be 16-byte aligned");
-  const bool pair = use_pair_kernel();
+  const bool pair = use_pair_kernel(n_tokens);
   ProjArgs a;
   CUtensorMap tmA, tmB;
   int rc = prepare(e_d, n_tokens, K, wkv_packed_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d, status_d, pair, &a,
@@ -1788,7 +1793,7 @@ extern "C" int engram_project_gate(const uint16_t* e_d, int64_t n_tokens, int64_
     return engram_gate_add(partials_d, v_d, h_d, mask_d, n_tokens, hidden, hc, eps, clamp, score_scale, gate_out_d,
                            stream);
   }
-  const bool pair = use_pair_kernel();
+  const bool pair = use_pair_kernel(n_tokens);
   ProjArgs a;
   CUtensorMap tmA, tmB;
   float* partials_d = static_cast<float*>(workspace_d);

@@ -121,6 +121,18 @@ def test_project_large_m_tiles():
     assert ok, (worst, strict)
 
 
+def _assert_same_update(hu_bits, hb_bits, g_u, v_u):
+    """Two computations of h <- bf16(h + g bf16(v)) whose fp32 sums ran in a
+    different order (fused or not, K split or not): bf16(v) may differ by one
+    bf16 step (2^-7 of |v|) and g by fp32 rounding, so h may differ by one
+    step of the result plus g times one step of v."""
+    hu, hb = bf16_bits_to_f64(hu_bits), bf16_bits_to_f64(hb_bits)
+    v = np.abs(bf16_bits_to_f64(bits(v_u)))[:, None, :]
+    gv = np.abs(g_u.cpu().numpy().astype(np.float64))[:, :, None] * v
+    bound = 2.0 ** -7 * (np.abs(hu) + 2.0 * gv) + 2e-5 * v + 1e-30
+    assert (np.abs(hu - hb) <= bound).all()
+
+
 @pytest.mark.parametrize("T,H,hc", [(128, 256, 4), (300, 256, 4), (1, 256, 4), (129, 512, 2), (257, 256, 1),
                                     (1537, 256, 4), (1600, 512, 2), (2100, 256, 4)])
 def test_project_gate_fused(T, H, hc):
@@ -154,9 +166,7 @@ def test_project_gate_fused(T, H, hc):
     partials, v_d = eg.engram_project(e_d, wp, h_u, qw_d, kw_d)
     eg.engram_gate_add(partials, v_d, h_u, m_d, gate_out=g_u)
     assert np.abs(g_u.cpu().numpy() - gf).max() <= 1e-5
-    hu = bf16_bits_to_f64(bits(h_u))
-    diff = np.abs(hu - bf16_bits_to_f64(hb))
-    assert (diff <= 2.0 ** -7 * np.maximum(np.abs(hu), 1e-30) + 1e-30).all()
+    _assert_same_update(bits(h_u), hb, g_u, v_d)
 
 
 def test_project_gate_fused_many_groups():
@@ -178,3 +188,35 @@ def test_project_gate_fused_many_groups():
     ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
     assert ok, (worst, strict)
     assert (bits(h_d)[mask] == h[mask]).all()
+
+
+@pytest.mark.parametrize("T", [256, 37])
+def test_project_gate_decode_shape(T):
+    """Decode-size batches at hidden 5120 (100 column tiles) through
+    engram_project_gate's two-kernel path: 256 tokens on the CTA-pair kernel,
+    37 on the single-CTA kernel.  Sampled rows against the oracle; every row
+    against engram_project + engram_gate_add to fp32 summation order."""
+    H, hc = 5120, 4
+    e, w, h, qw, kw = _inputs(T, H, hc, seed=500 + T)
+    mask = np.zeros(T, dtype=bool)
+    mask[[1, T - 2]] = True
+    wp = eg.engram_pack_wkv(bf16(w))
+    e_d, qw_d, kw_d, m_d = bf16(e), f32(qw), f32(kw), u8(mask)
+    h_d = bf16(h)
+    gate = torch.empty((T, hc), dtype=torch.float32, device=DEV)
+    st = status()
+    eg.engram_project_gate(e_d, wp, h_d, qw_d, kw_d, m_d, gate_out=gate, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    idx = np.unique(np.concatenate([np.arange(0, T, 16), [1, T - 2, T - 1]]))
+    k, v, hf, g, out, k_err, v_err = _oracle(e[idx], w, h[idx], qw, kw, mask[idx], len(idx), H, hc)
+    assert np.abs(gate.cpu().numpy()[idx] - g).max() <= GATE_ATOL
+    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
+    assert ok, (worst, strict)
+    assert (bits(h_d)[mask] == h[mask]).all()
+    h_u = bf16(h)
+    g_u = torch.empty((T, hc), dtype=torch.float32, device=DEV)
+    partials, v_u = eg.engram_project(e_d, wp, h_u, qw_d, kw_d)
+    eg.engram_gate_add(partials, v_u, h_u, m_d, gate_out=g_u)
+    assert np.abs(g_u.cpu().numpy() - gate.cpu().numpy()).max() <= 1e-5
+    _assert_same_update(bits(h_u), bits(h_d), g_u, v_u)

@@ -1,6 +1,8 @@
 """The alternative projection kernels pass the same parity tests as the
-defaults: the single-CTA bf16 kernels (ENGRAM_SINGLE_CTA_MMA=1) and the
-CTA-pair block-FP8 kernels (ENGRAM_FP8_PAIR=1).
+defaults: the single-CTA bf16 kernels at every size (ENGRAM_SINGLE_CTA_MMA=1),
+the CTA-pair bf16 kernels at every size (=0; by default batches of at most
+128 tokens take the single-CTA kernel), and the CTA-pair block-FP8 kernels
+(ENGRAM_FP8_PAIR=1).
 
 The selection is read once per process, so the tests run in a child process.
 """
@@ -29,5 +31,15 @@ def test_fp8_pair_kernels_pass_fp8_parity():
     here = os.path.dirname(os.path.abspath(__file__))
     env = dict(os.environ, ENGRAM_FP8_PAIR="1")
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_fp8.py"), "-m", "gpu", "-q",
+                        "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+
+
+
+def test_pair_kernels_at_every_size_pass_projection_parity():
+    require_gpu()
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, ENGRAM_SINGLE_CTA_MMA="0")
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_project.py"), "-m", "gpu", "-q",
                         "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
