@@ -136,3 +136,9 @@ def test_fp8_layer_fused_path():
 def test_fp8_layer_prefill_sampled():
     """The prefill batch (16,384 tokens, hidden 5120) through the fused FP8 kernel, every 61st token."""
     _fp8_layer_case("prefill", sample=61, seed=2)
+
+
+@pytest.mark.parametrize("T", [256, 37])
+def test_fp8_layer_decode_size(T):
+    """Decode-size batches at hidden 5120 through the two-kernel FP8 path, every 16th token."""
+    _fp8_layer_case("prefill", T_cut=T, sample=16, seed=3)
