@@ -1468,8 +1468,8 @@ size_t project_smem_bytes(bool pair) {
 // The CTA-pair kernel is the default from 129 tokens on.  A batch of at most
 // 128 tokens (one 128-row block) runs the single-CTA kernel: the pair's second
 // CTA would hold no rows, and as 128 x 256 tiles the column tiles fill the SMs
-// in one wave where the pairs need two (GB300, hidden 5120, 128 tokens, L2
-// flushed: 72 us single-CTA vs 87 us pair).  ENGRAM_SINGLE_CTA_MMA=1 selects
+// in one wave where the pairs need two (GB300, hidden 5120, 128 tokens, after
+// writing a buffer larger than L2: 72 us single-CTA vs 87 us pair).  ENGRAM_SINGLE_CTA_MMA=1 selects
 // the single-CTA kernel and =0 the pair at every size (for comparisons).
 bool use_pair_kernel(int64_t n_tokens) {
   static const int forced = [] {
