@@ -134,13 +134,15 @@ def _assert_same_update(hu_bits, hb_bits, g_u, v_u):
 
 
 @pytest.mark.parametrize("T,H,hc", [(128, 256, 4), (300, 256, 4), (1, 256, 4), (129, 512, 2), (257, 256, 1),
-                                    (1537, 256, 4), (1600, 512, 2), (2100, 256, 4)])
+                                    (1537, 256, 4), (1600, 512, 2), (2100, 256, 4),
+                                    (100, 256, 8), (300, 256, 6), (1600, 256, 8), (1800, 256, 5)])
 def test_project_gate_fused(T, H, hc):
     """engram_project_gate against the oracle and against the unfused kernels.
 
     Up to 1536 tokens the entry point runs the two-kernel path in its
     workspace; from 1537 tokens on (ragged: 6 pair blocks + 1 row) the fused
-    cooperative kernel."""
+    cooperative kernel.  5 to 8 residual streams take the fused value
+    epilogue's path for streams beyond the fourth."""
     e, w, h, qw, kw = _inputs(T, H, hc, seed=1000 + T)
     mask = np.zeros(T, dtype=bool)
     mask[5::11] = True
