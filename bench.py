@@ -685,13 +685,17 @@ def decode_bench(args, w, inp, layer, flush, dev):
     work = eg.project_gate_workspace(B, wd.hidden, wd.hc, dev)
     stream = torch.cuda.current_stream(dev)
 
-    def run(k, ev=None):
+    def run(k, ev=None, fused=True):
         if ev is not None:
             ev[0].record(stream)
-        eg.engram_hash_step(layer.layout, 0, steps[k], slots, layer.token_map, hist, rows, mask)
+        if fused:
+            eg.engram_hash_gather_step(layer.layout, 0, steps[k], slots, layer.token_map, layer.table, hist, e, mask)
+        else:
+            eg.engram_hash_step(layer.layout, 0, steps[k], slots, layer.token_map, hist, rows, mask)
         if ev is not None:
             ev[1].record(stream)
-        eg.engram_gather_dequant(layer.table, layer.total_rows, rows, e)
+        if not fused:
+            eg.engram_gather_dequant(layer.table, layer.total_rows, rows, e)
         if ev is not None:
             ev[2].record(stream)
         eg.engram_project_gate(e, layer.wkv_packed, h, layer.q_w, layer.k_w, mask, layer.eps, layer.clamp,
@@ -699,23 +703,37 @@ def decode_bench(args, w, inp, layer, flush, dev):
         if ev is not None:
             ev[3].record(stream)
 
-    for k in range(3):
-        flush()
-        run(k)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
-    for k in range(n):
-        flush()
-        run(3 + k, evs[k])
-    torch.cuda.synchronize()
-    step = statistics.mean(ev[0].elapsed_time(ev[3]) for ev in evs) / 1e3
-    proj = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs) / 1e3
+    def timed(fused):
+        for k in range(3):
+            flush()
+            run(k, fused=fused)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        for k in range(n):
+            flush()
+            run(3 + k, evs[k], fused=fused)
+        torch.cuda.synchronize()
+        return evs
+
+    def mean_ms(evs, i, j):
+        return statistics.mean(ev[i].elapsed_time(ev[j]) for ev in evs)
+
+    # the separate hash step and gather first (for the split), then the fused
+    # step from the same start; both advance the histories through the same steps
+    evs = timed(False)
+    hist.fill_(layer.layout.pad_id)
+    eg.engram_hash(layer.layout, 0, torch.from_numpy(dw.prefix.raw_ids).to(dev),
+                   torch.from_numpy(dw.prefix.cu_seqlens).to(dev), layer.token_map, hist)
+    evf = timed(True)
+    step = mean_ms(evf, 0, 3) / 1e3
+    proj = mean_ms(evf, 2, 3) / 1e3
     wkv_bytes = 6144 * (wd.hc + 1) * wd.hidden * 2
     out = {"workload": f"decode: {B} sequences x 1 token, histories from U[0, 8192] prefixes, table of the "
                        f"{w.name} workload", "steps": n,
            "step_ms": step * 1e3, "steps_per_s": 1 / step, "tokens_per_s": B / step,
-           "hash_step_ms": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
-           "gather_ms": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs),
-           "project_gate_ms": proj * 1e3, "wkv_gbs": wkv_bytes / proj / 1e9}
+           "hash_gather_ms": mean_ms(evf, 0, 1), "project_gate_ms": proj * 1e3, "wkv_gbs": wkv_bytes / proj / 1e9,
+           "kernels": "engram_hash_gather_step (hash + history roll + gather in one kernel), engram_project_gate",
+           "separate_calls": {"step_ms": mean_ms(evs, 0, 3), "hash_step_ms": mean_ms(evs, 0, 1),
+                              "gather_ms": mean_ms(evs, 1, 2), "project_gate_ms": mean_ms(evs, 2, 3)}}
     if args.fp8_steps <= 0:
         return out
 
@@ -730,11 +748,10 @@ def decode_bench(args, w, inp, layer, flush, dev):
     def run8(k, ev=None):
         if ev is not None:
             ev[0].record(stream)
-        eg.engram_hash_step(layer.layout, 0, steps[k], slots, layer.token_map, hist, rows, mask)
+        eg.engram_hash_gather_step_fp8(layer.layout, 0, steps[k], slots, layer.token_map, layer.table, hist, e8,
+                                       sfa, mask)
         if ev is not None:
             ev[1].record(stream)
-        eg.engram_gather_fp8(layer.table, layer.total_rows, rows, e8, sfa)
-        if ev is not None:
             ev[2].record(stream)
         eg.engram_project_gate_fp8(e8, sfa, w8p, sfb, h, layer.q_w, layer.k_w, mask, layer.eps, layer.clamp,
                                    layer.score_scale, None, work)
@@ -754,7 +771,7 @@ def decode_bench(args, w, inp, layer, flush, dev):
     wkv8_bytes = 6144 * (wd.hc + 1) * wd.hidden * (1 + 1 / 32)
     out["fp8"] = {"workload": "the same steps with block-FP8 wkv (E4M3, E8M0 per 32 of k), rows gathered as stored",
                   "step_ms": step8 * 1e3, "tokens_per_s": B / step8,
-                  "gather_ms": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs),
+                  "hash_gather_ms": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
                   "project_gate_ms": proj8 * 1e3, "wkv_gbs": wkv8_bytes / proj8 / 1e9}
     return out
 

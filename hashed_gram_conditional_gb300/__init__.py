@@ -20,6 +20,8 @@ import torch
 
 __all__ = [
     "EngramError", "Layout", "build_layout", "engram_hash", "engram_hash_all_layers", "engram_hash_step",
+    "engram_hash_gather", "engram_hash_gather_step", "engram_hash_gather_fp8", "engram_hash_gather_step_fp8",
+    "engram_gather_fp8",
     "engram_gather_dequant", "engram_dequant_rows", "engram_host_gather", "engram_host_gather_async",
     "engram_pack_wkv", "engram_project", "engram_gate_add", "engram_fill_synthetic_table",
     "engram_selftest_mod", "engram_project_gate", "project_gate_workspace", "partials_shape", "EngramLayer",
@@ -110,6 +112,10 @@ _SIGS = {
     "engram_gather_fp8": [_P, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _P],
     "engram_hash_gather_fp8": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _I64, _P, _P,
                                _P, _P, _P, _P],
+    "engram_hash_gather_step": [ctypes.POINTER(_Layout), _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P, _I64, _P, _P,
+                                _P, _P, _P],
+    "engram_hash_gather_step_fp8": [ctypes.POINTER(_Layout), _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P, _I64, _P,
+                                    _P, _P, _P, _P, _P],
     "engram_pack_wkv_fp8": [_P, _P, _I64, _I64, _P, _P, _P],
     "engram_project_fp8": [_P, _P, _I64, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P],
     "engram_project_gate_fp8": [_P, _P, _I64, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P, _F32, _F32, _F32, _P, _P,
@@ -347,6 +353,73 @@ def engram_hash_step(layout: Layout, layer: int, raw_ids: torch.Tensor, slots: t
                               token_map.numel(), _ptr(hist), hist.numel() // depth, _ptr(row_ids), _ptr(mask),
                               _ptr(status), _stream(dev)), "engram_hash_step")
     return row_ids, mask
+
+
+def _step_args(layout: Layout, raw_ids: torch.Tensor, slots: torch.Tensor, token_map: torch.Tensor,
+               table: torch.Tensor, hist: torch.Tensor, mask, row_ids):
+    """Checks shared by the fused decode steps; returns (B, n_slots, mask)."""
+    dev = raw_ids.device
+    B = raw_ids.numel()
+    _need(raw_ids, "raw_ids", torch.int32)
+    _need(slots, "slots", torch.int32, dev, B)
+    _need(token_map, "token_map", torch.int32, dev)
+    _need(hist, "hist", torch.int32, dev)
+    if table.is_cuda:
+        _need(table, "table", torch.uint8, dev)
+    elif not (table.dtype == torch.uint8 and table.is_pinned() and table.is_contiguous()):
+        raise ValueError("a host table must be a contiguous pinned uint8 tensor (read over NVLink-C2C)")
+    depth = layout.max_ngram - 1
+    if hist.numel() % depth:
+        raise ValueError("hist must be [n_slots][max_ngram-1]")
+    if mask is None:
+        mask = torch.empty(B, dtype=torch.uint8, device=dev)
+    _need(mask, "mask", torch.uint8, dev, B)
+    if row_ids is not None:
+        _need(row_ids, "row_ids", torch.int32, dev, B * layout.n_cols)
+    return B, hist.numel() // depth, mask
+
+
+def engram_hash_gather_step(layout: Layout, layer: int, raw_ids: torch.Tensor, slots: torch.Tensor,
+                            token_map: torch.Tensor, table: torch.Tensor, hist: torch.Tensor,
+                            e: Optional[torch.Tensor] = None, mask: Optional[torch.Tensor] = None,
+                            row_ids: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """One decode step hashed and gathered in one kernel: returns (e bf16 [B][n_cols*256], mask uint8 [B]);
+    hist [S][max_ngram-1] is rolled in place; row_ids is filled only when given."""
+    L = _load()
+    dev = raw_ids.device
+    B, n_slots, mask = _step_args(layout, raw_ids, slots, token_map, table, hist, mask, row_ids)
+    C = layout.n_cols
+    if e is None:
+        e = torch.empty((B, C * HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    _need(e, "e", torch.bfloat16, dev, B * C * HEAD_DIM)
+    _check(L.engram_hash_gather_step(layout.ref, layer, _ptr(raw_ids), _ptr(slots), B, _ptr(token_map),
+                                     token_map.numel(), _ptr(hist), n_slots, _ptr(table), table.numel(), _ptr(e),
+                                     _ptr(mask), _ptr(row_ids), _ptr(status), _stream(dev)),
+           "engram_hash_gather_step")
+    return e, mask
+
+
+def engram_hash_gather_step_fp8(layout: Layout, layer: int, raw_ids: torch.Tensor, slots: torch.Tensor,
+                                token_map: torch.Tensor, table: torch.Tensor, hist: torch.Tensor,
+                                e8: Optional[torch.Tensor] = None, sf: Optional[torch.Tensor] = None,
+                                mask: Optional[torch.Tensor] = None, row_ids: Optional[torch.Tensor] = None,
+                                status: Optional[torch.Tensor] = None):
+    """engram_hash_gather_step with FP8 outputs; returns (e8, sf, mask)."""
+    L = _load()
+    dev = raw_ids.device
+    B, n_slots, mask = _step_args(layout, raw_ids, slots, token_map, table, hist, mask, row_ids)
+    C = layout.n_cols
+    if e8 is None:
+        e8 = torch.empty((B, C * HEAD_DIM), dtype=torch.uint8, device=dev)
+    if sf is None:
+        sf = torch.empty((2 * C, B), dtype=torch.int32, device=dev)
+    _need(e8, "e8", torch.uint8, dev, B * C * HEAD_DIM)
+    _need(sf, "sf", torch.int32, dev, 2 * C * B)
+    _check(L.engram_hash_gather_step_fp8(layout.ref, layer, _ptr(raw_ids), _ptr(slots), B, _ptr(token_map),
+                                         token_map.numel(), _ptr(hist), n_slots, _ptr(table), table.numel(),
+                                         _ptr(e8), _ptr(sf), _ptr(mask), _ptr(row_ids), _ptr(status), _stream(dev)),
+           "engram_hash_gather_step_fp8")
+    return e8, sf, mask
 
 
 def engram_gather_dequant(table: torch.Tensor, total_rows: int, row_ids: torch.Tensor,
@@ -922,9 +995,8 @@ class EngramLayer:
                conv_state: Optional[tuple] = None):
         B = raw_ids.numel()
         b = self._buffers(B, raw_ids.device)
-        engram_hash_step(self.layout, self.layer, raw_ids, slots, self.token_map, hist, b["rows"], b["mask"],
-                         status)
-        engram_gather_dequant(self.table, self.total_rows, b["rows"], b["e"], status)
+        engram_hash_gather_step(self.layout, self.layer, raw_ids, slots, self.token_map, self.table, hist, b["e"],
+                                b["mask"], b["rows"], status)
         self._gate(b, h, status, gate_out, slots=slots, conv_state=conv_state)
         return b
 

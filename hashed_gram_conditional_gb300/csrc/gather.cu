@@ -233,6 +233,33 @@ struct HashedRows {
   }
 };
 
+// ... or computed from a decode entry's new id and its carried history, the
+// history rolled in the same warp once every lane has read its slot (entries
+// of one call name distinct slots, so no other warp touches it).
+struct StepRows {
+  hashdev::HashConsts c;
+  const int32_t* raw;
+  const int32_t* slots;
+  const int32_t* tmap;
+  int32_t* hist;
+  int64_t n_slots;
+  int32_t* rows_out;  // or null
+  uint8_t* mask;
+  int32_t* status;
+  __device__ __forceinline__ int32_t operator()(int64_t b, uint32_t lane, int n_cols) const {
+    bool pad_row;
+    int32_t xnew;
+    const int32_t slot = hashdev::step_slot(c, b, raw, slots, tmap, hist, n_slots, status, &pad_row, &xnew);
+    int32_t row;
+    const bool dead = hashdev::window_rows(slot, c, &row);
+    if (rows_out != nullptr && lane < static_cast<uint32_t>(n_cols)) rows_out[b * n_cols + lane] = row;
+    if (lane == 0) mask[b] = (dead || pad_row) ? 1 : 0;
+    __syncwarp();
+    hashdev::step_commit(c, b, slots, hist, pad_row, xnew, slot);
+    return row;
+  }
+};
+
 // What a warp writes for a position once its rows sit in shared memory
 // (row j at sb + j * 272 + 8 if odd): dequantised bf16 rows ...
 struct Bf16Out {
@@ -561,6 +588,56 @@ extern "C" int engram_hash_gather_fp8(const engram_layout* layout, int32_t layer
   if (hist_d != nullptr)
     return hashdev::launch_hist_commit(c, raw_ids_d, cu_seqlens_d, n_seqs, token_map_d, hist_d, status_d, st);
   return ENGRAM_OK;
+}
+
+namespace {
+// Shared checks and launch of the fused decode steps (bf16 or FP8 outputs).
+template <class Out>
+int hash_gather_step(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d, const int32_t* slots_d,
+                     int32_t batch, const int32_t* token_map_d, int64_t vocab_raw, int32_t* hist_d, int64_t n_slots,
+                     const uint8_t* table_d, int64_t table_bytes, void* out_d, uint8_t* mask_d, int32_t* row_ids_d,
+                     int32_t* status_d, void* stream, Out out) {
+  hashdev::HashConsts c;
+  int rc = hashdev::make_consts(layout, layer, vocab_raw, &c);
+  if (rc) return rc;
+  const int64_t total_rows = layout->total_rows[layer];
+  if (batch < 0 || n_slots < 0) return fail(ENGRAM_E_INVALID, "negative batch or n_slots");
+  if (table_bytes < total_rows * kRowBytes)
+    return fail(ENGRAM_E_SHAPE, "table_bytes %lld < total_rows * 264", (long long)table_bytes);
+  if (batch == 0) return ENGRAM_OK;
+  if (!raw_ids_d || !slots_d || !token_map_d || !table_d || !out_d || !mask_d || (n_slots > 0 && !hist_d))
+    return fail(ENGRAM_E_INVALID, "null device pointer");
+  if (!aligned(table_d, 16) || !aligned(out_d, 16)) return fail(ENGRAM_E_ALIGN, "table and e must be 16-byte aligned");
+  int sms = 0;
+  if ((rc = check_device(&sms))) return rc;
+  int stages = 0;
+  size_t smem = 0;
+  if ((rc = gather_config(c.n_cols, &stages, &smem))) return rc;
+  GatherArgs a{table_d, total_rows, table_bytes, nullptr, batch, c.n_cols, stages, nullptr, status_d};
+  StepRows src{c, raw_ids_d, slots_d, token_map_d, hist_d, n_slots, row_ids_d, mask_d, status_d};
+  return launch_ldgsts(a, src, out, smem, sms, as_stream(stream));
+}
+}  // namespace
+
+extern "C" int engram_hash_gather_step(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
+                                       const int32_t* slots_d, int32_t batch, const int32_t* token_map_d,
+                                       int64_t vocab_raw, int32_t* hist_d, int64_t n_slots, const uint8_t* table_d,
+                                       int64_t table_bytes, uint16_t* e_d, uint8_t* mask_d, int32_t* row_ids_d,
+                                       int32_t* status_d, void* stream) {
+  return hash_gather_step(layout, layer, raw_ids_d, slots_d, batch, token_map_d, vocab_raw, hist_d, n_slots, table_d,
+                          table_bytes, e_d, mask_d, row_ids_d, status_d, stream, Bf16Out{e_d});
+}
+
+extern "C" int engram_hash_gather_step_fp8(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
+                                           const int32_t* slots_d, int32_t batch, const int32_t* token_map_d,
+                                           int64_t vocab_raw, int32_t* hist_d, int64_t n_slots,
+                                           const uint8_t* table_d, int64_t table_bytes, uint8_t* e8_d,
+                                           uint32_t* sf_d, uint8_t* mask_d, int32_t* row_ids_d, int32_t* status_d,
+                                           void* stream) {
+  if (batch > 0 && (sf_d == nullptr || !aligned(sf_d, 4)))
+    return fail(ENGRAM_E_INVALID, "sf must be a 4-byte aligned device pointer");
+  return hash_gather_step(layout, layer, raw_ids_d, slots_d, batch, token_map_d, vocab_raw, hist_d, n_slots, table_d,
+                          table_bytes, e8_d, mask_d, row_ids_d, status_d, stream, Fp8Out{e8_d, sf_d, batch});
 }
 
 extern "C" int engram_dequant_rows(const uint8_t* rows_d, int64_t n_rows, int64_t rows_bytes, int32_t n_cols,

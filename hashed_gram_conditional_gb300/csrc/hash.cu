@@ -94,33 +94,16 @@ __global__ void __launch_bounds__(256) hash_step_kernel(
     HashConsts c, const int32_t* __restrict__ raw, const int32_t* __restrict__ slots, int32_t batch,
     const int32_t* __restrict__ tmap, int32_t* hist, int64_t n_slots, int32_t* __restrict__ rows,
     uint8_t* __restrict__ mask, int32_t* status) {
-  const uint32_t lane = lane_id();
   const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (b >= batch) return;
-  const int depth = c.max_ngram - 1;
-  int32_t sl = slots[b];
-  bool pad_row = sl < 0;
-  if (sl >= 0 && static_cast<int64_t>(sl) >= n_slots) {
-    if (lane == 0 && status) atomicOr(status, static_cast<int>(ENGRAM_ST_BAD_SLOT));
-    pad_row = true;
-  }
-  int32_t slot = c.pad_id;
-  int32_t xnew = kDead;
-  if (lane == 0) {
-    xnew = compress_id(raw[b], tmap, c, status);
-    slot = xnew;
-  } else if (lane < static_cast<uint32_t>(c.max_ngram) && !pad_row) {
-    slot = check_hist(hist[static_cast<int64_t>(sl) * depth + (lane - 1)], c, status);
-  }
+  bool pad_row;
+  int32_t xnew;
+  const int32_t slot = step_slot(c, b, raw, slots, tmap, hist, n_slots, status, &pad_row, &xnew);
   // Every lane's history read has been consumed by the shuffles inside
   // hash_window before any lane writes the row below.
   hash_window(slot, c, rows + static_cast<int64_t>(b) * c.n_cols, mask + b, pad_row);
   __syncwarp();
-  // Roll (h0, h1, ...) <- (x', h0, ...): lane i holds window slot g_i =
-  // x'_{t-i}, which is exactly the new history entry i (most recent first).
-  if (!pad_row && lane < static_cast<uint32_t>(depth)) {
-    hist[static_cast<int64_t>(sl) * depth + lane] = (lane == 0) ? xnew : slot;
-  }
+  step_commit(c, b, slots, hist, pad_row, xnew, slot);
 }
 
 __global__ void selftest_mod_kernel(HashConsts c, const uint64_t* __restrict__ x, int64_t n,

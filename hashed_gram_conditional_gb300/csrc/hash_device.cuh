@@ -177,6 +177,46 @@ __device__ __forceinline__ int32_t prefill_slot(const HashConsts& c, int64_t t, 
   return slot;
 }
 
+// The window slot of lane i < max_ngram for decode entry b: lane 0 the new
+// compressed id, lanes 1.. the entry's carried history (most recent first),
+// all pad for a padding entry (slot < 0) or a slot >= n_slots (which also
+// sets ENGRAM_ST_BAD_SLOT).  *pad_row tells the caller the entry commits
+// nothing; *xnew (lane 0) is the new id.
+__device__ __forceinline__ int32_t step_slot(const HashConsts& c, int64_t b, const int32_t* __restrict__ raw,
+                                             const int32_t* __restrict__ slots, const int32_t* __restrict__ tmap,
+                                             const int32_t* hist, int64_t n_slots, int32_t* status, bool* pad_row,
+                                             int32_t* xnew) {
+  const uint32_t lane = lane_id();
+  const int depth = c.max_ngram - 1;
+  const int32_t sl = slots[b];
+  bool pad = sl < 0;
+  if (sl >= 0 && static_cast<int64_t>(sl) >= n_slots) {
+    if (lane == 0 && status) atomicOr(status, static_cast<int>(ENGRAM_ST_BAD_SLOT));
+    pad = true;
+  }
+  int32_t slot = c.pad_id;
+  *xnew = kDead;
+  if (lane == 0) {
+    *xnew = compress_id(raw[b], tmap, c, status);
+    slot = *xnew;
+  } else if (lane < static_cast<uint32_t>(c.max_ngram) && !pad) {
+    slot = check_hist(hist[static_cast<int64_t>(sl) * depth + (lane - 1)], c, status);
+  }
+  *pad_row = pad;
+  return slot;
+}
+
+// Commit of decode entry b after every lane has consumed its window slot:
+// (h0, h1, ...) <- (x', h0, ...).  Lane i holds g_i = x'_{t-i}, which is the
+// new history entry i (most recent first).
+__device__ __forceinline__ void step_commit(const HashConsts& c, int64_t b, const int32_t* __restrict__ slots,
+                                            int32_t* hist, bool pad_row, int32_t xnew, int32_t slot) {
+  const uint32_t lane = lane_id();
+  const int depth = c.max_ngram - 1;
+  if (!pad_row && lane < static_cast<uint32_t>(depth))
+    hist[static_cast<int64_t>(slots[b]) * depth + lane] = (lane == 0) ? xnew : slot;
+}
+
 // Launches the history commit of a prefill chunk (hash.cu): the last
 // max_ngram-1 compressed ids of each sequence, most recent first.
 int launch_hist_commit(const HashConsts& c, const int32_t* raw, const int64_t* cu, int32_t n_seqs,

@@ -262,6 +262,32 @@ int engram_hash_gather_fp8(const engram_layout* layout, int32_t layer, const int
                            uint8_t* e8_d, uint32_t* sf_d, uint8_t* mask_d, int32_t* row_ids_d, int32_t* status_d,
                            void* stream);
 
+/* One decode step fused with its gather: the hash of engram_hash_step and
+ * the gather of engram_gather_dequant in one kernel ([P-O1] §4.4: the decode
+ * hash state is the last 3 ids of each sequence; [P-O1] §2.4: the rows depend
+ * only on the token ids).  The warp that gathers entry b computes its row ids
+ * from raw_ids_d[b] and the history row slots_d[b], then rolls that history
+ * row; entries of one call must name distinct slots.  Arguments as in
+ * engram_hash_step and engram_gather_dequant, with the table of layer `layer`:
+ *   table_d    uint8 [total_rows][264], 16-byte aligned; table_bytes >= total_rows * 264
+ *   e_d        bf16 [batch][n_cols*256] out, 16-byte aligned
+ *   mask_d     uint8 [batch] out (1 = DEAD or padding entry)
+ *   row_ids_d  int32 [batch][n_cols] out, or NULL (not written)
+ * Status bits as for the two calls it fuses. */
+int engram_hash_gather_step(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
+                            const int32_t* slots_d, int32_t batch, const int32_t* token_map_d, int64_t vocab_raw,
+                            int32_t* hist_d, int64_t n_slots, const uint8_t* table_d, int64_t table_bytes,
+                            uint16_t* e_d, uint8_t* mask_d, int32_t* row_ids_d, int32_t* status_d, void* stream);
+
+/* engram_hash_gather_step with the FP8 outputs of engram_gather_fp8
+ * (e8_d uint8 [batch][n_cols*256] 16-byte aligned, sf_d uint32 [n_cols*2][batch]
+ * 4-byte aligned). */
+int engram_hash_gather_step_fp8(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
+                                const int32_t* slots_d, int32_t batch, const int32_t* token_map_d,
+                                int64_t vocab_raw, int32_t* hist_d, int64_t n_slots, const uint8_t* table_d,
+                                int64_t table_bytes, uint8_t* e8_d, uint32_t* sf_d, uint8_t* mask_d,
+                                int32_t* row_ids_d, int32_t* status_d, void* stream);
+
 /* Dequantise rows that already sit contiguously in device memory (e.g. after
  * a host-side gather and one DMA): e_d[i/n_cols][256*(i%n_cols) + c] from
  * row i of rows_d, for i < n_rows (a multiple of n_cols).  Same arithmetic as

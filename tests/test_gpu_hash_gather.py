@@ -96,3 +96,53 @@ def test_empty_batch_commits_history_only():
     e, mask, _, hist, st = _fused(lay, np.zeros(0, np.int32), np.array([0, 0, 0]), tm, table, hist0, rows=False)
     assert st == 0 and e.shape[0] == 0
     assert (hist == hist0).all()
+
+
+def test_decode_step_fused_equals_oracle_and_separate_calls():
+    """engram_hash_gather_step (bf16) and its FP8 variant over 6 decode steps:
+    row ids, mask and rolled history equal the oracle's decode step; the rows
+    equal the oracle's dequantised rows and, bit for bit, engram_hash_step +
+    engram_gather_dequant / engram_gather_fp8.  Entry 3 is padding (slot -1),
+    entry 5 names slot 40 of 12 (ST_BAD_SLOT, treated as padding), and the
+    slots are a permutation, so entries do not hit their own rows."""
+    w, tm, lay_o, lay = setup("tiny")
+    total = lay_o.layers[0].total_rows
+    table = device_table(total, w.seed)
+    S, B = 12, 9
+    rng = np.random.default_rng(11)
+    hist0 = rng.integers(0, w.v, size=(S, 3)).astype(np.int64)
+    hist0[2, 1] = DEAD                      # a DEAD entry carried in the history
+    slots = rng.permutation(S)[:B].astype(np.int32)
+    slots[3] = -1
+    slots[5] = 40
+    H = hist0.copy()
+    h_fused, h_sep, h_fp8 = i32(hist0), i32(hist0), i32(hist0)
+    st_f, st_s, st_8 = status(), status(), status()
+    for step in range(6):
+        raw = rng.integers(0, w.v_raw, size=B).astype(np.int32)
+        if step == 2:
+            raw[0] = DEAD                   # an image position
+        slots_o = slots.copy()
+        slots_o[5] = -1                     # what the kernel does with the bad slot
+        rows_o, mask_o, H = OH.hash_step(raw, slots_o, H, tm, lay_o, 0)
+        rid = torch.empty((B, lay.n_cols), dtype=torch.int32, device="cuda")
+        e, mask = eg.engram_hash_gather_step(lay, 0, i32(raw), i32(slots), i32(tm), table, h_fused, row_ids=rid,
+                                             status=st_f)
+        rows_s, mask_s = eg.engram_hash_step(lay, 0, i32(raw), i32(slots), i32(tm), h_sep, status=st_s)
+        e_s = eg.engram_gather_dequant(table, total, rows_s)
+        rid8 = torch.empty((B, lay.n_cols), dtype=torch.int32, device="cuda")
+        e8, sf, mask8 = eg.engram_hash_gather_step_fp8(lay, 0, i32(raw), i32(slots), i32(tm), table, h_fp8,
+                                                       row_ids=rid8, status=st_8)
+        e8_s, sf_s = eg.engram_gather_fp8(table, total, rows_s)
+        torch.cuda.synchronize()
+        assert (rid.cpu().numpy() == rows_o).all(), step
+        assert (mask.cpu().numpy().astype(bool) == mask_o).all(), step
+        assert (h_fused.cpu().numpy() == H).all(), step
+        assert (bits(e) == bits(e_s)).all(), step
+        ref = OD.gather_dequant(rows_o, lambda r: table_rows(w.seed, r))
+        assert (OD.bf16_bits(ref) == bits(e)).all(), step
+        assert (rid8.cpu().numpy() == rows_o).all() and (mask8.cpu().numpy() == mask.cpu().numpy()).all()
+        assert (e8.cpu().numpy() == e8_s.cpu().numpy()).all() and (sf.cpu().numpy() == sf_s.cpu().numpy()).all()
+        assert (h_fp8.cpu().numpy() == H).all() and (h_sep.cpu().numpy() == H).all()
+    for st in (st_f, st_s, st_8):
+        assert int(st.item()) == eg.ST_BAD_SLOT
