@@ -735,6 +735,8 @@ def decode_bench(args, w, inp, layer, flush, dev):
            "separate_calls": {"step_ms": mean_ms(evs, 0, 3), "hash_step_ms": mean_ms(evs, 0, 1),
                               "gather_ms": mean_ms(evs, 1, 2), "project_gate_ms": mean_ms(evs, 2, 3)}}
     if args.fp8_steps <= 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = decode_cpu_baseline(w, inp, dw, 10)
         return out
 
     # The same steps with block-FP8 wkv: rows gathered as stored, block-scaled projection.
@@ -769,11 +771,52 @@ def decode_bench(args, w, inp, layer, flush, dev):
     step8 = statistics.mean(ev[0].elapsed_time(ev[3]) for ev in evs) / 1e3
     proj8 = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in evs) / 1e3
     wkv8_bytes = 6144 * (wd.hc + 1) * wd.hidden * (1 + 1 / 32)
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = decode_cpu_baseline(w, inp, dw, 10)
     out["fp8"] = {"workload": "the same steps with block-FP8 wkv (E4M3, E8M0 per 32 of k), rows gathered as stored",
                   "step_ms": step8 * 1e3, "tokens_per_s": B / step8,
                   "hash_gather_ms": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
                   "project_gate_ms": proj8 * 1e3, "wkv_gbs": wkv8_bytes / proj8 / 1e9}
     return out
+
+
+def oracle_wkv(inp):
+    """wkv as float64 for the oracle (made once per run)."""
+    from workloads import bf16_bits_to_f64
+    if "wkv_f64" not in inp:
+        inp["wkv_f64"] = bf16_bits_to_f64(inp["lw"].wkv_bits)
+    return inp["wkv_f64"]
+
+
+def decode_cpu_baseline(w, inp, dw, n_steps):
+    """The oracle on the first n_steps decode steps of the same 256 sequences.
+    The carried histories come from the oracle's prefill of each prefix's last
+    three tokens (a history is the last three compressed ids, so this equals
+    the whole prefix's)."""
+    from oracle import hashing as OH
+    from oracle import layout as OL
+    from oracle import pipeline as OP
+    from workloads import bf16_bits_to_f64, residual_bits, table_rows
+
+    tm = inp["tm"]
+    lay_o = OL.build_layout(w.v, w.base_rows, [w.layer_id], pad_id=int(tm[0]))
+    cu = dw.prefix.cu_seqlens
+    tails = [dw.prefix.raw_ids[max(cu[s], cu[s + 1] - 3):cu[s + 1]] for s in range(len(cu) - 1)]
+    tcu = np.concatenate([[0], np.cumsum([len(t) for t in tails])]).astype(np.int64)
+    _, _, hist = OH.hash_prefill(np.concatenate(tails), tcu, tm, lay_o, 0)
+    B = len(tails)
+    slots = np.arange(B)
+    W = oracle_wkv(inp)
+    h = bf16_bits_to_f64(residual_bits(B, w.hc, w.hidden, w.seed))
+    t0 = time.perf_counter()
+    for k in range(n_steps):
+        res = OP.layer_decode_step(lay_o, 0, dw.steps[k], slots, hist, tm, lambda r: table_rows(w.seed, r), W, h,
+                                   inp["lw"].q_w, inp["lw"].k_w)
+        hist, h = res.hist, res.h_out
+    dt = time.perf_counter() - t0
+    return {"value": B * n_steps / dt, "unit": "tokens/s", "steps_per_s": n_steps / dt, "cores": os.cpu_count(),
+            "kind": "oracle", "sample": f"first {n_steps} decode steps of the {B} sequences, full layer per step "
+                                        f"(numpy fp64, BLAS threads = all cores); {dt:.1f} s"}
 
 
 def fp8_weights(w, inp, dev):
@@ -1023,7 +1066,7 @@ def oracle_sample(w, inp, n_tokens):
     def table(r):
         return np.stack([cache[int(x)] for x in r])
 
-    W = bf16_bits_to_f64(inp["lw"].wkv_bits)
+    W = oracle_wkv(inp)
     h = bf16_bits_to_f64(inp["h_bits"][:n])
 
     def run():

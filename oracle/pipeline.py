@@ -45,6 +45,21 @@ def layer_forward(layout: Layout, layer: int, raw_ids, cu_seqlens, token_map, ta
     return LayerResult(rows, mask, new_hist, e, g, v, h_out)
 
 
+def layer_decode_step(layout: Layout, layer: int, raw_ids, slots, hist: np.ndarray, token_map, table_rows,
+                      wkv, h, q_w, k_w, eps: float = 1e-6, clamp: float = 1e-6, score_scale=None) -> LayerResult:
+    """One decode step of one Engram layer: entry b hashes raw_ids[b] against
+    the carried history hist[slots[b]] (slot -1 = padding, masked), then the
+    same gather, projection, gate and residual as prefill.  h: float64 [B][hc][H]."""
+    rows, mask, new_hist = hashing.hash_step(raw_ids, slots, hist, token_map, layout, layer)
+    e = dequant.gather_dequant(rows, table_rows)
+    hc, H = h.shape[1], h.shape[2]
+    kv = gate.project(e, wkv)
+    k, v = gate.split_kv(kv, H, hc)
+    g = gate.gate(h, k, q_w, k_w, mask, eps, clamp, score_scale)
+    h_out = gate.residual(h, g, v, mask)
+    return LayerResult(rows, mask, new_hist, e, g, v, h_out)
+
+
 @dataclasses.dataclass
 class ConvParams:
     """The short convolution of the original Engram layer ([P-DETAIL] §4.2)."""

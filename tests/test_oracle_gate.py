@@ -130,3 +130,35 @@ def test_tiny_pipeline_runs_and_is_consistent():
     t = 17
     direct = D.dequant_rows(table_rows(0, res.rows[t]))
     assert (res.e[t].reshape(24, 256) == direct).all()
+
+
+def test_decode_step_equals_prefill_of_prefix_plus_token():
+    """Three sequences (prefix lengths 0, 2, 9): a decode step from the
+    prefill-carried history gives the rows, mask, gate and residual of the
+    last position of prefill over prefix + token."""
+    w = WORKLOADS["tiny"]
+    tm = token_map(w.v_raw, w.v, 0)
+    lay = L.build_layout(w.v, w.base_rows, [w.layer_id], pad_id=int(tm[0]))
+    lw = layer_weights(w)
+    W = bf16_bits_to_f64(lw.wkv_bits)
+    rng = np.random.default_rng(5)
+    lens = [0, 2, 9]
+    prefixes = [rng.integers(0, w.v_raw, size=n).astype(np.int64) for n in lens]
+    new = rng.integers(0, w.v_raw, size=3).astype(np.int64)
+    h = bf16_bits_to_f64(residual_bits(3, w.hc, w.hidden, 9))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    _, _, hist = Hs.hash_prefill(np.concatenate(prefixes), cu, tm, lay, 0)
+    # history slot i holds sequence perm[i]; entry b names the slot of sequence b
+    perm = np.array([1, 2, 0])
+    slots = np.argsort(perm)
+    step = P.layer_decode_step(lay, 0, new, slots, hist[perm], tm, lambda r: table_rows(0, r), W, h, lw.q_w, lw.k_w)
+    for b in range(3):
+        seq = np.concatenate([prefixes[b], [new[b]]])
+        full = P.layer_forward(lay, 0, seq, np.array([0, len(seq)]), tm, lambda r: table_rows(0, r), W,
+                               np.repeat(h[b:b + 1], len(seq), axis=0), lw.q_w, lw.k_w)
+        assert (step.rows[b] == full.rows[-1]).all() and step.mask[b] == full.mask[-1]
+        assert (step.e[b] == full.e[-1]).all()
+        # the fp64 GEMM of one row and of a batch may round differently in the last bits
+        assert np.abs(step.gate[b] - full.gate[-1]).max() <= 1e-12
+        d = np.abs(step.h_out[b] - full.h_out[-1])
+        assert (d <= 2.0 ** -7 * np.abs(full.h_out[-1])).all() and (d == 0).mean() > 0.999
