@@ -734,6 +734,7 @@ def decode_bench(args, w, inp, layer, flush, dev):
            "kernels": "engram_hash_gather_step (hash + history roll + gather in one kernel), engram_project_gate",
            "separate_calls": {"step_ms": mean_ms(evs, 0, 3), "hash_step_ms": mean_ms(evs, 0, 1),
                               "gather_ms": mean_ms(evs, 1, 2), "project_gate_ms": mean_ms(evs, 2, 3)}}
+    out["graph"] = decode_graph_timing(layer, steps, slots, hist, h, n, flush, stream)
     if args.fp8_steps <= 0:
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = decode_cpu_baseline(w, inp, dw, 10)
@@ -778,6 +779,48 @@ def decode_bench(args, w, inp, layer, flush, dev):
                   "hash_gather_ms": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
                   "project_gate_ms": proj8 * 1e3, "wkv_gbs": wkv8_bytes / proj8 / 1e9}
     return out
+
+
+def decode_graph_timing(layer, steps, slots, hist, h, n, flush, stream):
+    """The layer's decode step captured as a CUDA graph (EngramLayer.decode_graph)
+    against eager EngramLayer.decode calls: device time per step (L2 flushed,
+    CUDA events) and wall-clock time per step of n steps issued back to back,
+    which includes the host's launch work."""
+    import torch
+
+    B = slots.numel()
+    graph = layer.decode_graph(B, hist, h)
+    graph.slots.copy_(slots)
+    n_avail = steps.shape[0]
+
+    def eager(k):
+        layer.decode(steps[k % n_avail], slots, hist, h)
+
+    def replay(k):
+        graph.raw_ids.copy_(steps[k % n_avail])
+        graph.replay()
+
+    def wall(fn):
+        for k in range(3):
+            fn(k)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k in range(n):
+            fn(k)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / n * 1e6
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for k in range(n):
+        flush()
+        evs[k][0].record(stream)
+        replay(k)
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    return {"step_ms": statistics.mean(a.elapsed_time(b) for a, b in evs),
+            "wall_us_per_step_graph": wall(replay), "wall_us_per_step_eager": wall(eager),
+            "note": "wall: steps issued back to back without L2 flush, synchronised once at the end; eager = "
+                    "EngramLayer.decode (Python binding + C entry points per step)"}
 
 
 def oracle_wkv(inp):

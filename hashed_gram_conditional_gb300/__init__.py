@@ -25,7 +25,7 @@ __all__ = [
     "engram_gather_dequant", "engram_dequant_rows", "engram_host_gather", "engram_host_gather_async",
     "engram_pack_wkv", "engram_project", "engram_gate_add", "engram_fill_synthetic_table",
     "engram_selftest_mod", "engram_project_gate", "project_gate_workspace", "partials_shape", "EngramLayer",
-    "library_path", "ST_BAD_TOKEN", "ST_BAD_ROW", "ST_BAD_SLOT", "ST_TIMEOUT", "DEAD", "ROW_BYTES",
+    "library_path", "ST_BAD_TOKEN", "ST_BAD_ROW", "ST_BAD_SLOT", "ST_TIMEOUT", "DEAD", "ROW_BYTES", "DecodeGraph",
 ]
 
 MAX_LAYERS = 8
@@ -990,6 +990,11 @@ class EngramLayer:
         pf.slot["busy"] = False
         return b
 
+    def decode_graph(self, batch: int, hist: torch.Tensor, h: torch.Tensor, status: Optional[torch.Tensor] = None,
+                     gate_out: Optional[torch.Tensor] = None, conv_state: Optional[tuple] = None) -> "DecodeGraph":
+        """The decode step for a fixed batch captured as a CUDA graph (see DecodeGraph)."""
+        return DecodeGraph(self, batch, hist, h, status, gate_out, conv_state)
+
     def decode(self, raw_ids: torch.Tensor, slots: torch.Tensor, hist: torch.Tensor, h: torch.Tensor,
                status: Optional[torch.Tensor] = None, gate_out: Optional[torch.Tensor] = None,
                conv_state: Optional[tuple] = None):
@@ -1018,6 +1023,36 @@ class EngramLayer:
         else:
             engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
             engram_gate_add(b["partials"], b["v"], h, b["mask"], self.eps, self.clamp, self.score_scale, gate_out)
+
+
+class DecodeGraph:
+    """One decode step of a layer, for a fixed batch, captured as a CUDA graph.
+
+    Write the step's raw ids (and the slots, when they change) into
+    ``raw_ids`` / ``slots`` in place, then ``replay()``: the same kernels as
+    ``EngramLayer.decode`` run on the current stream without any host-side
+    launch work.  ``hist``, ``h``, ``status``, ``gate_out`` and the
+    short-convolution state are the tensors given here; the step updates
+    them in place exactly as ``decode`` does.  The graph keeps the layer's
+    work buffers for this batch size alive for its own lifetime.
+    """
+
+    def __init__(self, layer: "EngramLayer", batch: int, hist: torch.Tensor, h: torch.Tensor,
+                 status: Optional[torch.Tensor] = None, gate_out: Optional[torch.Tensor] = None,
+                 conv_state: Optional[tuple] = None):
+        dev = h.device
+        self.raw_ids = torch.zeros(batch, dtype=torch.int32, device=dev)
+        self.slots = torch.arange(batch, dtype=torch.int32, device=dev)
+        self.hist, self.h, self.status, self.gate_out, self.conv_state = hist, h, status, gate_out, conv_state
+        self.buffers = layer._buffers(batch, dev)
+        _load()
+        self.graph = torch.cuda.CUDAGraph()
+        # capture records the launches only: hist and h are not touched here
+        with torch.cuda.graph(self.graph):
+            layer.decode(self.raw_ids, self.slots, hist, h, status, gate_out, conv_state)
+
+    def replay(self):
+        self.graph.replay()
 
 
 class ShortConv:

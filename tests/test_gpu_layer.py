@@ -124,3 +124,44 @@ def test_layer_decode_steps():
     torch.cuda.synchronize()
     assert (hist_d.cpu().numpy() == H).all()
     assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("conv", [False, True])
+def test_decode_graph_replays_equal_eager_steps(conv):
+    """A captured decode step replayed for 6 steps (new raw ids written in
+    place each time, one padding entry) gives bit for bit the residual, gates,
+    history (and short-convolution state) of eager EngramLayer.decode calls."""
+    w, tm, lay_o, lay, lw, layer = _make_layer("tiny")
+    if conv:
+        from workloads import conv_weights
+        cw, gamma = conv_weights(4, w.hc, w.hidden, w.seed)
+        layer = eg.EngramLayer(lay, 0, layer.table, layer.token_map, layer.wkv_packed, layer.q_w, layer.k_w,
+                               conv=eg.ShortConv(f32(cw), f32(gamma), 3))
+    B, S = 37, 40
+    rng = np.random.default_rng(3)
+    hist0 = i32(rng.integers(0, w.v, size=(S, 3)))
+    h0 = bf16(normal_bf16_bits((B, w.hc, w.hidden), 1.0, 5, 1))
+    slots = rng.permutation(S)[:B].astype(np.int32)
+    slots[7] = -1
+    states = []
+    for _ in range(2):
+        cs = layer.new_conv_state(S, DEV) if conv else None
+        states.append((hist0.clone(), h0.clone(), torch.empty((B, w.hc), dtype=torch.float32, device=DEV),
+                       status(), cs))
+    hist_e, h_e, g_e, st_e, cs_e = states[0]
+    hist_g, h_g, g_g, st_g, cs_g = states[1]
+    graph = layer.decode_graph(B, hist_g, h_g, st_g, g_g, cs_g)
+    graph.slots.copy_(i32(slots))
+    for step in range(6):
+        raw = rng.integers(0, w.v_raw, size=B).astype(np.int32)
+        layer.decode(i32(raw), i32(slots), hist_e, h_e, st_e, g_e, cs_e)
+        graph.raw_ids.copy_(i32(raw))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert (bits(h_g) == bits(h_e)).all(), step
+        assert (g_g.cpu().numpy() == g_e.cpu().numpy()).all(), step
+        assert (hist_g.cpu().numpy() == hist_e.cpu().numpy()).all(), step
+        if conv:
+            assert (cs_g[0].cpu().numpy() == cs_e[0].cpu().numpy()).all(), step
+            assert (cs_g[1].cpu().numpy() == cs_e[1].cpu().numpy()).all(), step
+    assert int(st_e.item()) == 0 and int(st_g.item()) == 0
