@@ -112,6 +112,7 @@ _SIGS = {
     "engram_gather_fp8": [_P, _I64, _I64, _P, _I64, _I32, _P, _P, _P, _P],
     "engram_hash_gather_fp8": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _I64, _P, _P,
                                _P, _P, _P, _P],
+    "engram_selftest_wait": [_I32, _P, _P, _P],
     "engram_hash_gather_step": [ctypes.POINTER(_Layout), _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P, _I64, _P, _P,
                                 _P, _P, _P],
     "engram_hash_gather_step_fp8": [ctypes.POINTER(_Layout), _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P, _I64, _P,
@@ -847,6 +848,20 @@ def engram_selftest_mod(layout: Layout, layer: int, x: torch.Tensor) -> torch.Te
 
 
 # --------------------------------------------------------------------------- layer
+
+
+def engram_selftest_wait(which: int, status: torch.Tensor, scratch: Optional[torch.Tensor] = None):
+    """Diagnostic: a bounded wait that nothing satisfies (which 0: an mbarrier
+    phase, 1: a global counter) runs out after about a second and sets
+    ST_TIMEOUT in ``status``; asynchronous on the current stream."""
+    L = _load()
+    dev = status.device
+    _need(status, "status", torch.int32, dev, 1)
+    if scratch is None:
+        scratch = torch.empty(2, dtype=torch.int32, device=dev)
+    _need(scratch, "scratch", torch.int32, dev, 2)
+    _check(L.engram_selftest_wait(which, _ptr(scratch), _ptr(status), _stream(dev)), "engram_selftest_wait")
+    return scratch
 
 
 class EngramLayer:

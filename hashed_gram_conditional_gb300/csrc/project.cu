@@ -267,6 +267,24 @@ __device__ bool wait_published(const int32_t* cnt, int target, const volatile in
   }
 }
 
+// Diagnostic: a wait that nothing will satisfy gives up after the budget and
+// records ENGRAM_ST_TIMEOUT (engram_selftest_wait).
+__global__ void selftest_wait_kernel(int which, int32_t* scratch, int32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ int cta_abort;
+  if (threadIdx.x != 0) return;
+  bool ok;
+  if (which == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    ok = mbar_wait_bounded(smem_u32(&bar), 0, nullptr);  // phase 0 never completes
+  } else {
+    cta_abort = 0;
+    ok = wait_published(scratch, 1, scratch + 1, &cta_abort);  // the counter stays 0
+  }
+  if (!ok && status != nullptr) atomicOr(status, static_cast<int>(ENGRAM_ST_TIMEOUT));
+}
+
 __device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
 // Two bf16 lanes of h and v: bf16_rne(h + g * v) in fp32 per lane.
@@ -1890,4 +1908,16 @@ extern "C" int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_
   cudaError_t err = cudaMemsetAsync(a.cnt, 0, ws.counter_words * sizeof(int32_t), st);
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaMemsetAsync(counters): %s", cudaGetErrorString(err));
   return launch8(pair, true, tmA, tmB, a, sfa_d, sfb_d, st);
+}
+
+extern "C" int engram_selftest_wait(int32_t which, int32_t* scratch_d, int32_t* status_d, void* stream) {
+  if (which != 0 && which != 1) return fail(ENGRAM_E_INVALID, "which must be 0 or 1");
+  if (!scratch_d || !status_d) return fail(ENGRAM_E_INVALID, "null device pointer");
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t err = cudaMemsetAsync(scratch_d, 0, 2 * sizeof(int32_t), st);
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaMemsetAsync(scratch): %s", cudaGetErrorString(err));
+  selftest_wait_kernel<<<1, 32, 0, st>>>(which, scratch_d, status_d);
+  return check_launch("selftest_wait_kernel");
 }

@@ -568,6 +568,18 @@ int engram_fill_synthetic_table(uint8_t* table_d, int64_t n_rows, uint64_t seed,
 int engram_selftest_mod(const engram_layout* layout, int32_t layer, const uint64_t* x_d, int64_t n,
                         int64_t* out_d, void* stream);
 
+/* Diagnostic of the bounded on-chip waits: one thread waits for something
+ * that never happens, with the budget every kernel's waits use (2^31 SM
+ * cycles, about a second), and the kernel then sets ENGRAM_ST_TIMEOUT in
+ * status_d and returns -- no trap, no hang, the context stays usable.
+ *   which      0: an mbarrier phase that no arrival completes (the TMA /
+ *              tensor-core pipelines' waits); 1: a global counter that no
+ *              CTA increments (the fused projection's wait for its block's
+ *              gates)
+ *   scratch_d  int32 [2] device scratch, zeroed by the call before the launch
+ *   status_d   int32 status word (not cleared) */
+int engram_selftest_wait(int32_t which, int32_t* scratch_d, int32_t* status_d, void* stream);
+
 /* Thread-local message of the last failure (empty string if none). */
 const char* engram_last_error(void);
 /* Name of an ENGRAM_* return code. */
