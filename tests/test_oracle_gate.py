@@ -162,3 +162,19 @@ def test_decode_step_equals_prefill_of_prefix_plus_token():
         assert np.abs(step.gate[b] - full.gate[-1]).max() <= 1e-12
         d = np.abs(step.h_out[b] - full.h_out[-1])
         assert (d <= 2.0 ** -7 * np.abs(full.h_out[-1])).all() and (d == 0).mean() > 0.999
+
+
+def test_residual_rounds_v_before_the_product_worked_example():
+    """A hand-worked case where rounding v to bf16 first decides the result
+    (the residual uses bf16(v), and h + g bf16(v) is rounded once):
+    h = 1, g = 1/2, v = 3 + 2^-6 + 2^-20.  bf16(v) = 3 + 2^-6, so the sum is
+    2.5 + 2^-7, exactly half a bf16 step (2^-6) above 2.5: a tie, which goes
+    to the even significand, 2.5.  With v unrounded the sum would sit above
+    the tie and round up to 2.5 + 2^-6."""
+    H, hc = 256, 1
+    h = np.ones((1, hc, H))
+    g = np.full((1, hc), 0.5)
+    v = np.full((1, H), 3 + 2.0 ** -6 + 2.0 ** -20)
+    out = G.residual(h, g, v, np.zeros(1, bool))
+    assert (out == 2.5).all()
+    assert (D.bf16_round(np.float64(3 + 2.0 ** -6 + 2.0 ** -20)) == 3 + 2.0 ** -6)
