@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "EngramError", "Layout", "build_layout", "engram_hash", "engram_hash_all_layers", "engram_hash_step",
     "engram_hash_gather", "engram_hash_gather_step", "engram_hash_gather_fp8", "engram_hash_gather_step_fp8",
-    "engram_gather_fp8",
+    "engram_gather_fp8", "engram_gather_rows_bf16", "engram_hash_gather_rows_bf16", "engram_fill_synthetic_rows_bf16",
     "engram_gather_dequant", "engram_dequant_rows", "engram_host_gather", "engram_host_gather_async",
     "engram_pack_wkv", "engram_project", "engram_gate_add", "engram_fill_synthetic_table",
     "engram_selftest_mod", "engram_project_gate", "project_gate_workspace", "partials_shape", "EngramLayer",
@@ -113,6 +113,10 @@ _SIGS = {
     "engram_hash_gather_fp8": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _I64, _P, _P,
                                _P, _P, _P, _P],
     "engram_selftest_wait": [_I32, _P, _P, _P],
+    "engram_gather_rows_bf16": [_P, _I64, _I32, _P, _I64, _I32, _P, _P, _P],
+    "engram_hash_gather_rows_bf16": [ctypes.POINTER(_Layout), _I32, _P, _I64, _P, _I32, _P, _I64, _P, _P, _I32, _P,
+                                     _P, _P, _P, _P],
+    "engram_fill_synthetic_rows_bf16": [_P, _I64, _I32, ctypes.c_uint64, _P],
     "engram_hash_gather_step": [ctypes.POINTER(_Layout), _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P, _I64, _P, _P,
                                 _P, _P, _P],
     "engram_hash_gather_step_fp8": [ctypes.POINTER(_Layout), _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P, _I64, _P,
@@ -818,6 +822,72 @@ def engram_project_gate(e: torch.Tensor, wkv_packed: torch.Tensor, h: torch.Tens
     return gate_out
 
 
+def engram_gather_rows_bf16(table: torch.Tensor, row_ids: torch.Tensor, e: Optional[torch.Tensor] = None,
+                            status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Gather from a table of plain bf16 rows (bf16 [total_rows][row_dim]):
+    returns e bf16 [T][n_cols*row_dim], the rows concatenated as stored."""
+    L = _load()
+    dev = row_ids.device
+    _need(table, "table", torch.bfloat16, dev)
+    if table.dim() != 2:
+        raise ValueError("a bf16-row table is [total_rows][row_dim]")
+    _need(row_ids, "row_ids", torch.int32, dev)
+    T, C = row_ids.shape
+    R = table.shape[1]
+    if e is None:
+        e = torch.empty((T, C * R), dtype=torch.bfloat16, device=dev)
+    _need(e, "e", torch.bfloat16, dev, T * C * R)
+    _check(L.engram_gather_rows_bf16(_ptr(table), table.shape[0], R, _ptr(row_ids), T, C, _ptr(e), _ptr(status),
+                                     _stream(dev)), "engram_gather_rows_bf16")
+    return e
+
+
+def engram_hash_gather_rows_bf16(layout: Layout, layer: int, raw_ids: torch.Tensor, cu_seqlens: torch.Tensor,
+                                 token_map: torch.Tensor, table: torch.Tensor, hist: Optional[torch.Tensor] = None,
+                                 e: Optional[torch.Tensor] = None, mask: Optional[torch.Tensor] = None,
+                                 row_ids: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None):
+    """Hash + gather from a bf16-row table in one kernel, then the history commit;
+    returns (e bf16 [T][n_cols*row_dim], mask uint8 [T])."""
+    L = _load()
+    dev = raw_ids.device
+    T = raw_ids.numel()
+    C = layout.n_cols
+    _need(raw_ids, "raw_ids", torch.int32)
+    _need(cu_seqlens, "cu_seqlens", torch.int64, dev)
+    _need(token_map, "token_map", torch.int32, dev)
+    _need(table, "table", torch.bfloat16, dev)
+    if table.dim() != 2 or table.shape[0] < layout.total_rows(layer):
+        raise ValueError("the bf16-row table must be [>= total_rows][row_dim]")
+    R = table.shape[1]
+    n_seqs = cu_seqlens.numel() - 1
+    if hist is not None:
+        _need(hist, "hist", torch.int32, dev, n_seqs * (layout.max_ngram - 1))
+    if e is None:
+        e = torch.empty((T, C * R), dtype=torch.bfloat16, device=dev)
+    if mask is None:
+        mask = torch.empty(T, dtype=torch.uint8, device=dev)
+    _need(e, "e", torch.bfloat16, dev, T * C * R)
+    _need(mask, "mask", torch.uint8, dev, T)
+    if row_ids is not None:
+        _need(row_ids, "row_ids", torch.int32, dev, T * C)
+    _check(L.engram_hash_gather_rows_bf16(layout.ref, layer, _ptr(raw_ids), T, _ptr(cu_seqlens), n_seqs,
+                                          _ptr(token_map), token_map.numel(), _ptr(hist), _ptr(table), R, _ptr(e),
+                                          _ptr(mask), _ptr(row_ids), _ptr(status), _stream(dev)),
+           "engram_hash_gather_rows_bf16")
+    return e, mask
+
+
+def engram_fill_synthetic_rows_bf16(table: torch.Tensor, seed: int) -> torch.Tensor:
+    """Fill a device bf16-row table [n_rows][row_dim] with the seeded synthetic rows."""
+    L = _load()
+    _need(table, "table", torch.bfloat16)
+    if table.dim() != 2:
+        raise ValueError("a bf16-row table is [n_rows][row_dim]")
+    _check(L.engram_fill_synthetic_rows_bf16(_ptr(table), table.shape[0], table.shape[1], seed,
+                                             _stream(table.device)), "engram_fill_synthetic_rows_bf16")
+    return table
+
+
 def engram_fill_synthetic_table(table: torch.Tensor, n_rows: int, seed: int,
                                 device: Optional[torch.device] = None) -> torch.Tensor:
     """Fill a device table, or a pinned host table (written by the kernel through
@@ -890,6 +960,10 @@ class EngramLayer:
         self.eps, self.clamp = eps, clamp
         self.score_scale = self.hidden ** -0.5 if score_scale is None else score_scale
         self.total_rows = layout.total_rows(layer)
+        # a bf16 [rows][row_dim] table holds plain rows (generic shapes); a uint8
+        # table holds the 264-byte E4M3 + E8M0 rows
+        self.row_dim = table.shape[1] if table.dtype == torch.bfloat16 else None
+        self.e_dim = layout.n_cols * (self.row_dim if self.row_dim is not None else HEAD_DIM)
         self.fused = fused
         self._ws = {}
         self._pf = {}          # T -> [two prefetch slots]
@@ -901,7 +975,7 @@ class EngramLayer:
             self._ws = {key: dict(
                 rows=torch.empty((T, self.layout.n_cols), dtype=torch.int32, device=device),
                 mask=torch.empty(T, dtype=torch.uint8, device=device),
-                e=torch.empty((T, self.layout.n_cols * HEAD_DIM), dtype=torch.bfloat16, device=device),
+                e=torch.empty((T, self.e_dim), dtype=torch.bfloat16, device=device),
                 partials=torch.empty(partials_shape(T, self.hidden, self.hc), dtype=torch.float32, device=device),
                 v=torch.empty((T, self.hidden), dtype=torch.bfloat16, device=device),
                 work=project_gate_workspace(T, self.hidden, self.hc, device),
@@ -924,8 +998,12 @@ class EngramLayer:
         layer with the short convolution (None: zeros before every sequence)."""
         T = raw_ids.numel()
         b = self._buffers(T, raw_ids.device)
-        engram_hash_gather(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, self.table, hist, b["e"],
-                           b["mask"], b["rows"], status)
+        if self.row_dim is not None:
+            engram_hash_gather_rows_bf16(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, self.table,
+                                         hist, b["e"], b["mask"], b["rows"], status)
+        else:
+            engram_hash_gather(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, self.table, hist,
+                               b["e"], b["mask"], b["rows"], status)
         self._gate(b, h, status, gate_out, cu_seqlens=cu_seqlens, conv_state=conv_state)
         return b
 
@@ -961,7 +1039,10 @@ class EngramLayer:
         pinned staging buffer, one DMA moves it to the device and the rows are
         dequantised there.  With a device table the gather follows the hash on
         the current stream.  At most two batches may be waiting at a time.
+        (E4M3 + E8M0 tables only.)
         """
+        if self.row_dim is not None:
+            raise ValueError("prefetch handles the 264-byte E4M3 + E8M0 row tables only")
         dev = raw_ids.device
         T = raw_ids.numel()
         slot = self._prefetch_slot(T, dev)
@@ -1015,8 +1096,13 @@ class EngramLayer:
                conv_state: Optional[tuple] = None):
         B = raw_ids.numel()
         b = self._buffers(B, raw_ids.device)
-        engram_hash_gather_step(self.layout, self.layer, raw_ids, slots, self.token_map, self.table, hist, b["e"],
-                                b["mask"], b["rows"], status)
+        if self.row_dim is not None:
+            engram_hash_step(self.layout, self.layer, raw_ids, slots, self.token_map, hist, b["rows"], b["mask"],
+                             status)
+            engram_gather_rows_bf16(self.table, b["rows"], b["e"], status)
+        else:
+            engram_hash_gather_step(self.layout, self.layer, raw_ids, slots, self.token_map, self.table, hist,
+                                    b["e"], b["mask"], b["rows"], status)
         self._gate(b, h, status, gate_out, slots=slots, conv_state=conv_state)
         return b
 

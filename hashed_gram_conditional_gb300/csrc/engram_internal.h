@@ -109,6 +109,16 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// SplitMix64 output number n+1 of a stream starting at `seed` (Steele, Lea &
+// Flood 2014): finaliser applied to seed + (n+1) * golden gamma.  Used only by
+// the synthetic-table generators (test and benchmark inputs).
+__device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t n) {
+  uint64_t z = seed + (n + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
 #endif  // __CUDACC__
 
 }  // namespace engram

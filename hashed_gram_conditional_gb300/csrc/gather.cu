@@ -394,15 +394,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArg
   }
 }
 
-// SplitMix64 output number n+1 of a stream starting at `seed` (Steele, Lea &
-// Flood 2014): finaliser applied to seed + (n+1) * golden gamma.
-__device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t n) {
-  uint64_t z = seed + (n + 1) * 0x9E3779B97F4A7C15ull;
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-  return z ^ (z >> 31);
-}
-
 __global__ void fill_table_kernel(uint8_t* table, int64_t n_words, uint64_t seed) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t wi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; wi < n_words;

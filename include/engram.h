@@ -288,6 +288,30 @@ int engram_hash_gather_step_fp8(const engram_layout* layout, int32_t layer, cons
                                 int64_t table_bytes, uint8_t* e8_d, uint32_t* sf_d, uint8_t* mask_d,
                                 int32_t* row_ids_d, int32_t* status_d, void* stream);
 
+/* Stage 4 for a table of plain bf16 rows of any width (the generic-shape row
+ * format: the Engram paper's 27B model reads 16 rows of 80 elements per
+ * position into hidden 2560, [P-DETAIL] §5 after its worked example; the page
+ * sizes that table at 2 bytes per element, §8.4).  Rows are copied as stored:
+ *   e_d[t][j*row_dim + c] = table_d[row_ids_d[t][j]][c]
+ *   table_d    bf16 [total_rows][row_dim], 16-byte aligned; row_dim a multiple
+ *              of 8 in [8, 4096]
+ *   row_ids_d  int32 [n_tokens][n_cols]
+ *   e_d        bf16 [n_tokens][n_cols*row_dim] out, 16-byte aligned
+ * A row id outside [0, total_rows) sets ENGRAM_ST_BAD_ROW and its row_dim
+ * outputs are +0.  The projection takes e as is (K = n_cols*row_dim, a
+ * multiple of 64). */
+int engram_gather_rows_bf16(const uint16_t* table_d, int64_t total_rows, int32_t row_dim, const int32_t* row_ids_d,
+                            int64_t n_tokens, int32_t n_cols, uint16_t* e_d, int32_t* status_d, void* stream);
+
+/* Stages 1-4 fused for a bf16-row table: the hash of engram_hash_gather with
+ * the copy of engram_gather_rows_bf16 (total_rows from the layout), then the
+ * history commit.  Arguments and status bits as in those two calls. */
+int engram_hash_gather_rows_bf16(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
+                                 int64_t n_tokens, const int64_t* cu_seqlens_d, int32_t n_seqs,
+                                 const int32_t* token_map_d, int64_t vocab_raw, int32_t* hist_d,
+                                 const uint16_t* table_d, int32_t row_dim, uint16_t* e_d, uint8_t* mask_d,
+                                 int32_t* row_ids_d, int32_t* status_d, void* stream);
+
 /* Dequantise rows that already sit contiguously in device memory (e.g. after
  * a host-side gather and one DMA): e_d[i/n_cols][256*(i%n_cols) + c] from
  * row i of rows_d, for i < n_rows (a multiple of n_cols).  Same arithmetic as
@@ -561,6 +585,15 @@ int engram_project_gate_add_noalloc(const uint16_t* e_d, int64_t n_tokens, int64
  *   table_d  uint8 [n_rows][264], 8-byte aligned; device memory or a pinned
  *            (mapped) host buffer, which the kernel writes over NVLink-C2C */
 int engram_fill_synthetic_table(uint8_t* table_d, int64_t n_rows, uint64_t seed, void* stream);
+
+/* Fill a bf16-row table with synthetic rows: element c of row r is 16-bit
+ * piece (c mod 4) of SplitMix64 output number r*(row_dim/4) + c/4 + 1 of the
+ * stream at `seed`, with its 8 exponent bits replaced by 120 + (those bits
+ * mod 11), so every value is finite with magnitude in [2^-7, 2^4).  Test and
+ * benchmark input generation, not part of the method.
+ *   table_d  bf16 [n_rows][row_dim], 8-byte aligned; row_dim a multiple of 4 */
+int engram_fill_synthetic_rows_bf16(uint16_t* table_d, int64_t n_rows, int32_t row_dim, uint64_t seed,
+                                    void* stream);
 
 /* Diagnostic of the on-device modulo: out_d[i][j] = x_d[i] mod p_j + offset_j
  * for the layer's n_cols columns, computed by the same device routine as

@@ -113,3 +113,16 @@ def gather_dequant(row_ids: np.ndarray, table_rows) -> np.ndarray:
     T, C = rid.shape
     vals = dequant_rows(table_rows(rid.reshape(-1)))
     return vals.reshape(T, C * HEAD_DIM)
+
+
+def gather_rows(row_ids: np.ndarray, table_rows) -> np.ndarray:
+    """e[t] = concat_j row(row_ids[t][j]) for a table of plain bf16 rows,
+    float64 [T][n_cols * row_dim] ([P-DETAIL] §5: the per-head rows are
+    concatenated in column order into the memory vector).
+
+    ``table_rows(ids)`` returns the rows as float64 bf16 values [n][row_dim].
+    """
+    rid = np.asarray(row_ids, dtype=np.int64)
+    T, C = rid.shape
+    vals = np.asarray(table_rows(rid.reshape(-1)), dtype=np.float64)
+    return vals.reshape(T, C * vals.shape[1])

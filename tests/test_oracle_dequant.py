@@ -102,3 +102,31 @@ def test_dequant_mx_weights_blocks_along_k():
     w = dequant_mx_weights(codes, scales)
     assert w[0, 0] == 1.0 and w[31, 0] == 1.0 and w[32, 0] == 2.0 ** -7 and w[63, 0] == 2.0 ** -7
     assert w[31, 1] == 448.0 * 8 and w[32, 1] == 0.25 and w[0, 1] == 8.0
+
+
+def test_bf16_row_generator_layout_and_range():
+    """The synthetic bf16-row table: element c of row r comes from 16-bit piece
+    c mod 4 (little-endian) of SplitMix64 output r*(row_dim/4) + c/4, with the
+    exponent field forced into 120..130; every value is finite."""
+    from workloads import splitmix64_at, table_rows_bf16
+    row_dim = 80
+    rows = np.array([0, 1, 12345, 2 ** 30 + 7])
+    got = table_rows_bf16(7, rows, row_dim)
+    assert got.shape == (4, row_dim) and got.dtype == np.uint16
+    for i, r in enumerate(rows):
+        for c in (0, 1, 3, 4, 77, 79):
+            word = int(splitmix64_at(7, np.array([r * (row_dim // 4) + c // 4]))[0])
+            b = (word >> (16 * (c % 4))) & 0xFFFF
+            want = (b & 0x807F) | ((120 + ((b >> 7) & 0xFF) % 11) << 7)
+            assert int(got[i, c]) == want
+    ex = (got >> 7) & 0xFF
+    assert ex.min() >= 120 and ex.max() <= 130
+    from workloads import bf16_bits_to_f64
+    vals = np.abs(bf16_bits_to_f64(table_rows_bf16(3, np.arange(500), row_dim)))
+    assert np.isfinite(vals).all() and vals.min() >= 2.0 ** -7 and vals.max() < 16.0
+
+
+def test_gather_rows_concatenates_in_column_order():
+    rows = {5: np.full(8, 1.0), 9: np.full(8, 2.0), 11: np.full(8, 3.0)}
+    e = D.gather_rows(np.array([[9, 5, 11]]), lambda ids: np.stack([rows[int(i)] for i in ids]))
+    assert (e[0] == np.repeat([2.0, 1.0, 3.0], 8)).all()

@@ -281,9 +281,27 @@ class LayerWeights:
     k_w: np.ndarray        # float32 [H][hc]
 
 
-def layer_weights(w: Workload, n_cols: int = 24, seed: Optional[int] = None) -> LayerWeights:
+def table_rows_bf16(seed: int, rows: np.ndarray, row_dim: int) -> np.ndarray:
+    """bf16 bit patterns of the requested rows of a synthetic bf16-row table,
+    uint16 [len(rows)][row_dim].
+
+    Element c of row r is 16-bit piece (c mod 4) (little-endian) of
+    splitmix64_at(seed, r*(row_dim/4) + c/4), with its 8 exponent bits
+    (bits 7..14) replaced by 120 + (those bits mod 11): finite values of
+    magnitude in [2^-7, 2^4).
+    """
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1)
+    per = row_dim // 4
+    ctr = rows[:, None] * per + np.arange(per, dtype=np.int64)[None, :]
+    b = splitmix64_at(seed, ctr).astype("<u8").view("<u2").reshape(len(rows), row_dim).astype(np.uint32)
+    ex = np.uint32(120) + ((b >> np.uint32(7)) & np.uint32(0xFF)) % np.uint32(11)
+    return ((b & np.uint32(0x807F)) | (ex << np.uint32(7))).astype(np.uint16)
+
+
+def layer_weights(w: Workload, n_cols: int = 24, seed: Optional[int] = None,
+                  row_dim: int = HEAD_DIM) -> LayerWeights:
     seed = w.seed if seed is None else seed
-    k = n_cols * HEAD_DIM
+    k = n_cols * row_dim
     n = (w.hc + 1) * w.hidden
     wkv = normal_bf16_bits((k, n), 0.02, seed, 20)
     q_w = uniform_f32((w.hidden, w.hc), 0.5, 1.5, seed, 21)
