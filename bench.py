@@ -78,6 +78,8 @@ def parse():
     p.add_argument("--decode-steps", type=int, default=200, help="steps of the decode phase")
     p.add_argument("--conv-steps", type=int, default=30, help="steps of the short-convolution layer phase")
     p.add_argument("--fp8-steps", type=int, default=200, help="steps of the block-FP8 projection layer phase")
+    p.add_argument("--generic-steps", type=int, default=30,
+                   help="steps of the Engram-27B-shaped layer phase (bf16 rows of 80, hidden 2560)")
     p.add_argument("--fullscale-passes", type=int, default=2,
                    help="timed passes over the 131,072-token full-scale sequence (101 GB table; 0 skips it)")
     p.add_argument("--host-steps", type=int, default=20,
@@ -327,6 +329,7 @@ def run_ours(args, rank, world, local):
     dec = decode_bench(args, w, inp, layer, flush, dev) if side and args.decode_steps > 0 else None
     conv = conv_bench(args, w, inp, layer, flush, dev) if side and args.conv_steps > 0 else None
     fp8 = fp8_bench(args, w, inp, layer, flush, dev) if side and args.fp8_steps > 0 else None
+    gen = generic_bench(args, w, flush, dev) if side and args.generic_steps > 0 else None
     host = host_table_bench(args, w, inp, layer, flush, dev, statistics.mean(step_ms)) \
         if side and args.host_steps > 0 else None
     full = fullscale_bench(args, inp, layer, dev) if side and args.fullscale_passes > 0 else None
@@ -346,13 +349,15 @@ def run_ours(args, rank, world, local):
         hgg["hash_gather_frac_hbm"] = hgg["hash_gather_gbs"] / peaks["hbm_gbs"]
     if full is not None and "hash_gather_gbs" in full:
         full["hash_gather_frac_hbm"] = full["hash_gather_gbs"] / peaks["hbm_gbs"]
+    if gen is not None:
+        gen["hash_gather_frac_hbm"] = gen["hash_gather_gbs"] / peaks["hbm_gbs"]
     if dec is not None:
         dec["wkv_frac_hbm"] = dec["wkv_gbs"] / peaks["hbm_gbs"]
     if fp8 is not None:
         # fp8 dense tensor peak: the measured bf16 figure times the nominal fp8 / bf16 ratio (4.5 / 2.25)
         fp8_sust = fp8["timed_s"] >= 2.0
         pk = 2.0 * (peaks["bf16_tflops_sustained"] if fp8_sust else peaks["bf16_tflops"])
-        fp8["roofline"] = {"bound": "tensor", "kernel": "project8_kernel<fused> (tcgen05 kind::mxf8f6f4)",
+        fp8["roofline"] = {"bound": "tensor", "kernel": "project8_kernel<unfused> (tcgen05 kind::mxf8f6f4)",
                            "achieved": fp8["project_tflops"], "peak": pk, "unit": "TFLOP/s",
                            "frac": fp8["project_tflops"] / pk,
                            "peak_source": f"{peak_src} bf16_tflops{'_sustained' if fp8_sust else ''} x 2 "
@@ -405,6 +410,7 @@ def run_ours(args, rank, world, local):
         "decode_step": dec,
         "short_conv_layer": conv,
         "fp8_layer": fp8,
+        "generic_27b_shape": gen,
         "fullscale": full,
         "host_table": host,
         "gpu_launches": args.steps * 3,
@@ -893,7 +899,6 @@ def fp8_bench(args, w, inp, layer, flush, dev):
     e8 = torch.empty((T, K), dtype=torch.uint8, device=dev)
     sfa = torch.empty((2 * 24, T), dtype=torch.int32, device=dev)
     mask = torch.empty(T, dtype=torch.uint8, device=dev)
-    work = eg.project_gate_workspace(T, w.hidden, w.hc, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -904,16 +909,20 @@ def fp8_bench(args, w, inp, layer, flush, dev):
                                   status)
         if ev is not None:
             ev[1].record(stream)
-        eg.engram_project_gate_fp8(e8, sfa, w8p, sfb, h, layer.q_w, layer.k_w, mask, layer.eps, layer.clamp,
-                                   layer.score_scale, None, work, status)
+        # the two kernels engram_project_gate_fp8 runs, with an event between them
+        eg.engram_project_fp8(e8, sfa, w8p, sfb, h, layer.q_w, layer.k_w, bufs["partials"], bufs["v"], status)
+        if ev is not None:
+            ev[3].record(stream)
+        eg.engram_gate_add(bufs["partials"], bufs["v"], h, mask, layer.eps, layer.clamp, layer.score_scale)
         if ev is not None:
             ev[2].record(stream)
 
+    bufs = layer._buffers(T, dev)
     for _ in range(5):
         flush()
         run()
     n = args.fp8_steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for k in range(n):
@@ -922,14 +931,90 @@ def fp8_bench(args, w, inp, layer, flush, dev):
     torch.cuda.synchronize()
     timed = time.perf_counter() - t0
     step = statistics.mean(ev[0].elapsed_time(ev[2]) for ev in evs) / 1e3
-    proj = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs) / 1e3
+    pg = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs) / 1e3
+    proj = statistics.mean(ev[1].elapsed_time(ev[3]) for ev in evs) / 1e3
     hg = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs) / 1e3
     flops = 2.0 * T * K * N
     return {"workload": f"{w.name} batch ({T} tokens), block-FP8 wkv (E4M3, E8M0 per 32 of k), L2 flushed",
             "steps": n, "step_ms": step * 1e3, "tokens_per_s": T / step, "hash_gather_ms": hg * 1e3,
-            "project_gate_ms": proj * 1e3, "project_tflops": flops / proj / 1e12, "timed_s": timed,
+            "project_gate_ms": pg * 1e3, "project_ms": proj * 1e3, "gate_ms": (pg - proj) * 1e3,
+            "project_tflops": flops / proj / 1e12, "timed_s": timed,
+            "kernels": "gather_ldgsts_kernel<HashedRows, Fp8Out>, project8_kernel<unfused>, gate_add_kernel "
+                       "(what engram_hash_gather_fp8 + engram_project_gate_fp8 run)",
             "hash_gather_bytes_per_token": 4 + 24 * 264 + 24 * 256 + 24 * 8,
             "device_status": int(status.item())}
+
+
+def generic_bench(args, w, flush, dev):
+    """The Engram-27B shape of the Engram paper on the same token batch shape:
+    2/3-grams x 8 heads = 16 columns of plain bf16 rows of 80 elements
+    (K = 1280), hidden 2560, 4 streams, table from base 2,000,000 (~32 M rows,
+    5.1 GB), filled on the device."""
+    import torch
+    import hashed_gram_conditional_gb300 as eg
+    from workloads import Workload, layer_weights, prefill_batch, residual_bits, token_map
+
+    R = 80
+    wg = Workload("generic27b", w.v_raw, w.v, w.base_rows, 15, w.n_seqs, w.seq_len, 2560, 4, w.dead_frac,
+                  seed=w.seed)
+    tm = token_map(wg.v_raw, wg.v, wg.seed)
+    lay = eg.build_layout(wg.v, wg.base_rows, [2, 15], max_ngram=3, n_heads=8, pad_id=int(tm[0]),
+                          expected_vocab=wg.v)
+    total = lay.total_rows(1)
+    table = eg.engram_fill_synthetic_rows_bf16(torch.empty((total, R), dtype=torch.bfloat16, device=dev), wg.seed)
+    lw = layer_weights(wg, n_cols=lay.n_cols, row_dim=R)
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    layer = eg.EngramLayer(lay, 1, table, torch.from_numpy(tm).to(dev), eg.engram_pack_wkv(bf16(lw.wkv_bits)),
+                           torch.from_numpy(lw.q_w).to(dev), torch.from_numpy(lw.k_w).to(dev))
+    b = prefill_batch(wg, seed=wg.seed)
+    T = len(b.raw_ids)
+    raw = torch.from_numpy(b.raw_ids).to(dev)
+    cu = torch.from_numpy(b.cu_seqlens).to(dev)
+    h = bf16(residual_bits(T, wg.hc, wg.hidden, wg.seed))
+    hist = torch.full((wg.n_seqs, 2), lay.pad_id, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    bufs = layer._buffers(T, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def run(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        eg.engram_hash_gather_rows_bf16(lay, 1, raw, cu, layer.token_map, table, hist, bufs["e"], bufs["mask"], None,
+                                        status)
+        if ev is not None:
+            ev[1].record(stream)
+        eg.engram_project_gate(bufs["e"], layer.wkv_packed, h, layer.q_w, layer.k_w, bufs["mask"], layer.eps,
+                               layer.clamp, layer.score_scale, None, bufs["work"], status)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(3):
+        flush()
+        run()
+    n = args.generic_steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for k in range(n):
+        flush()
+        run(evs[k])
+    torch.cuda.synchronize()
+    step = statistics.mean(ev[0].elapsed_time(ev[2]) for ev in evs) / 1e3
+    hg = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs) / 1e3
+    proj = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs) / 1e3
+    C = lay.n_cols
+    hg_bytes = 4 + 2 * C * R * 2
+    flops = 2.0 * C * R * (wg.hc + 1) * wg.hidden
+    out = {"workload": f"{T} tokens ({wg.n_seqs} x {wg.seq_len}), 2/3-grams x 8 heads = {C} rows of {R} bf16, "
+                       f"table {total} rows ({total * R * 2 / 1e9:.1f} GB), hidden {wg.hidden}, hc {wg.hc}, "
+                       "L2 flushed", "steps": n,
+           "step_ms": step * 1e3, "tokens_per_s": T / step, "hash_gather_ms": hg * 1e3,
+           "hash_gather_gbs": hg_bytes * T / hg / 1e9, "hash_gather_bytes_per_token": hg_bytes,
+           "project_gate_ms": proj * 1e3, "project_tflops": flops * T / proj / 1e12,
+           "device_status": int(status.item())}
+    del table
+    return out
 
 
 def conv_bench(args, w, inp, layer, flush, dev):

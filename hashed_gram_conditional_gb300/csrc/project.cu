@@ -1767,6 +1767,27 @@ namespace {
 // (measured on GB300: 256 tokens 114 us fused vs ~99 us two-kernel; break-even
 // near 2048 tokens).
 constexpr int64_t kTwoKernelMaxTokens = 1536;
+// Below this K the bf16 path always runs the two kernels: with few k-blocks per
+// tile the fused kernel's value tiles wait on their block's gates and their h
+// traffic is not hidden behind the main loop (GB300, 16,384 tokens, hidden
+// 2560: K 1280 fused 715 us vs 470 us, K 2560 807 vs 725 us; from K 4096 the
+// fused kernel wins, 1027 vs 1090 us, and at K 6144, hidden 5120, 3.05 vs
+// 3.29 ms).
+constexpr int64_t kFusedMinK = 3200;
+
+// The block-FP8 projection keeps a single accumulator buffer (TMEM also holds
+// the scale factors), so its fused epilogue cannot overlap the next tile's
+// main loop; the two kernels are faster at every size measured (16,384
+// tokens, hidden 5120: 2.53 ms per layer step vs 3.22 ms fused).
+// ENGRAM_FP8_FUSED=1 selects the fused FP8 kernel above 1536 tokens (for
+// comparisons).
+bool use_fp8_fused() {
+  static const bool v = [] {
+    const char* e = std::getenv("ENGRAM_FP8_FUSED");
+    return e != nullptr && e[0] == '1';
+  }();
+  return v;
+}
 
 struct FusedWs {
   size_t partials, counters_off, counter_words, gates_off, v_off, total;
@@ -1780,7 +1801,7 @@ FusedWs fused_ws(int64_t n_tokens, int32_t hidden, int32_t hc) {
   w.counter_words = mt * hc * 4 + mt + 1;
   w.gates_off = w.counters_off + (w.counter_words * 4 + 255) / 256 * 256;
   w.v_off = w.gates_off + (mt * BM * hc * sizeof(float) + 255) / 256 * 256;
-  w.total = w.v_off + (n_tokens <= kTwoKernelMaxTokens ? static_cast<size_t>(n_tokens) * hidden * 2 : 0);
+  w.total = w.v_off + static_cast<size_t>(n_tokens) * hidden * 2;  // v of the two-kernel path
   return w;
 }
 }  // namespace
@@ -1800,7 +1821,7 @@ extern "C" int engram_project_gate(const uint16_t* e_d, int64_t n_tokens, int64_
   const size_t need = engram_project_gate_workspace_bytes(n_tokens, hidden, hc);
   if (n_tokens > 0 && workspace_bytes < need)
     return fail(ENGRAM_E_SHAPE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
-  if (n_tokens > 0 && n_tokens <= kTwoKernelMaxTokens) {
+  if (n_tokens > 0 && (n_tokens <= kTwoKernelMaxTokens || K < kFusedMinK)) {
     const FusedWs ws = fused_ws(n_tokens, hidden, hc);
     unsigned char* base = static_cast<unsigned char*>(workspace_d);
     float* partials_d = reinterpret_cast<float*>(base);
@@ -1879,7 +1900,7 @@ extern "C" int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_
     return fail(ENGRAM_E_SHAPE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
   const FusedWs ws = fused_ws(n_tokens, hidden, hc);
   unsigned char* base = static_cast<unsigned char*>(workspace_d);
-  if (n_tokens > 0 && n_tokens <= kTwoKernelMaxTokens) {
+  if (n_tokens > 0 && (n_tokens <= kTwoKernelMaxTokens || !use_fp8_fused())) {
     float* partials_d = reinterpret_cast<float*>(base);
     uint16_t* v_d = reinterpret_cast<uint16_t*>(base + ws.v_off);
     int rc = engram_project_fp8(e8_d, sfa_d, n_tokens, K, w8_packed_d, sfb_d, hidden, hc, h_d, q_w_d, k_w_d,

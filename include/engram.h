@@ -416,7 +416,12 @@ int engram_project_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tok
                        const uint16_t* h_d, const float* q_w_d, const float* k_w_d, float* partials_d,
                        uint16_t* v_d, int32_t* status_d, void* stream);
 
-/* engram_project_gate on FP8 operands (same workspace, engram_project_gate_workspace_bytes). */
+/* engram_project_gate on FP8 operands (same workspace, engram_project_gate_workspace_bytes).
+ * It runs engram_project_fp8 and engram_gate_add inside the workspace: the
+ * FP8 kernel keeps one accumulator buffer, so a fused epilogue would not
+ * overlap the next tile's main loop, and the two kernels are faster at every
+ * size measured.  (ENGRAM_FP8_FUSED=1 in the environment selects the fused
+ * FP8 kernel above 1536 tokens, for comparisons.) */
 int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K,
                             const uint8_t* w8_packed_d, const uint32_t* sfb_d, int32_t hidden, int32_t hc,
                             uint16_t* h_d, const float* q_w_d, const float* k_w_d, const uint8_t* mask_d, float eps,
@@ -510,8 +515,8 @@ int engram_short_conv_add(const float* gate_d, const uint16_t* v_d, uint16_t* h_
 /* Bytes of the workspace of engram_project_gate: the partial sums
  * (engram_project_partials_bytes), then int32 counters
  * (2*ceil(n_tokens/256) * (4*hc + 1) + 1 words), then fp32 gates
- * (2*ceil(n_tokens/256) * 128 * hc), then, for at most 1536 tokens, bf16 v
- * (n_tokens * hidden); each part on a 256-byte boundary. */
+ * (2*ceil(n_tokens/256) * 128 * hc), then bf16 v (n_tokens * hidden) for the
+ * two-kernel path; each part on a 256-byte boundary. */
 size_t engram_project_gate_workspace_bytes(int64_t n_tokens, int32_t hidden, int32_t hc);
 
 /* The same result as engram_project followed by engram_gate_add, computed in
@@ -523,9 +528,11 @@ size_t engram_project_gate_workspace_bytes(int64_t n_tokens, int32_t hidden, int
  * stored.  The gate kernel of the unfused path sums with a shuffle tree, so
  * gates agree with engram_gate_add to fp32 rounding, not bit for bit; the
  * fused result itself is deterministic.  For at most 1536 tokens (decode
- * sizes, where the projection is only a wave or two of tiles) the call runs
- * engram_project and engram_gate_add inside the workspace instead, which is
- * faster there; the results agree to the same rounding.
+ * sizes, where the projection is only a wave or two of tiles) and for K below
+ * 3200 (few k-blocks per tile, so the value tiles' wait and h traffic are not
+ * hidden behind the main loop) the call runs engram_project and
+ * engram_gate_add inside the workspace instead, which is faster there; the
+ * results agree to the same rounding.
  *   e_d, wkv_packed_d, h_d, q_w_d, k_w_d   as engram_project (h_d updated in place)
  *   mask_d, eps, clamp, score_scale,
  *   gate_out_d                            as engram_gate_add

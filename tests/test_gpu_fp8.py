@@ -128,13 +128,14 @@ def test_fp8_layer_two_kernel_path(T):
     _fp8_layer_case("tiny", T_cut=T)
 
 
-def test_fp8_layer_fused_path():
-    """1700 tokens: the fused cooperative FP8 kernel (gate and residual in the epilogue)."""
+def test_fp8_layer_1700_tokens():
+    """1700 tokens (ragged M tail): the FP8 projection and the gate kernel, or the
+    fused cooperative FP8 kernel when ENGRAM_FP8_FUSED=1."""
     _fp8_layer_case("tiny", T_cut=1700, seed=1)
 
 
 def test_fp8_layer_prefill_sampled():
-    """The prefill batch (16,384 tokens, hidden 5120) through the fused FP8 kernel, every 61st token."""
+    """The prefill batch (16,384 tokens, hidden 5120) through the FP8 path, every 61st token."""
     _fp8_layer_case("prefill", sample=61, seed=2)
 
 

@@ -1,8 +1,9 @@
 """The alternative projection kernels pass the same parity tests as the
 defaults: the single-CTA bf16 kernels at every size (ENGRAM_SINGLE_CTA_MMA=1),
 the CTA-pair bf16 kernels at every size (=0; by default batches of at most
-128 tokens take the single-CTA kernel), and the CTA-pair block-FP8 kernels
-(ENGRAM_FP8_PAIR=1).
+128 tokens take the single-CTA kernel), the CTA-pair block-FP8 kernels
+(ENGRAM_FP8_PAIR=1) and the fused block-FP8 kernels (ENGRAM_FP8_FUSED=1; by
+default the FP8 gate runs as a separate kernel).
 
 The selection is read once per process, so the tests run in a child process.
 """
@@ -41,5 +42,15 @@ def test_pair_kernels_at_every_size_pass_projection_parity():
     here = os.path.dirname(os.path.abspath(__file__))
     env = dict(os.environ, ENGRAM_SINGLE_CTA_MMA="0")
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_project.py"), "-m", "gpu", "-q",
+                        "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_fused_fp8_kernels_pass_fp8_parity(pair):
+    require_gpu()
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, ENGRAM_FP8_FUSED="1", ENGRAM_FP8_PAIR=pair)
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_fp8.py"), "-m", "gpu", "-q",
                         "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
