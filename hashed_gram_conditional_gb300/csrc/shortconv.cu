@@ -67,6 +67,48 @@ __device__ __forceinline__ float silu(float x) {
   return x * r;
 }
 
+// Pairs of fp32 values in one 64-bit register pair, for the packed
+// two-lane fp32 instructions of sm_100+ (add/mul/fma .rn.f32x2): each lane
+// is the IEEE round-to-nearest result of the scalar operation, so the packed
+// code computes exactly what the scalar code does, in half the instructions.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t f2_bf16(uint32_t w) {  // the two bf16 of a word, widened
+  return f2(bf16_lo(w), bf16_hi(w));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// silu of both lanes, as silu() above
+__device__ __forceinline__ uint64_t silu2(uint64_t x) {
+  float m0, m1, e0, e1, d0, d1, r0, r1;
+  f2_split(f2_mul(x, f2(-1.4426950408889634f, -1.4426950408889634f)), m0, m1);
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(m0));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(m1));
+  f2_split(f2_add(f2(1.0f, 1.0f), f2(e0, e1)), d0, d1);
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d0));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d1));
+  return f2_mul(x, f2(r0, r1));
+}
+
 struct ConvArgs {
   const float* gate;      // [T][hc]
   const uint4* v;         // [T][H/8]
@@ -185,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, 2) conv_add_kernel(ConvArgs a, int w
   if (p - lane >= a.hc * nchunk) return;
   const int m = p / nchunk, c = p - m * nchunk;
   const int hc = a.hc, dil = a.dil;
-  float wg[K][kCh];
+  constexpr int kP = kCh / 2;  // channel pairs per thread
+  uint64_t wg[K][kP];           // filter taps with the RMSNorm weight folded in, packed pairs
   {
     const float4* gq = reinterpret_cast<const float4*>(a.gamma + static_cast<int64_t>(m) * a.hidden + c * kCh);
     const float4 gx = __ldg(gq), gy = __ldg(gq + 1);
@@ -196,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 2) conv_add_kernel(ConvArgs a, int w
       const float4 x = __ldg(wp), y = __ldg(wp + 1);
       const float wk[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 #pragma unroll
-      for (int j = 0; j < kCh; ++j) wg[k][j] = wk[j] * gam[j];
+      for (int j = 0; j < kP; ++j) wg[k][j] = f2(wk[2 * j] * gam[2 * j], wk[2 * j + 1] * gam[2 * j + 1]);
     }
   }
   // this block's walk: positions t0 + rho + j*dil, j < walk_len, below t1
@@ -241,21 +284,21 @@ __global__ void __launch_bounds__(kThreads, 2) conv_add_kernel(ConvArgs a, int w
   };
   for (int s = 0; s < kInStages - 1; ++s) issue(s);
 
-  // window slot (u - k) mod 3 holds x of k steps back at unrolled step u
-  float win[3][kCh];
+  // window slot (u - k) mod 3 holds x of k steps back at unrolled step u (packed pairs)
+  uint64_t win[3][kP];
 #pragma unroll
   for (int k = 1; k <= 3; ++k) {
     const int64_t q = first - static_cast<int64_t>(k) * dil;
-    float* wdst = win[(3 - k) % 3];
+    uint64_t* wdst = win[(3 - k) % 3];
     if (k < K && q >= 0) {
       const float rq = __ldg(a.r + q * hc + m);
-      float f[kCh];
-      unpack8(__ldg(a.v + q * nchunk + c), f);
+      const uint4 vq = __ldg(a.v + q * nchunk + c);
+      const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
 #pragma unroll
-      for (int j = 0; j < kCh; ++j) wdst[j] = rq * f[j];
+      for (int j = 0; j < kP; ++j) wdst[j] = f2_mul(f2(rq, rq), f2_bf16(vw[j]));
     } else {
 #pragma unroll
-      for (int j = 0; j < kCh; ++j) wdst[j] = 0.f;
+      for (int j = 0; j < kP; ++j) wdst[j] = f2(0.f, 0.f);
     }
   }
 
@@ -294,22 +337,22 @@ __global__ void __launch_bounds__(kThreads, 2) conv_add_kernel(ConvArgs a, int w
           gt_n = __ldg(gp);
           lt_n = __ldg(pp);
         }
-        float xt[kCh];
+        const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+        uint64_t xt[kP];
         {
-          float vt[kCh];
-          unpack8(vv, vt);
+          const uint64_t rt2 = f2(rt, rt);
 #pragma unroll
-          for (int q = 0; q < kCh; ++q) xt[q] = rt * vt[q];
+          for (int q = 0; q < kP; ++q) xt[q] = f2_mul(rt2, f2_bf16(vw[q]));
         }
         if (lt >= 0) {
-          float acc[kCh];
+          uint64_t acc[kP];
 #pragma unroll
-          for (int q = 0; q < kCh; ++q) acc[q] = wg[0][q] * xt[q];
+          for (int q = 0; q < kP; ++q) acc[q] = f2_mul(wg[0][q], xt[q]);
           if (lt >= tail) {
 #pragma unroll
             for (int k = 1; k < K; ++k) {
 #pragma unroll
-              for (int q = 0; q < kCh; ++q) acc[q] = fmaf(wg[k][q], win[(u - k + 3) % 3][q], acc[q]);
+              for (int q = 0; q < kP; ++q) acc[q] = f2_fma(wg[k][q], win[(u - k + 3) % 3][q], acc[q]);
             }
           } else {
 #pragma unroll
@@ -317,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 2) conv_add_kernel(ConvArgs a, int w
               const int ql = lt - k * dil;
               if (ql >= 0) {
 #pragma unroll
-                for (int q = 0; q < kCh; ++q) acc[q] = fmaf(wg[k][q], win[(u - k + 3) % 3][q], acc[q]);
+                for (int q = 0; q < kP; ++q) acc[q] = f2_fma(wg[k][q], win[(u - k + 3) % 3][q], acc[q]);
               } else if (a.state != nullptr) {
                 const int64_t tc = first + static_cast<int64_t>(j) * dil;
                 const int64_t t_start = tc - lt;  // the sequence's first position
@@ -327,19 +370,20 @@ __global__ void __launch_bounds__(kThreads, 2) conv_add_kernel(ConvArgs a, int w
                 const float4* sp = reinterpret_cast<const float4*>(
                     a.state + ((static_cast<int64_t>(slot) * a.ring + idx) * hc + m) * a.hidden + c * kCh);
                 const float4 x = sp[0], y = sp[1];
-                const float sx[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+                const uint64_t sx[4] = {f2(x.x, x.y), f2(x.z, x.w), f2(y.x, y.y), f2(y.z, y.w)};
 #pragma unroll
-                for (int q = 0; q < kCh; ++q) acc[q] = fmaf(wg[k][q], sx[q], acc[q]);
+                for (int q = 0; q < kP; ++q) acc[q] = f2_fma(wg[k][q], sx[q], acc[q]);
               }
             }
           }
           // h + (g v + SiLU(c)), a pair of channels at a time
-          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+          const uint64_t gt2 = f2(gt, gt);
           uint32_t ow[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float lo = bf16_lo(hw[q]) + (gt * bf16_lo(vw[q]) + silu(acc[2 * q]));
-            const float hi = bf16_hi(hw[q]) + (gt * bf16_hi(vw[q]) + silu(acc[2 * q + 1]));
+          for (int q = 0; q < kP; ++q) {
+            float lo, hi;
+            f2_split(f2_add(f2_bf16(hw[q]), f2_fma(gt2, f2_bf16(vw[q]), silu2(acc[q]))), lo, hi);
             ow[q] = pack_bf16(lo, hi);
           }
           *hdst = make_uint4(ow[0], ow[1], ow[2], ow[3]);  // padding positions are not written
@@ -347,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 2) conv_add_kernel(ConvArgs a, int w
         hdst += hstride;
         // the window slot of x_t is the one that held x of three steps back
 #pragma unroll
-        for (int q = 0; q < kCh; ++q) win[u][q] = xt[q];
+        for (int q = 0; q < kP; ++q) win[u][q] = xt[q];
         rt = rt_n;
         gt = gt_n;
         lt = lt_n;
