@@ -935,7 +935,19 @@ def fp8_bench(args, w, inp, layer, flush, dev):
     proj = statistics.mean(ev[1].elapsed_time(ev[3]) for ev in evs) / 1e3
     hg = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs) / 1e3
     flops = 2.0 * T * K * N
-    return {"workload": f"{w.name} batch ({T} tokens), block-FP8 wkv (E4M3, E8M0 per 32 of k), L2 flushed",
+    out = {}
+    if not args.no_cpu_baseline:
+        from oracle import dequant as OD
+        from oracle import pipeline as OP
+        from workloads import bf16_bits_to_f64, mxfp8_weights
+        n_o, raw_o, cu_o, tm_o, lay_o, table_o = oracle_prefix(w, inp, 2048)
+        W8 = OD.dequant_mx_weights(*mxfp8_weights(K, N, w.seed))
+        h_o = bf16_bits_to_f64(inp["h_bits"][:n_o])
+        out["cpu_baseline"] = oracle_timed(
+            lambda: OP.layer_forward(lay_o, 0, raw_o, cu_o, tm_o, table_o, W8, h_o, inp["lw"].q_w, inp["lw"].k_w),
+            n_o, f"first {n_o} packed positions, one full layer pass with the dequantised block-FP8 wkv")
+        del W8
+    return {**out, "workload": f"{w.name} batch ({T} tokens), block-FP8 wkv (E4M3, E8M0 per 32 of k), L2 flushed",
             "steps": n, "step_ms": step * 1e3, "tokens_per_s": T / step, "hash_gather_ms": hg * 1e3,
             "project_gate_ms": pg * 1e3, "project_ms": proj * 1e3, "gate_ms": (pg - proj) * 1e3,
             "project_tflops": flops / proj / 1e12, "timed_s": timed,
@@ -1006,13 +1018,30 @@ def generic_bench(args, w, flush, dev):
     C = lay.n_cols
     hg_bytes = 4 + 2 * C * R * 2
     flops = 2.0 * C * R * (wg.hc + 1) * wg.hidden
+    base = {}
+    if not args.no_cpu_baseline:
+        from oracle import dequant as OD
+        from oracle import layout as OL
+        from oracle import pipeline as OP
+        from workloads import bf16_bits_to_f64, table_rows_bf16
+        n_o = 2048
+        cu_o = np.minimum(b.cu_seqlens, n_o)
+        cu_o = cu_o[: int(np.searchsorted(cu_o, n_o)) + 1]
+        lay_o = OL.build_layout(wg.v, wg.base_rows, [2, 15], max_ngram=3, n_heads=8, pad_id=int(tm[0]))
+        W = bf16_bits_to_f64(lw.wkv_bits)
+        h_o = bf16_bits_to_f64(residual_bits(n_o, wg.hc, wg.hidden, wg.seed))
+        base["cpu_baseline"] = oracle_timed(
+            lambda: OP.layer_forward(lay_o, 1, b.raw_ids[:n_o], cu_o, tm,
+                                     lambda r: bf16_bits_to_f64(table_rows_bf16(wg.seed, r, R)), W, h_o, lw.q_w,
+                                     lw.k_w, gather=OD.gather_rows),
+            n_o, f"first {n_o} packed positions, one full layer pass")
     out = {"workload": f"{T} tokens ({wg.n_seqs} x {wg.seq_len}), 2/3-grams x 8 heads = {C} rows of {R} bf16, "
                        f"table {total} rows ({total * R * 2 / 1e9:.1f} GB), hidden {wg.hidden}, hc {wg.hc}, "
                        "L2 flushed", "steps": n,
            "step_ms": step * 1e3, "tokens_per_s": T / step, "hash_gather_ms": hg * 1e3,
            "hash_gather_gbs": hg_bytes * T / hg / 1e9, "hash_gather_bytes_per_token": hg_bytes,
            "project_gate_ms": proj * 1e3, "project_tflops": flops * T / proj / 1e12,
-           "device_status": int(status.item())}
+           "device_status": int(status.item()), **base}
     del table
     return out
 
@@ -1064,7 +1093,18 @@ def conv_bench(args, w, inp, layer, flush, dev):
     step = statistics.mean(ev[0].elapsed_time(ev[2]) for ev in evs) / 1e3
     conv_s = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs) / 1e3
     cbytes = CONV_BYTES_PER_TOKEN(w.hc, w.hidden) * T
-    return {"workload": f"{w.name} batch, kernel 4, dilation 3, state ring kept per sequence", "steps": n,
+    out = {}
+    if not args.no_cpu_baseline:
+        from oracle import pipeline as OP
+        from workloads import bf16_bits_to_f64
+        n_o, raw_o, cu_o, tm_o, lay_o, table_o = oracle_prefix(w, inp, 2048)
+        h_o = bf16_bits_to_f64(inp["h_bits"][:n_o])
+        cp = OP.ConvParams(cw.astype(np.float64), gamma.astype(np.float64), 3)
+        out["cpu_baseline"] = oracle_timed(
+            lambda: OP.layer_forward_conv(lay_o, 0, raw_o, cu_o, tm_o, table_o, oracle_wkv(inp), h_o,
+                                          inp["lw"].q_w, inp["lw"].k_w, cp),
+            n_o, f"first {n_o} packed positions, one full layer pass with the short convolution")
+    return {**out, "workload": f"{w.name} batch, kernel 4, dilation 3, state ring kept per sequence", "steps": n,
             "step_ms": step * 1e3, "tokens_per_s": T / step, "conv_ms": conv_s * 1e3,
             "conv_gbs": cbytes / conv_s / 1e9, "algorithmic_bytes": cbytes, "device_status": int(status.item()),
             "kernels": "conv_prep_kernel + conv_add_kernel + conv_state_kernel",
@@ -1200,6 +1240,37 @@ def oracle_sample(w, inp, n_tokens):
     def run():
         return OP.layer_forward(lay_o, 0, raw, cu, tm, table, W, h, inp["lw"].q_w, inp["lw"].k_w)
     return n, run
+
+
+def oracle_timed(run, n, label):
+    """Time one bounded oracle run (the oracle as it stands) as a cpu_baseline entry."""
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{label} (numpy fp64, BLAS threads = all cores); {dt:.1f} s"}
+
+
+def oracle_prefix(w, inp, n_tokens):
+    """The first n_tokens packed positions of the batch, their layout and table reader for the oracle."""
+    from oracle import hashing as OH
+    from oracle import layout as OL
+    from workloads import table_rows
+
+    b = inp["batch"]
+    n = min(n_tokens, len(b.raw_ids))
+    raw = b.raw_ids[:n]
+    cu = np.minimum(b.cu_seqlens, n)
+    cu = cu[: int(np.searchsorted(cu, n)) + 1]
+    tm = inp["tm"]
+    lay_o = OL.build_layout(w.v, w.base_rows, [w.layer_id], pad_id=int(tm[0]))
+    rows, _, _ = OH.hash_prefill(raw, cu, tm, lay_o, 0)
+    uniq = np.unique(rows)
+    cache = dict(zip(uniq.tolist(), table_rows(w.seed, uniq)))   # table bytes, read by the oracle below
+
+    def table(r):
+        return np.stack([cache[int(x)] for x in r])
+    return n, raw, cu, tm, lay_o, table
 
 
 def cpu_baseline(w, inp, n_tokens):

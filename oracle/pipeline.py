@@ -30,13 +30,15 @@ class LayerResult:
 
 def layer_forward(layout: Layout, layer: int, raw_ids, cu_seqlens, token_map, table_rows,
                   wkv, h, q_w, k_w, hist: Optional[np.ndarray] = None, eps: float = 1e-6,
-                  clamp: float = 1e-6, score_scale=None) -> LayerResult:
+                  clamp: float = 1e-6, score_scale=None, gather=dequant.gather_dequant) -> LayerResult:
     """Prefill of one Engram layer on packed sequences.
 
-    wkv: float64 [n_cols*256][(hc+1)H]; h: float64 [T][hc][H].
+    wkv: float64 [n_cols*row_dim][(hc+1)H]; h: float64 [T][hc][H].  ``gather``
+    turns row ids into e: the E4M3 + E8M0 rows by default, or
+    dequant.gather_rows for a table of plain bf16 rows.
     """
     rows, mask, new_hist = hashing.hash_prefill(raw_ids, cu_seqlens, token_map, layout, layer, hist)
-    e = dequant.gather_dequant(rows, table_rows)
+    e = gather(rows, table_rows)
     hc, H = h.shape[1], h.shape[2]
     kv = gate.project(e, wkv)
     k, v = gate.split_kv(kv, H, hc)
