@@ -941,6 +941,11 @@ class EngramLayer:
     stream and updates the residual ``h`` in place (``fused=False`` runs the
     projection and the gate kernel separately).
 
+    ``wkv_packed`` is either the bf16 wkv from ``engram_pack_wkv`` or the pair
+    (w8p, sfb) from ``engram_pack_wkv_fp8`` (block-FP8 weights): the layer then
+    gathers the rows as stored (E4M3 + E8M0) and runs the block-scaled FP8
+    projection ([P-O1] §2.3).
+
     The table may be a device tensor or a pinned host tensor (Grace memory).
     ``prefetch`` + ``prefill_prefetched`` split the layer at the point the
     Engram pages use for offloading: the rows a batch needs depend only on its
@@ -955,6 +960,11 @@ class EngramLayer:
         self.conv = conv
         self.layout, self.layer = layout, layer
         self.table, self.token_map = table, token_map
+        self.fp8 = isinstance(wkv_packed, (tuple, list))
+        if self.fp8:
+            self.w8p, self.sfb = wkv_packed
+            if table.dtype != torch.uint8:
+                raise ValueError("block-FP8 weights go with the E4M3 + E8M0 row table")
         self.wkv_packed, self.q_w, self.k_w = wkv_packed, q_w, k_w
         self.hidden, self.hc = q_w.shape[0], q_w.shape[1]
         self.eps, self.clamp = eps, clamp
@@ -975,7 +985,9 @@ class EngramLayer:
             self._ws = {key: dict(
                 rows=torch.empty((T, self.layout.n_cols), dtype=torch.int32, device=device),
                 mask=torch.empty(T, dtype=torch.uint8, device=device),
-                e=torch.empty((T, self.e_dim), dtype=torch.bfloat16, device=device),
+                e=torch.empty((T, self.e_dim), dtype=torch.bfloat16, device=device) if not self.fp8 else None,
+                e8=torch.empty((T, self.e_dim), dtype=torch.uint8, device=device) if self.fp8 else None,
+                sf=torch.empty((2 * self.layout.n_cols, T), dtype=torch.int32, device=device) if self.fp8 else None,
                 partials=torch.empty(partials_shape(T, self.hidden, self.hc), dtype=torch.float32, device=device),
                 v=torch.empty((T, self.hidden), dtype=torch.bfloat16, device=device),
                 work=project_gate_workspace(T, self.hidden, self.hc, device),
@@ -1001,6 +1013,9 @@ class EngramLayer:
         if self.row_dim is not None:
             engram_hash_gather_rows_bf16(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, self.table,
                                          hist, b["e"], b["mask"], b["rows"], status)
+        elif self.fp8:
+            engram_hash_gather_fp8(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, self.table, hist,
+                                   b["e8"], b["sf"], b["mask"], b["rows"], status)
         else:
             engram_hash_gather(self.layout, self.layer, raw_ids, cu_seqlens, self.token_map, self.table, hist,
                                b["e"], b["mask"], b["rows"], status)
@@ -1041,8 +1056,8 @@ class EngramLayer:
         the current stream.  At most two batches may be waiting at a time.
         (E4M3 + E8M0 tables only.)
         """
-        if self.row_dim is not None:
-            raise ValueError("prefetch handles the 264-byte E4M3 + E8M0 row tables only")
+        if self.row_dim is not None or self.fp8:
+            raise ValueError("prefetch handles the 264-byte E4M3 + E8M0 row tables with bf16 weights only")
         dev = raw_ids.device
         T = raw_ids.numel()
         slot = self._prefetch_slot(T, dev)
@@ -1100,6 +1115,9 @@ class EngramLayer:
             engram_hash_step(self.layout, self.layer, raw_ids, slots, self.token_map, hist, b["rows"], b["mask"],
                              status)
             engram_gather_rows_bf16(self.table, b["rows"], b["e"], status)
+        elif self.fp8:
+            engram_hash_gather_step_fp8(self.layout, self.layer, raw_ids, slots, self.token_map, self.table, hist,
+                                        b["e8"], b["sf"], b["mask"], b["rows"], status)
         else:
             engram_hash_gather_step(self.layout, self.layer, raw_ids, slots, self.token_map, self.table, hist,
                                     b["e"], b["mask"], b["rows"], status)
@@ -1111,19 +1129,30 @@ class EngramLayer:
             # the original layer: gates, then the short convolution with the residual add
             c = self.conv
             T = h.shape[0]
-            engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
+            self._project(b, h, status)
             g = engram_gates(b["partials"], T, self.hidden, self.hc, b["mask"], self.eps, self.clamp,
                              self.score_scale, gate_out if gate_out is not None else b["gate"])
             state, head = conv_state if conv_state is not None else (None, None)
             engram_short_conv_add(g, b["v"], h, b["mask"], c.w, c.gamma, c.dilation, c.eps, cu_seqlens,
                                   slots if cu_seqlens is None else None, state, head, b["conv_ws"], status)
             return
-        if self.fused:
+        if self.fused and self.fp8:
+            engram_project_gate_fp8(b["e8"], b["sf"], self.w8p, self.sfb, h, self.q_w, self.k_w, b["mask"], self.eps,
+                                    self.clamp, self.score_scale, gate_out, b["work"], status)
+        elif self.fused:
             engram_project_gate(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["mask"], self.eps, self.clamp,
                                 self.score_scale, gate_out, b["work"], status)
         else:
-            engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
+            self._project(b, h, status)
             engram_gate_add(b["partials"], b["v"], h, b["mask"], self.eps, self.clamp, self.score_scale, gate_out)
+
+    def _project(self, b, h, status):
+        """The unfused projection: partial sums and bf16 v into the layer's buffers."""
+        if self.fp8:
+            engram_project_fp8(b["e8"], b["sf"], self.w8p, self.sfb, h, self.q_w, self.k_w, b["partials"], b["v"],
+                               status)
+        else:
+            engram_project(b["e"], self.wkv_packed, h, self.q_w, self.k_w, b["partials"], b["v"], status)
 
 
 class DecodeGraph:

@@ -143,3 +143,57 @@ def test_fp8_layer_prefill_sampled():
 def test_fp8_layer_decode_size(T):
     """Decode-size batches at hidden 5120 through the two-kernel FP8 path, every 16th token."""
     _fp8_layer_case("prefill", T_cut=T, sample=16, seed=3)
+
+
+def test_engram_layer_with_fp8_weights_prefill_and_decode():
+    """EngramLayer built with (w8p, sfb) from engram_pack_wkv_fp8: prefill of a
+    ragged batch against the oracle, then decode steps bit for bit against the
+    direct calls (fused FP8 decode step + FP8 projection and gate)."""
+    w, tm, lay_o, lay = setup("tiny")
+    total = lay_o.layers[0].total_rows
+    table = device_table(total, w.seed)
+    K, N = 24 * 256, (w.hc + 1) * w.hidden
+    w8, sfw = mxfp8_weights(K, N, 21)
+    w8p, sfb = eg.engram_pack_wkv_fp8(u8(w8), u8(sfw))
+    lw = layer_weights(w)
+    layer = eg.EngramLayer(lay, 0, table, i32(tm), (w8p, sfb), f32(lw.q_w), f32(lw.k_w))
+    rng = np.random.default_rng(12)
+    lens = [1, 150, 149]
+    raw = rng.integers(0, w.v_raw, size=sum(lens)).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T = len(raw)
+    h_bits = residual_bits(T, w.hc, w.hidden, 13)
+    h = bf16(h_bits)
+    gate = torch.empty((T, w.hc), dtype=torch.float32, device=DEV)
+    hist = i32(np.full((3, 3), lay.pad_id))
+    st = status()
+    layer.prefill(i32(raw), i64(cu), h, hist, status=st, gate_out=gate)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rows_o, mask_o, hist_o = OH.hash_prefill(raw, cu, tm, lay_o, 0)
+    assert (hist.cpu().numpy() == hist_o).all()
+    e = OD.gather_dequant(rows_o, lambda r: table_rows(w.seed, r))
+    W = OD.dequant_mx_weights(w8, sfw)
+    k, v = OG.split_kv(OG.project(e, W), w.hidden, w.hc)
+    hf = bf16_bits_to_f64(h_bits)
+    g = OG.gate(hf, k, lw.q_w, lw.k_w, mask_o)
+    out = OG.residual(hf, g, v, mask_o)
+    assert np.abs(gate.cpu().numpy() - g).max() <= GATE_ATOL
+    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h)), out, hf, g, v,
+                                       dot_error_bound(e, W[:, w.hc * w.hidden:]))
+    assert ok, (worst, strict)
+    # decode: the layer against the direct calls, from the same history
+    slots = i32(np.array([2, 0, 1], dtype=np.int32))
+    hist_d = hist.clone()
+    h_l = bf16(residual_bits(3, w.hc, w.hidden, 14))
+    h_d = h_l.clone()
+    work = eg.project_gate_workspace(3, w.hidden, w.hc, DEV)
+    for step in range(3):
+        new = i32(rng.integers(0, w.v_raw, size=3).astype(np.int32))
+        layer.decode(new, slots, hist, h_l, status=st)
+        e8, sf, m = eg.engram_hash_gather_step_fp8(lay, 0, new, slots, i32(tm), table, hist_d)
+        eg.engram_project_gate_fp8(e8, sf, w8p, sfb, h_d, f32(lw.q_w), f32(lw.k_w), m, workspace=work)
+        torch.cuda.synchronize()
+        assert (bits(h_l) == bits(h_d)).all(), step
+        assert (hist.cpu().numpy() == hist_d.cpu().numpy()).all(), step
+    assert int(st.item()) == 0
