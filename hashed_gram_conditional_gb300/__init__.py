@@ -1027,10 +1027,16 @@ class EngramLayer:
         if key not in self._pf:
             C = self.layout.n_cols
             host = not self.table.is_cuda
+            fp8 = self.fp8
             self._pf = {key: [dict(
                 rows=torch.empty((T, C), dtype=torch.int32, device=device),
                 mask=torch.empty(T, dtype=torch.uint8, device=device),
-                e=torch.empty((T, C * HEAD_DIM), dtype=torch.bfloat16, device=device),
+                e=torch.empty((T, C * HEAD_DIM), dtype=torch.bfloat16, device=device) if not fp8 else None,
+                e8=torch.empty((T, C * HEAD_DIM), dtype=torch.uint8, device=device) if fp8 else None,
+                sf=torch.empty((2 * C, T), dtype=torch.int32, device=device) if fp8 else None,
+                # the staged rows in order: row t*C + j of the staging buffer is column j of position t
+                staged_ids=(torch.arange(T * C, dtype=torch.int32, device=device).view(T, C)
+                            if fp8 and host else None),
                 rows_h=torch.empty((T, C), dtype=torch.int32, pin_memory=True) if host else None,
                 staging=torch.empty(T * C * ROW_BYTES, dtype=torch.uint8, pin_memory=True) if host else None,
                 staged=torch.empty(T * C * ROW_BYTES, dtype=torch.uint8, device=device) if host else None,
@@ -1052,12 +1058,13 @@ class EngramLayer:
         a pinned host table the rest runs on ``copy_stream``: the row ids go to
         the host, ``n_threads`` host threads gather the 264-byte rows into a
         pinned staging buffer, one DMA moves it to the device and the rows are
-        dequantised there.  With a device table the gather follows the hash on
+        dequantised there (with block-FP8 weights: regrouped as stored for the
+        FP8 projection).  With a device table the gather follows the hash on
         the current stream.  At most two batches may be waiting at a time.
         (E4M3 + E8M0 tables only.)
         """
-        if self.row_dim is not None or self.fp8:
-            raise ValueError("prefetch handles the 264-byte E4M3 + E8M0 row tables with bf16 weights only")
+        if self.row_dim is not None:
+            raise ValueError("prefetch handles the 264-byte E4M3 + E8M0 row tables only")
         dev = raw_ids.device
         T = raw_ids.numel()
         slot = self._prefetch_slot(T, dev)
@@ -1067,7 +1074,10 @@ class EngramLayer:
                     status)
         ready = torch.cuda.Event()
         if self.table.is_cuda:
-            engram_gather_dequant(self.table, self.total_rows, slot["rows"], slot["e"], status)
+            if self.fp8:
+                engram_gather_fp8(self.table, self.total_rows, slot["rows"], slot["e8"], slot["sf"], status)
+            else:
+                engram_gather_dequant(self.table, self.total_rows, slot["rows"], slot["e"], status)
             ready.record(cur)
         else:
             cs = copy_stream if copy_stream is not None else torch.cuda.Stream(dev)
@@ -1079,7 +1089,11 @@ class EngramLayer:
                 engram_host_gather_async(self.table, self.total_rows, slot["rows_h"], slot["staging"], slot["bad"],
                                          cs, n_threads)
                 slot["staged"].copy_(slot["staging"], non_blocking=True)
-                engram_dequant_rows(slot["staged"], self.layout.n_cols, slot["e"], status)
+                if self.fp8:
+                    engram_gather_fp8(slot["staged"], T * self.layout.n_cols, slot["staged_ids"], slot["e8"],
+                                      slot["sf"], status)
+                else:
+                    engram_dequant_rows(slot["staged"], self.layout.n_cols, slot["e"], status)
                 ready.record(cs)
         slot["busy"] = True
         return Prefetched(slot, T, ready, cu_seqlens)
@@ -1095,7 +1109,7 @@ class EngramLayer:
         cur = torch.cuda.current_stream(dev)
         cur.wait_event(pf.ready)
         b = dict(self._buffers(pf.T, dev))
-        b.update(e=pf.slot["e"], mask=pf.slot["mask"], rows=pf.slot["rows"])
+        b.update(e=pf.slot["e"], e8=pf.slot["e8"], sf=pf.slot["sf"], mask=pf.slot["mask"], rows=pf.slot["rows"])
         self._gate(b, h, status, gate_out, cu_seqlens=pf.cu_seqlens, conv_state=conv_state)
         pf.slot["consumed"].record(cur)
         pf.slot["busy"] = False

@@ -97,3 +97,34 @@ def test_prefetch_pipeline_matches_device_table():
     idx = np.arange(0, T, 97)
     ref = OD.gather_dequant(rows_o[idx], lambda r: table_rows(w.seed, r))
     assert (e_bits[idx] == OD.bf16_bits(ref)).all()
+
+
+def test_fp8_prefetch_from_host_table_matches_device_table():
+    """A layer with block-FP8 weights over a pinned host table (tiny layout):
+    prefetch (host gather -> DMA -> rows regrouped as stored for the FP8
+    projection) then prefill_prefetched gives, bit for bit, the FP8 layer's
+    result over the device table."""
+    from workloads import mxfp8_weights
+    w, tm, lay_o, lay = setup("tiny")
+    total = lay_o.layers[0].total_rows
+    host = _host_table(total, w.seed)
+    K, N = 24 * 256, (w.hc + 1) * w.hidden
+    w8, sfw = mxfp8_weights(K, N, 31)
+    packed = eg.engram_pack_wkv_fp8(torch.from_numpy(w8).cuda(), torch.from_numpy(sfw).cuda())
+    lw = layer_weights(w)
+    args = (i32(tm), packed, f32(lw.q_w), f32(lw.k_w))
+    dev_layer = eg.EngramLayer(lay, 0, device_table(total, w.seed), *args)
+    host_layer = eg.EngramLayer(lay, 0, host, *args)
+    rng = np.random.default_rng(17)
+    raw = rng.integers(0, w.v_raw, size=300).astype(np.int32)
+    cu = np.array([0, 120, 300], dtype=np.int64)
+    h_bits = residual_bits(300, w.hc, w.hidden, 19)
+    st = status()
+    pf = host_layer.prefetch(i32(raw), i64(cu), status=st, copy_stream=torch.cuda.Stream())
+    h = bf16(h_bits)
+    host_layer.prefill_prefetched(pf, h, st)
+    h_ref = bf16(h_bits)
+    dev_layer.prefill(i32(raw), i64(cu), h_ref, status=st)
+    torch.cuda.synchronize()
+    assert pf.bad_rows == 0 and int(st.item()) == 0
+    assert (bits(h) == bits(h_ref)).all()
