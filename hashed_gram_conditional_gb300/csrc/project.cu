@@ -312,11 +312,21 @@ __device__ __forceinline__ EpiTile epi_tile(const ProjArgs& a, int nb) {
   return e;
 }
 
-// Before the accumulator is ready: stage q_w * k_w of a key tile's 256
-// columns in the warp's own copy (no cross-warp barrier).
-__device__ __forceinline__ void epilogue_stage(const ProjArgs& a, SmemCtl* ctl, int q, uint32_t lane,
+// Asks L2 for `bytes` (a multiple of 16) at a 16-byte-aligned global address.
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Before the accumulator is ready: ask L2 for the h row segments the key
+// tile's epilogue will read (each lane its own row: 256 columns of the key's
+// stream, 512 B), so that the epilogue's loads hit L2 rather than each chunk
+// waiting on DRAM; and stage q_w * k_w of the tile's 256 columns in the
+// warp's own copy (no cross-warp barrier).
+__device__ __forceinline__ void epilogue_stage(const ProjArgs& a, SmemCtl* ctl, int q, uint32_t lane, int mb,
                                                const EpiTile& et) {
   if (!et.key_tile) return;
+  const int64_t t = static_cast<int64_t>(mb) * BM + q * 32 + static_cast<int>(lane);
+  if (t < a.M) l2_prefetch(a.h + (t * a.hc + et.m) * a.H + et.c0, BN * 2);
   float* qk = ctl->qk[q];
   __syncwarp();
   for (int c = static_cast<int>(lane); c < BN; c += 32) {
@@ -344,20 +354,26 @@ __device__ __forceinline__ bool epilogue_tile(const ProjArgs& a, SmemCtl* ctl, i
   if (key_tile) {
     const uint4* hrow = reinterpret_cast<const uint4*>(a.h + (t * a.hc + m) * a.H + c0);
     float dot = 0.f, kk = 0.f, hh = 0.f;
-    // h of chunk ch+1 is requested while chunk ch is processed (one chunk ahead)
-    uint4 hnext[4];
+    // h of chunks ch+1 and ch+2 is in flight while chunk ch is processed
+    uint4 hn1[4], hn2[4];
     if (live) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) hnext[i] = __ldg(hrow + i);
+      for (int i = 0; i < 4; ++i) {
+        hn1[i] = __ldg(hrow + i);
+        hn2[i] = __ldg(hrow + 4 + i);
+      }
     }
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
       uint4 hv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) hv[i] = hnext[i];
-      if (live && ch + 1 < BN / 32) {
+      for (int i = 0; i < 4; ++i) {
+        hv[i] = hn1[i];
+        hn1[i] = hn2[i];
+      }
+      if (live && ch + 2 < BN / 32) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) hnext[i] = __ldg(hrow + (ch + 1) * 4 + i);
+        for (int i = 0; i < 4; ++i) hn2[i] = __ldg(hrow + (ch + 2) * 4 + i);
       }
       uint32_t r[32];
       __syncwarp();
@@ -648,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       const EpiTile et = epi_tile(a, nb);
-      epilogue_stage(a, ctl, q, lane, et);
+      epilogue_stage(a, ctl, q, lane, mb, et);
       if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag)) {
         if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
         break;
@@ -809,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       const EpiTile et = epi_tile(a, nb);
-      epilogue_stage(a, ctl, q, lane, et);
+      epilogue_stage(a, ctl, q, lane, mb, et);
       if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag)) {
         if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
         break;
@@ -893,6 +909,49 @@ __device__ __forceinline__ void tc_st4(uint32_t taddr, const uint32_t (&r)[4]) {
                "r"(r[2]), "r"(r[3])
                : "memory");
 }
+
+// Walks the (tile, k-block) sequence of one CTA (or CTA pair) for the scale
+// warps: pa points at the k-block's A-scale word of row m0 (the first row of
+// this CTA's 128), pb at its B-scale word of column n0 + lane.  The tile
+// coordinates are derived only when the walk enters a new tile.
+struct SfCursor {
+  int tile, stride, group, mtiles, rows_per_tile, row_off, kb;
+  int64_t m0;
+  const uint32_t* pa;
+  const uint32_t* pb;
+
+  __device__ __forceinline__ void enter(const ProjArgs& a, const uint32_t* sfa, const uint32_t* sfb, int64_t N,
+                                        uint32_t lane) {
+    kb = 0;
+    if (tile >= a.num_tiles) return;
+    int mb, nb;
+    tile_coords(tile, mtiles, a.nt, group, mb, nb);
+    m0 = static_cast<int64_t>(mb) * rows_per_tile + row_off;
+    pa = sfa + m0;
+    pb = sfb + static_cast<int64_t>(nb) * BN + lane;
+  }
+  __device__ __forceinline__ void start(const ProjArgs& a, int first, int step, int grp, int mt, int rows,
+                                        int off, const uint32_t* sfa, const uint32_t* sfb, int64_t N,
+                                        uint32_t lane) {
+    tile = first;
+    stride = step;
+    group = grp;
+    mtiles = mt;
+    rows_per_tile = rows;
+    row_off = off;
+    enter(a, sfa, sfb, N, lane);
+  }
+  __device__ __forceinline__ void next(const ProjArgs& a, int nkb, const uint32_t* sfa, const uint32_t* sfb,
+                                       int64_t N, uint32_t lane) {
+    if (++kb < nkb) {
+      pa += a.M;
+      pb += N;
+      return;
+    }
+    tile += stride;
+    enter(a, sfa, sfb, N, lane);
+  }
+};
 
 // sfa: [K/128][M] words (four E8M0 bytes: the k-block's four 32-element
 // scales of a row); sfb: [K/128][N] words likewise for the rows of wkv^T.
@@ -1007,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
       int mb, nb;
       tile_coords(tile, a.mt, a.nt, kGroupM, mb, nb);
       const EpiTile et = epi_tile(a, nb);
-      epilogue_stage(a, ctl, q, lane, et);
+      epilogue_stage(a, ctl, q, lane, mb, et);
       if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), local & 1, abort_flag)) {
         if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
         break;
@@ -1023,34 +1082,30 @@ __global__ void __launch_bounds__(kThreads8, 1)
     // ---------------- scale warps (6..9): one per TMEM lane quarter.  The
     // scales of the next kSfAhead k-blocks are in flight in registers while
     // the current one is written, so the global-memory latency stays off the
-    // MMA's critical path.
+    // MMA's critical path.  A cursor walks (tile, k-block) so the tile
+    // coordinates are derived once per tile: the scale warp runs once per
+    // k-block and would otherwise pace the MMA with its integer divisions.
     constexpr int kSfAhead = 4;
     const uint32_t q = static_cast<uint32_t>(warp & 3);
     const uint32_t lane_off = (q * 32u) << 16;
     const int my_tiles = blockIdx.x < a.num_tiles ? (a.num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
     const int total = my_tiles * nkb;
+    SfCursor cur;
+    cur.start(a, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), kGroupM, a.mt, BM, 0, sfa, sfb, N, lane);
     // this k-block's scales, replicated layout: column c holds row lane + 32 c
-    auto load = [&](int it, uint32_t (&r)[12]) {
-      const int tile = static_cast<int>(blockIdx.x) + (it / nkb) * static_cast<int>(gridDim.x);
-      const int kb = it % nkb;
-      int mb, nb;
-      tile_coords(tile, a.mt, a.nt, kGroupM, mb, nb);
-      const int64_t m0 = static_cast<int64_t>(mb) * BM;
-      const int64_t n0 = static_cast<int64_t>(nb) * BN;
-      const uint32_t* pa = sfa + static_cast<int64_t>(kb) * a.M;
-      const uint32_t* pb = sfb + static_cast<int64_t>(kb) * N + n0 + lane;
+    auto load = [&](uint32_t (&r)[12]) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int64_t row = m0 + lane + 32 * c;
-        r[c] = row < a.M ? __ldg(pa + row) : 0x7f7f7f7fu;
-        r[4 + c] = __ldg(pb + 32 * c);
-        r[8 + c] = __ldg(pb + 128 + 32 * c);
+        r[c] = cur.m0 + lane + 32 * c < a.M ? __ldg(cur.pa + lane + 32 * c) : 0x7f7f7f7fu;
+        r[4 + c] = __ldg(cur.pb + 32 * c);
+        r[8 + c] = __ldg(cur.pb + 128 + 32 * c);
       }
+      cur.next(a, nkb, sfa, sfb, N, lane);
     };
     uint32_t ring[kSfAhead][12];
 #pragma unroll
     for (int u = 0; u < kSfAhead; ++u)
-      if (u < total) load(u, ring[u]);
+      if (u < total) load(ring[u]);
     bool ok = true;
     for (int base = 0; ok && base < total; base += kSfAhead) {
 #pragma unroll
@@ -1079,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl8->sf_full[s]));
-        if (it + kSfAhead < total) load(it + kSfAhead, ring[u]);
+        if (it + kSfAhead < total) load(ring[u]);
       }
     }
   }
@@ -1250,7 +1305,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
       tile_coords(tile, a.mt2, a.nt, kGroupM2, mb2, nb);
       const int mb = mb2 * 2 + static_cast<int>(rank);
       const EpiTile et = epi_tile(a, nb);
-      epilogue_stage(a, ctl, q, lane, et);
+      epilogue_stage(a, ctl, q, lane, mb, et);
       if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), local & 1, abort_flag)) {
         if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
         break;
@@ -1264,34 +1319,28 @@ __global__ void __launch_bounds__(kThreads8, 1)
     }
   } else {
     // ---------------- scale warps (6..9 of both CTAs): this CTA's 128 rows of
-    // A and all 256 rows of B, kSfAhead k-blocks in flight in registers
+    // A and all 256 rows of B, kSfAhead k-blocks in flight in registers; a
+    // cursor derives the tile coordinates once per tile (as project8_kernel)
     constexpr int kSfAhead = 4;
     const uint32_t q = static_cast<uint32_t>(warp & 3);
     const uint32_t lane_off = (q * 32u) << 16;
     const uint32_t leader_sf = map_to_cta(smem_u32(&ctl8->sf_full[0]), 0);
     const int my_tiles = pair < a.num_tiles ? (a.num_tiles - 1 - pair) / npairs + 1 : 0;
     const int total = my_tiles * nkb;
-    auto load = [&](int it, uint32_t (&r)[12]) {
-      const int tile = pair + (it / nkb) * npairs;
-      const int kb = it % nkb;
-      int mb2, nb;
-      tile_coords(tile, a.mt2, a.nt, kGroupM2, mb2, nb);
-      const int64_t m0 = static_cast<int64_t>(mb2) * (2 * BM) + static_cast<int64_t>(rank) * BM;
-      const int64_t n0 = static_cast<int64_t>(nb) * BN;
-      const uint32_t* pa = sfa + static_cast<int64_t>(kb) * a.M;
-      const uint32_t* pb = sfb + static_cast<int64_t>(kb) * N + n0 + lane;
+    SfCursor cur;
+    cur.start(a, pair, npairs, kGroupM2, a.mt2, 2 * BM, static_cast<int>(rank) * BM, sfa, sfb, N, lane);
+    auto load = [&](uint32_t (&r)[12]) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int64_t row = m0 + lane + 32 * c;
-        r[c] = row < a.M ? __ldg(pa + row) : 0x7f7f7f7fu;
-      }
+      for (int c = 0; c < 4; ++c)
+        r[c] = cur.m0 + lane + 32 * c < a.M ? __ldg(cur.pa + lane + 32 * c) : 0x7f7f7f7fu;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) r[4 + c] = __ldg(pb + 32 * c);
+      for (int c = 0; c < 8; ++c) r[4 + c] = __ldg(cur.pb + 32 * c);
+      cur.next(a, nkb, sfa, sfb, N, lane);
     };
     uint32_t ring[kSfAhead][12];
 #pragma unroll
     for (int u = 0; u < kSfAhead; ++u)
-      if (u < total) load(u, ring[u]);
+      if (u < total) load(ring[u]);
     bool ok = true;
     for (int base = 0; ok && base < total; base += kSfAhead) {
 #pragma unroll
@@ -1322,7 +1371,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
         // the TMEM writes are ordered by wait::st and the tcgen05 fence; the
         // arrive needs no cluster-scope memory fence of its own
         if (lane == 0) mbar_arrive_remote(leader_sf + static_cast<uint32_t>(s * 8));
-        if (it + kSfAhead < total) load(it + kSfAhead, ring[u]);
+        if (it + kSfAhead < total) load(ring[u]);
       }
     }
   }
