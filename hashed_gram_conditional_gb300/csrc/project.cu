@@ -163,6 +163,17 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 
+// 32 lanes x 16 columns of 32-bit TMEM words, waited for.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // ---- CTA-pair primitives
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -877,12 +888,19 @@ constexpr int A8_BYTES = BM * BK8;
 constexpr int B8_BYTES = BN * BK8;
 constexpr int STAGE8_BYTES = A8_BYTES + B8_BYTES;
 constexpr int kThreads8 = 320;  // producer, MMA, 4 epilogue, 4 scale warps
-constexpr int kSfCols = 12;     // per stage: A (4 columns), B (8 columns)
+constexpr int kSfCols = 12;     // per scale slot: A (4 columns), B (8 columns)
 constexpr int kSfBase = BN;     // scale slots after the accumulator
+// Scale slots, more than the operand stages: a slot is freed by its own
+// commit (sf_empty) once the k-block's MMAs are done, so the scale warps run
+// ahead of the operand loads and their writes are never what the MMAs wait
+// for.  TMEM: 256 + 8 x 12 (single CTA) and 256 + 12 x 12 (pair) columns.
+constexpr int kSfSlots8 = 8;
+constexpr int kSfSlots82 = 12;
 constexpr int TMEM8_COLS = 512;
 
 struct __align__(8) Ctl8 {
-  uint64_t sf_full[STAGES8];
+  uint64_t sf_full[kSfSlots8];
+  uint64_t sf_empty[kSfSlots8];
 };
 
 // kind::mxf8f6f4 instruction descriptor: A and B E4M3, K-major, N = 256,
@@ -908,6 +926,179 @@ __device__ __forceinline__ void tc_st4(uint32_t taddr, const uint32_t (&r)[4]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
                "r"(r[2]), "r"(r[3])
                : "memory");
+}
+
+// Unfused FP8 projection (partial sums of the key tiles, bf16 v): 16 warps.
+// Warp 0 loads operands, warp 1 issues the MMAs, warps 4..7 write the scale
+// factors (warp w may only reach TMEM lane quarter w & 3), warps 8..15 are
+// the epilogue, two per lane quarter (warp w: quarter w & 3, tile columns
+// half * 128 .. +127 with half = (w >> 2) & 1).  Warps 2 and 3 idle.  The
+// fused form keeps the 10-warp layout of kThreads8.
+constexpr int kThreads8u = 512;
+
+// The two halves of a key tile's partial sums meet in shared memory: the
+// second half writes its (dot, kk, hh) and arrives on its quarter's barrier
+// (32 arrivals per key tile), the first half waits, adds and stores.  Slots
+// alternate by key tile.
+struct __align__(16) Comb8 {
+  float4 v[4][2][32];
+  uint64_t bar[4];
+};
+
+// The 8-warp epilogue of the unfused FP8 kernels.  The accumulator is
+// single-buffered (TMEM also holds the scale slots), so the time from the
+// accumulator being ready to its release stalls the tensor pipe.  To keep it
+// short, a key tile's h columns are loaded into registers before the
+// accumulator is ready; once it is, the warp only reads TMEM and does the
+// arithmetic of the partial sums, then releases the accumulator; the two
+// halves are combined after that.  Returns early (after raising the abort)
+// when a bounded wait gives up.
+template <bool kPair>
+__device__ __forceinline__ void epilogue8_split(const ProjArgs& a, SmemCtl* ctl, Comb8* comb, int warp,
+                                                uint32_t lane, uint32_t tmem_base, int first, int step,
+                                                uint32_t rank, uint32_t tempty_bar,
+                                                const volatile int* abort_flag) {
+  const int q = warp & 3;
+  const int half = (warp >> 2) & 1;
+  const int cb = half * 128;
+  float* qk = ctl->qk[q] + cb;
+  const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(cb);
+  const int ntile = a.H / BN;
+  int local = 0, keys = 0;
+  for (int tile = first; tile < a.num_tiles; tile += step, ++local) {
+    int mbx, nb;
+    if (kPair)
+      tile_coords(tile, a.mt2, a.nt, kGroupM2, mbx, nb);
+    else
+      tile_coords(tile, a.mt, a.nt, kGroupM, mbx, nb);
+    const int mb = kPair ? mbx * 2 + static_cast<int>(rank) : mbx;
+    const EpiTile et = epi_tile(a, nb);
+    const int64_t t = static_cast<int64_t>(mb) * BM + q * 32 + static_cast<int>(lane);
+    const bool live = t < a.M;
+    uint4 hv[16];
+    if (et.key_tile) {
+      __syncwarp();
+      for (int c = static_cast<int>(lane); c < 128; c += 32) {
+        const int64_t idx = static_cast<int64_t>(et.c0 + cb + c) * a.hc + et.m;
+        qk[c] = __ldg(a.q_w + idx) * __ldg(a.k_w + idx);
+      }
+      __syncwarp();
+      const uint4* hrow = reinterpret_cast<const uint4*>(a.h + (t * a.hc + et.m) * a.H + et.c0 + cb);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) hv[i] = live ? __ldg(hrow + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(smem_u32(&ctl->tfull[0]), local & 1, abort_flag);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) {
+      if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+      return;
+    }
+    tc_fence_after();
+    float dot = 0.f, kk = 0.f, hh = 0.f;
+    if (et.key_tile) {
+      // even and odd columns in the two lanes of packed fp32 sums; TMEM is
+      // read 16 columns at a time, which keeps the 64 registers of h plus the
+      // working set within the 128 a thread has (spilled values would come
+      // back through L1, which the operand loads of the next tile keep busy)
+      uint64_t d2 = f2(0.f, 0.f), k2s = f2(0.f, 0.f), h2s = f2(0.f, 0.f);
+#pragma unroll
+      for (int c16 = 0; c16 < 8; ++c16) {
+        uint32_t r[16];
+        __syncwarp();
+        tc_ld16(taddr + c16 * 16, r);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint4 hq = hv[c16 * 2 + i];
+          const uint32_t w4[4] = {hq.x, hq.y, hq.z, hq.w};
+          const float4 qa = *reinterpret_cast<const float4*>(qk + c16 * 16 + i * 8);
+          const float4 qb = *reinterpret_cast<const float4*>(qk + c16 * 16 + i * 8 + 4);
+          const uint64_t q2[4] = {f2(qa.x, qa.y), f2(qa.z, qa.w), f2(qb.x, qb.y), f2(qb.z, qb.w)};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t h2 = f2(bf16f(w4[j] & 0xffffu), bf16f(w4[j] >> 16));
+            const uint64_t k2 = f2(__uint_as_float(r[i * 8 + j * 2]), __uint_as_float(r[i * 8 + j * 2 + 1]));
+            d2 = f2_fma(f2_mul(h2, q2[j]), k2, d2);
+            k2s = f2_fma(k2, k2, k2s);
+            h2s = f2_fma(h2, h2, h2s);
+          }
+        }
+      }
+      float lo, hi;
+      f2_split(d2, lo, hi);
+      dot = lo + hi;
+      f2_split(k2s, lo, hi);
+      kk = lo + hi;
+      f2_split(h2s, lo, hi);
+      hh = lo + hi;
+    } else {
+      // v rounded to bf16, 16 columns at a time, turned through the warp's
+      // 1-KB staging area (32 rows x 32 B, 16-byte halves swapped on every
+      // other group of 4 rows against bank conflicts) so that two lanes write
+      // each row's 32 contiguous bytes
+      uint4* stage = reinterpret_cast<uint4*>(&ctl->sv[0][0][0]) + (warp - 8) * 64;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t r[32];
+        __syncwarp();
+        tc_ld32(taddr + ch * 32, r);
+#pragma unroll
+        for (int hx = 0; hx < 2; ++hx) {
+#pragma unroll
+          for (int sg = 0; sg < 2; ++sg) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[hx * 16 + sg * 8 + j * 2]),
+                                                       __uint_as_float(r[hx * 16 + sg * 8 + j * 2 + 1]));
+              pk[j] = *reinterpret_cast<uint32_t*>(&b);
+            }
+            stage[lane * 2 + (sg ^ ((lane >> 2) & 1))] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int rl = k * 16 + static_cast<int>(lane >> 1);
+            const int sg = static_cast<int>(lane & 1);
+            const uint4 x = stage[rl * 2 + (sg ^ ((rl >> 2) & 1))];
+            const int64_t tr = static_cast<int64_t>(mb) * BM + q * 32 + rl;
+            if (tr < a.M)
+              *reinterpret_cast<uint4*>(a.v + tr * a.H + et.c0 + cb + ch * 32 + hx * 16 + sg * 8) = x;
+          }
+          __syncwarp();
+        }
+      }
+    }
+    float4* slot = &comb->v[q][keys & 1][lane];
+    if (et.key_tile && half == 1) {
+      *slot = make_float4(dot, kk, hh, 0.f);
+      mbar_arrive(smem_u32(&comb->bar[q]));
+    }
+    if (et.key_tile && half == 0) {
+      // the other half's sums; it releases the accumulator without waiting
+      if (lane == 0) ok = mbar_wait_bounded(smem_u32(&comb->bar[q]), keys & 1, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) {
+        if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+        return;
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (kPair)
+        mbar_arrive_cluster(tempty_bar);
+      else
+        mbar_arrive(tempty_bar);
+    }
+    if (et.key_tile) {
+      if (half == 0 && live) {
+        const float4 o = *slot;
+        a.partials[(t * a.hc + et.m) * ntile + et.c0 / BN] = make_float4(dot + o.x, kk + o.y, hh + o.z, 0.f);
+      }
+      ++keys;
+    }
+  }
 }
 
 // Walks the (tile, k-block) sequence of one CTA (or CTA pair) for the scale
@@ -956,7 +1147,7 @@ struct SfCursor {
 // sfa: [K/128][M] words (four E8M0 bytes: the k-block's four 32-element
 // scales of a row); sfb: [K/128][N] words likewise for the rows of wkv^T.
 template <bool kFuse>
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
     project8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ProjArgs a,
                     const uint32_t* __restrict__ sfa, const uint32_t* __restrict__ sfb) {
   extern __shared__ uint8_t smem_raw[];
@@ -965,6 +1156,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
   uint8_t* smB = smem + STAGES8 * A8_BYTES;
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + STAGES8 * STAGE8_BYTES);
   Ctl8* ctl8 = reinterpret_cast<Ctl8*>(ctl + 1);
+  Comb8* comb = reinterpret_cast<Comb8*>((reinterpret_cast<uintptr_t>(ctl8 + 1) + 15) & ~uintptr_t(15));
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const int nkb = a.K / BK8;
@@ -975,10 +1167,15 @@ __global__ void __launch_bounds__(kThreads8, 1)
     for (int s = 0; s < STAGES8; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
-      mbar_init(smem_u32(&ctl8->sf_full[s]), 4);
+    }
+    for (int j = 0; j < kSfSlots8; ++j) {
+      mbar_init(smem_u32(&ctl8->sf_full[j]), 4);
+      mbar_init(smem_u32(&ctl8->sf_empty[j]), 1);
     }
     mbar_init(smem_u32(&ctl->tfull[0]), 1);
-    mbar_init(smem_u32(&ctl->tempty[0]), 4);
+    mbar_init(smem_u32(&ctl->tempty[0]), kFuse ? 4 : 8);
+    if (!kFuse)
+      for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&comb->bar[qq]), 32);
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -1037,8 +1234,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % STAGES8;
           const uint32_t ph = (it / STAGES8) & 1;
+          const int j = it % kSfSlots8;
           if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag) ||
-              !mbar_wait_bounded(smem_u32(&ctl8->sf_full[s]), ph, abort_flag)) {
+              !mbar_wait_bounded(smem_u32(&ctl8->sf_full[j]), (it / kSfSlots8) & 1, abort_flag)) {
             if (!*abort_flag) raise_abort(ctl, a);
             ok = false;
             break;
@@ -1046,39 +1244,45 @@ __global__ void __launch_bounds__(kThreads8, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(smA + s * A8_BYTES);
           const uint32_t b0 = smem_u32(smB + s * B8_BYTES);
-          const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + s * kSfCols);
+          const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + j * kSfCols);
 #pragma unroll
           for (int k = 0; k < BK8 / 32; ++k)
             tc_mma8(tmem_base, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc8(static_cast<uint32_t>(k)), sf,
                     sf + 4u, (kb | k) != 0 ? 1u : 0u);
           tc_commit(smem_u32(&ctl->empty[s]));
+          tc_commit(smem_u32(&ctl8->sf_empty[j]));
         }
         if (ok) tc_commit(smem_u32(&ctl->tfull[0]));
       }
       tc_commit(smem_u32(&ctl->drain));
       mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr);
     }
-  } else if (warp < 6) {
-    // ---------------- epilogue (warps 2..5)
-    const int q = warp & 3;
-    int local = 0;
-    for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++local) {
-      int mb, nb;
-      tile_coords(tile, a.mt, a.nt, kGroupM, mb, nb);
-      const EpiTile et = epi_tile(a, nb);
-      epilogue_stage(a, ctl, q, lane, mb, et);
-      if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), local & 1, abort_flag)) {
-        if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
-        break;
+  } else if (kFuse ? warp < 6 : warp >= 8) {
+    if constexpr (!kFuse) {
+      epilogue8_split<false>(a, ctl, comb, warp, lane, tmem_base, static_cast<int>(blockIdx.x),
+                             static_cast<int>(gridDim.x), 0, smem_u32(&ctl->tempty[0]), abort_flag);
+    } else {
+      // ---------------- epilogue (warps 2..5)
+      const int q = warp & 3;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++local) {
+        int mb, nb;
+        tile_coords(tile, a.mt, a.nt, kGroupM, mb, nb);
+        const EpiTile et = epi_tile(a, nb);
+        epilogue_stage(a, ctl, q, lane, mb, et);
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), local & 1, abort_flag)) {
+          if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        if (!epilogue_tile<kFuse>(a, ctl, q, lane, taddr, mb, et, abort_flag)) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[0]));
       }
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      if (!epilogue_tile<kFuse>(a, ctl, q, lane, taddr, mb, et, abort_flag)) break;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[0]));
     }
-  } else {
+  } else if (kFuse || warp >= 4) {
     // ---------------- scale warps (6..9): one per TMEM lane quarter.  The
     // scales of the next kSfAhead k-blocks are in flight in registers while
     // the current one is written, so the global-memory latency stays off the
@@ -1112,10 +1316,10 @@ __global__ void __launch_bounds__(kThreads8, 1)
       for (int u = 0; u < kSfAhead; ++u) {
         const int it = base + u;
         if (it >= total) break;
-        const int s = it % STAGES8;
-        const uint32_t ph = (it / STAGES8) & 1;
+        const int s = it % kSfSlots8;
+        const uint32_t ph = (it / kSfSlots8) & 1;
         bool free_slot = true;
-        if (lane == 0) free_slot = mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag);
+        if (lane == 0) free_slot = mbar_wait_bounded(smem_u32(&ctl8->sf_empty[s]), ph ^ 1, abort_flag);
         free_slot = __shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0) != 0;
         if (!free_slot) {
           if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
@@ -1163,7 +1367,8 @@ constexpr int B82_BYTES = (BN / 2) * BK8;
 constexpr int STAGE82_BYTES = A8_BYTES + B82_BYTES;
 
 struct __align__(8) Ctl82 {
-  uint64_t sf_full[STAGES82];
+  uint64_t sf_full[kSfSlots82];
+  uint64_t sf_empty[kSfSlots82];
 };
 
 __device__ __forceinline__ void tc_mma8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -1184,7 +1389,7 @@ __device__ __forceinline__ uint32_t idesc82(uint32_t sf_id) {
 }
 
 template <bool kFuse>
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
     project82_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ProjArgs a,
                      const uint32_t* __restrict__ sfa, const uint32_t* __restrict__ sfb) {
   extern __shared__ uint8_t smem_raw[];
@@ -1193,6 +1398,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
   uint8_t* smB = smem + STAGES82 * A8_BYTES;
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + STAGES82 * STAGE82_BYTES);
   Ctl82* ctl8 = reinterpret_cast<Ctl82*>(ctl + 1);
+  Comb8* comb = reinterpret_cast<Comb8*>((reinterpret_cast<uintptr_t>(ctl8 + 1) + 15) & ~uintptr_t(15));
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const uint32_t rank = cluster_rank();
@@ -1206,10 +1412,15 @@ __global__ void __launch_bounds__(kThreads8, 1)
     for (int s = 0; s < STAGES82; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
-      mbar_init(smem_u32(&ctl8->sf_full[s]), 8);
+    }
+    for (int j = 0; j < kSfSlots82; ++j) {
+      mbar_init(smem_u32(&ctl8->sf_full[j]), 8);
+      mbar_init(smem_u32(&ctl8->sf_empty[j]), 1);
     }
     mbar_init(smem_u32(&ctl->tfull[0]), 1);
-    mbar_init(smem_u32(&ctl->tempty[0]), 8);
+    mbar_init(smem_u32(&ctl->tempty[0]), kFuse ? 8 : 16);
+    if (!kFuse)
+      for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&comb->bar[qq]), 32);
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -1274,8 +1485,9 @@ __global__ void __launch_bounds__(kThreads8, 1)
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % STAGES82;
           const uint32_t ph = (it / STAGES82) & 1;
+          const int j = it % kSfSlots82;
           if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag) ||
-              !mbar_wait_bounded(smem_u32(&ctl8->sf_full[s]), ph, abort_flag)) {
+              !mbar_wait_bounded(smem_u32(&ctl8->sf_full[j]), (it / kSfSlots82) & 1, abort_flag)) {
             if (!*abort_flag) raise_abort(ctl, a);
             ok = false;
             break;
@@ -1283,41 +1495,47 @@ __global__ void __launch_bounds__(kThreads8, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(smA + s * A8_BYTES);
           const uint32_t b0 = smem_u32(smB + s * B82_BYTES);
-          const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + s * kSfCols);
+          const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + j * kSfCols);
 #pragma unroll
           for (int k = 0; k < BK8 / 32; ++k)
             tc_mma8_pair(tmem_base, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc82(static_cast<uint32_t>(k)),
                          sf, sf + 4u, (kb | k) != 0 ? 1u : 0u);
           tc_commit_pair(smem_u32(&ctl->empty[s]));
+          tc_commit_pair(smem_u32(&ctl8->sf_empty[j]));
         }
         if (ok) tc_commit_pair(smem_u32(&ctl->tfull[0]));
       }
       tc_commit_pair(smem_u32(&ctl->drain));
       mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr);
     }
-  } else if (warp < 6) {
-    // ---------------- epilogue (warps 2..5 of both CTAs; each its own 128 rows)
-    const int q = warp & 3;
-    const uint32_t leader_tempty = map_to_cta(smem_u32(&ctl->tempty[0]), 0);
-    int local = 0;
-    for (int tile = pair; tile < a.num_tiles; tile += npairs, ++local) {
-      int mb2, nb;
-      tile_coords(tile, a.mt2, a.nt, kGroupM2, mb2, nb);
-      const int mb = mb2 * 2 + static_cast<int>(rank);
-      const EpiTile et = epi_tile(a, nb);
-      epilogue_stage(a, ctl, q, lane, mb, et);
-      if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), local & 1, abort_flag)) {
-        if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
-        break;
+  } else if (kFuse ? warp < 6 : warp >= 8) {
+    if constexpr (!kFuse) {
+      epilogue8_split<true>(a, ctl, comb, warp, lane, tmem_base, pair, npairs, rank,
+                            map_to_cta(smem_u32(&ctl->tempty[0]), 0), abort_flag);
+    } else {
+      // ---------------- epilogue (warps 2..5 of both CTAs; each its own 128 rows)
+      const int q = warp & 3;
+      const uint32_t leader_tempty = map_to_cta(smem_u32(&ctl->tempty[0]), 0);
+      int local = 0;
+      for (int tile = pair; tile < a.num_tiles; tile += npairs, ++local) {
+        int mb2, nb;
+        tile_coords(tile, a.mt2, a.nt, kGroupM2, mb2, nb);
+        const int mb = mb2 * 2 + static_cast<int>(rank);
+        const EpiTile et = epi_tile(a, nb);
+        epilogue_stage(a, ctl, q, lane, mb, et);
+        if (!mbar_wait_bounded(smem_u32(&ctl->tfull[0]), local & 1, abort_flag)) {
+          if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        if (!epilogue_tile<kFuse>(a, ctl, q, lane, taddr, mb, et, abort_flag)) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(leader_tempty);
       }
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      if (!epilogue_tile<kFuse>(a, ctl, q, lane, taddr, mb, et, abort_flag)) break;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_tempty);
     }
-  } else {
+  } else if (kFuse || warp >= 4) {
     // ---------------- scale warps (6..9 of both CTAs): this CTA's 128 rows of
     // A and all 256 rows of B, kSfAhead k-blocks in flight in registers; a
     // cursor derives the tile coordinates once per tile (as project8_kernel)
@@ -1347,10 +1565,10 @@ __global__ void __launch_bounds__(kThreads8, 1)
       for (int u = 0; u < kSfAhead; ++u) {
         const int it = base + u;
         if (it >= total) break;
-        const int s = it % STAGES82;
-        const uint32_t ph = (it / STAGES82) & 1;
+        const int s = it % kSfSlots82;
+        const uint32_t ph = (it / kSfSlots82) & 1;
         bool free_slot = true;
-        if (lane == 0) free_slot = mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1, abort_flag);
+        if (lane == 0) free_slot = mbar_wait_bounded(smem_u32(&ctl8->sf_empty[s]), ph ^ 1, abort_flag);
         free_slot = __shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0) != 0;
         if (!free_slot) {
           if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
@@ -1704,8 +1922,9 @@ int prepare8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64
 }
 
 size_t project8_smem_bytes(bool pair) {
-  return pair ? 1024 + STAGES82 * STAGE82_BYTES + sizeof(SmemCtl) + sizeof(Ctl82)
-              : 1024 + STAGES8 * STAGE8_BYTES + sizeof(SmemCtl) + sizeof(Ctl8);
+  return (pair ? 1024 + STAGES82 * STAGE82_BYTES + sizeof(SmemCtl) + sizeof(Ctl82)
+               : 1024 + STAGES8 * STAGE8_BYTES + sizeof(SmemCtl) + sizeof(Ctl8)) +
+         16 + sizeof(Comb8);
 }
 
 int launch8(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB, const ProjArgs& a,
@@ -1721,7 +1940,8 @@ int launch8(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tm
   int rc = check_device(&sms);
   if (rc) return rc;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads8);
+  const int threads = fused ? kThreads8 : kThreads8u;
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -1741,7 +1961,7 @@ int launch8(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tm
       return fail(ENGRAM_E_CUDA, "no resident CTA pair for the FP8 projection: %s", cudaGetErrorString(err));
   } else {
     int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads8, smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
     if (err != cudaSuccess || per_sm < 1)
       return fail(ENGRAM_E_CUDA, "no resident CTA for the FP8 projection: %s", cudaGetErrorString(err));
     units = sms * per_sm;

@@ -67,36 +67,10 @@ __device__ __forceinline__ float silu(float x) {
   return x * r;
 }
 
-// Pairs of fp32 values in one 64-bit register pair, for the packed
-// two-lane fp32 instructions of sm_100+ (add/mul/fma .rn.f32x2): each lane
-// is the IEEE round-to-nearest result of the scalar operation, so the packed
-// code computes exactly what the scalar code does, in half the instructions.
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_split(uint64_t x, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-}
 __device__ __forceinline__ uint64_t f2_bf16(uint32_t w) {  // the two bf16 of a word, widened
   return f2(bf16_lo(w), bf16_hi(w));
 }
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
+
 // silu of both lanes, as silu() above
 __device__ __forceinline__ uint64_t silu2(uint64_t x) {
   float m0, m1, e0, e1, d0, d1, r0, r1;
