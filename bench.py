@@ -44,6 +44,7 @@ GATHER_BYTES_PER_TOKEN = 4 + 24 * 264 + 24 * 256 * 2   # raw id + 24 rows + bf16
 KERNEL_SOURCES = {
     "project2_kernel": ["project.cu", "engram_internal.h"],
     "project2_kernel_unfused": ["project.cu", "engram_internal.h"],
+    "project8_kernel_unfused": ["project.cu", "engram_internal.h"],
     "gather_ldgsts_kernel": ["gather.cu", "hash_device.cuh", "engram_internal.h"],
     "gather_ldgsts_kernel_ids": ["gather.cu", "hash_device.cuh", "engram_internal.h"],
     "hash_prefill_kernel": ["hash.cu", "hash_device.cuh", "engram_internal.h"],
@@ -361,7 +362,8 @@ def run_ours(args, rank, world, local):
                            "achieved": fp8["project_tflops"], "peak": pk, "unit": "TFLOP/s",
                            "frac": fp8["project_tflops"] / pk,
                            "peak_source": f"{peak_src} bf16_tflops{'_sustained' if fp8_sust else ''} x 2 "
-                                          "(nominal fp8 / bf16 dense ratio)"}
+                                          "(nominal fp8 / bf16 dense ratio)",
+                           "traffic": traffic.get("project8_kernel_unfused")}
     if conv is not None:
         conv["conv_frac_hbm"] = conv["conv_gbs"] / peaks["hbm_gbs"]
         conv["traffic_conv_add"] = traffic.get("conv_add_kernel")

@@ -871,17 +871,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // of k on both operands, fp32 accumulation), so there is no bf16 e at all.
 //
 // One CTA per 128 x 256 tile (one M = 128, N = 256 MMA per K = 32 step),
-// k-blocks of 128 bytes (four steps), 4 stages of 48 KB.  The scale factors do not go
-// through TMA: four "scale" warps (one per TMEM lane quarter) read each
-// k-block's scales from global memory and write them to a per-stage TMEM slot
-// with tcgen05.st in the layout the MMA reads -- lane L, column c, byte k
-// holds the scale of row (L mod 32) + 32 c for k-step k (c < 4 for the 128
+// k-blocks of 128 bytes (four steps), 4 stages of 48 KB.  The scale factors
+// do not go through TMA: four "scale" warps (one per TMEM lane quarter) read
+// each k-block's scales from global memory and write them to a TMEM scale
+// slot with tcgen05.st in the layout the MMA reads -- lane L, column c, byte
+// k holds the scale of row (L mod 32) + 32 c for k-step k (c < 4 for the 128
 // rows of A, c < 8 for the 256 rows of B), replicated in every lane quarter
-// (established on GB300 by a standalone probe).  The slot of a
-// stage is rewritten only after the MMAs that read it have completed (the
-// stage's "empty" barrier).  TMEM: the 256-column accumulator plus 4 x 12
-// scale columns, so the accumulator is single-buffered and the epilogue does
-// not overlap the next tile's main loop.  Epilogues are the bf16 kernels'.
+// (established on GB300 by a standalone probe).  A slot is rewritten only
+// after the MMAs that read it have completed (its own sf_empty commit).
+// TMEM: the 256-column accumulator plus the scale slots, which leaves no
+// room for a second accumulator: the epilogue stalls the tensor pipe from
+// the last MMA of a tile to the accumulator's release, so the unfused form
+// keeps that window short (epilogue8_split).  The fused form reuses the bf16
+// kernels' epilogue.
 constexpr int BK8 = 128;  // bytes = elements per k-block
 constexpr int STAGES8 = 4;
 constexpr int A8_BYTES = BM * BK8;
@@ -1868,9 +1870,11 @@ int launch(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB
   return check_launch("project kernel");
 }
 
-// The single-CTA FP8 kernel is the default: under the GB300 power cap it runs
-// the layer slightly faster than the CTA pair (3.12 vs 3.21 ms on 16,384
-// tokens), as both keep a single accumulator buffer.  ENGRAM_FP8_PAIR=1
+// The single-CTA FP8 kernel is the default.  The CTA pair moves a third fewer
+// operand bytes per SM, but the per-SM MMA rate is the same (an M = 256 pair
+// MMA takes as many cycles as an M = 128 one), its two CTAs gate each other
+// at every k-block, and both keep a single accumulator: on 16,384 tokens the
+// two measure within 2 % of each other (1.94-1.98 ms).  ENGRAM_FP8_PAIR=1
 // selects the pair.
 bool use_fp8_pair() {
   static const bool v = [] {
