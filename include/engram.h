@@ -111,7 +111,7 @@ typedef struct engram_layout {
  * one prime per head, never reused; the printed per-layer min/max/sum for
  * layers 1 and 14) and [P-O1] §2.2 (one ascending sequence consumed in
  * (layer, order, head) order; primality by deterministic Miller-Rabin).
- * This build takes the primes strictly greater than base_rows.
+ * The library takes the primes strictly greater than base_rows.
  * Offsets: [P-O1] §2.2 / [P-DS4] §布局与哈希探测 step 3 (cumulative sum).
  * Multipliers: [P-V41] §"哈希函数" under eq. (H) and [P-O1] §4.3 -- per
  * layer, odd, drawn from a generator seeded with 10007 * layer_id and bounded
@@ -440,7 +440,7 @@ int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t 
  * ([P-V41] §门控 and §"sigmoid 之前多一步带符号的平方根"; [P-DS4] §消费).
  * Masked positions (mask_d[t] != 0) leave h_d untouched and get g = 0
  * ([P-V41] image tokens; [P-DS4] step 4: the masked branch returns).
- * score_scale is H^-0.5 in this build's reading of the pages ([P-V41]
+ * score_scale is H^-0.5, the reading of the pages the library follows ([P-V41]
  * derives s = sqrt(d) cos(theta); [P-DS4] prints a sqrt(width) factor).
  *
  *   partials_d   from engram_project
