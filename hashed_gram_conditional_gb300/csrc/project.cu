@@ -1113,7 +1113,7 @@ struct SfCursor {
   const uint32_t* pa;
   const uint32_t* pb;
 
-  __device__ __forceinline__ void enter(const ProjArgs& a, const uint32_t* sfa, const uint32_t* sfb, int64_t N,
+  __device__ __forceinline__ void enter(const ProjArgs& a, const uint32_t* sfa, const uint32_t* sfb,
                                         uint32_t lane) {
     kb = 0;
     if (tile >= a.num_tiles) return;
@@ -1124,15 +1124,14 @@ struct SfCursor {
     pb = sfb + static_cast<int64_t>(nb) * BN + lane;
   }
   __device__ __forceinline__ void start(const ProjArgs& a, int first, int step, int grp, int mt, int rows,
-                                        int off, const uint32_t* sfa, const uint32_t* sfb, int64_t N,
-                                        uint32_t lane) {
+                                        int off, const uint32_t* sfa, const uint32_t* sfb, uint32_t lane) {
     tile = first;
     stride = step;
     group = grp;
     mtiles = mt;
     rows_per_tile = rows;
     row_off = off;
-    enter(a, sfa, sfb, N, lane);
+    enter(a, sfa, sfb, lane);
   }
   __device__ __forceinline__ void next(const ProjArgs& a, int nkb, const uint32_t* sfa, const uint32_t* sfb,
                                        int64_t N, uint32_t lane) {
@@ -1142,7 +1141,7 @@ struct SfCursor {
       return;
     }
     tile += stride;
-    enter(a, sfa, sfb, N, lane);
+    enter(a, sfa, sfb, lane);
   }
 };
 
@@ -1297,7 +1296,7 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
     const int my_tiles = blockIdx.x < a.num_tiles ? (a.num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
     const int total = my_tiles * nkb;
     SfCursor cur;
-    cur.start(a, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), kGroupM, a.mt, BM, 0, sfa, sfb, N, lane);
+    cur.start(a, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), kGroupM, a.mt, BM, 0, sfa, sfb, lane);
     // this k-block's scales, replicated layout: column c holds row lane + 32 c
     auto load = [&](uint32_t (&r)[12]) {
 #pragma unroll
@@ -1548,7 +1547,7 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
     const int my_tiles = pair < a.num_tiles ? (a.num_tiles - 1 - pair) / npairs + 1 : 0;
     const int total = my_tiles * nkb;
     SfCursor cur;
-    cur.start(a, pair, npairs, kGroupM2, a.mt2, 2 * BM, static_cast<int>(rank) * BM, sfa, sfb, N, lane);
+    cur.start(a, pair, npairs, kGroupM2, a.mt2, 2 * BM, static_cast<int>(rank) * BM, sfa, sfb, lane);
     auto load = [&](uint32_t (&r)[12]) {
 #pragma unroll
       for (int c = 0; c < 4; ++c)
