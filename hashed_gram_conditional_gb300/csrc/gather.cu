@@ -99,7 +99,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_dequant_kernel(GatherAr
   fence_mbar_init();
   __syncwarp();
 
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + w;
+  // warps numbered CTA-minor, so a small batch (a decode step) spreads over
+  // every CTA of the grid rather than filling the first few
+  const int64_t gw = static_cast<int64_t>(w) * gridDim.x + blockIdx.x;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
   const int n_cols = a.n_cols;
 
@@ -334,7 +336,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArg
   fence_mbar_init();
   __syncwarp();
 
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + w;
+  // warps numbered CTA-minor, so a small batch (a decode step) spreads over
+  // every CTA of the grid rather than filling the first few
+  const int64_t gw = static_cast<int64_t>(w) * gridDim.x + blockIdx.x;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
   const int n_cols = a.n_cols;
   const int pieces = n_cols * 17;
@@ -459,8 +463,8 @@ int launch_ldgsts(const GatherArgs& a, const RowSource& src, const Out& out, siz
   cudaError_t err = cudaFuncSetAttribute(gather_ldgsts_kernel<RowSource, Out>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(gather): %s", cudaGetErrorString(err));
-  const int64_t want = (a.n_tokens + kWarps - 1) / kWarps;
-  const int blocks = static_cast<int>(want < sms ? want : sms);
+  // one CTA per SM, or one per position when there are fewer positions
+  const int blocks = static_cast<int>(a.n_tokens < sms ? a.n_tokens : sms);
   gather_ldgsts_kernel<RowSource, Out><<<blocks, kWarps * 32, smem, st>>>(a, src, out);
   return check_launch("gather_ldgsts_kernel");
 }
@@ -492,8 +496,7 @@ extern "C" int engram_gather_dequant(const uint8_t* table_d, int64_t total_rows,
                                          227 * 1024);
   if (err != cudaSuccess)
     return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(gather): %s", cudaGetErrorString(err));
-  const int64_t want = (n_tokens + kWarps - 1) / kWarps;
-  const int blocks = static_cast<int>(want < sms ? want : sms);
+  const int blocks = static_cast<int>(n_tokens < sms ? n_tokens : sms);
   gather_dequant_kernel<<<blocks, kWarps * 32, smem, as_stream(stream)>>>(a);
   return check_launch("gather_dequant_kernel");
 }
