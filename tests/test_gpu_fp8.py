@@ -117,9 +117,9 @@ def _fp8_layer_case(name, T_cut=None, seed=0, sample=None):
     g = OG.gate(hf, k, lw.q_w, lw.k_w, mask_o[idx])
     out = OG.residual(hf, g, v, mask_o[idx])
     assert np.abs(gate.cpu().numpy()[idx] - g).max() <= GATE_ATOL
-    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h)[idx]), out, hf, g, v,
+    r = residual_close(bf16_bits_to_f64(bits(h)[idx]), out, hf, g, v,
                                        dot_error_bound(e, W[:, w.hc * w.hidden:]))
-    assert ok, (worst, strict)
+    assert r.ok, r
 
 
 @pytest.mark.parametrize("T", [128, 300, 1])
@@ -130,7 +130,7 @@ def test_fp8_layer_two_kernel_path(T):
 
 def test_fp8_layer_1700_tokens():
     """1700 tokens (ragged M tail): the FP8 projection and the gate kernel, or the
-    fused cooperative FP8 kernel when ENGRAM_FP8_FUSED=1."""
+    fused cooperative FP8 kernel when engram_kernel_options.fp8_fused is set."""
     _fp8_layer_case("tiny", T_cut=1700, seed=1)
 
 
@@ -179,9 +179,9 @@ def test_engram_layer_with_fp8_weights_prefill_and_decode():
     g = OG.gate(hf, k, lw.q_w, lw.k_w, mask_o)
     out = OG.residual(hf, g, v, mask_o)
     assert np.abs(gate.cpu().numpy() - g).max() <= GATE_ATOL
-    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h)), out, hf, g, v,
+    r = residual_close(bf16_bits_to_f64(bits(h)), out, hf, g, v,
                                        dot_error_bound(e, W[:, w.hc * w.hidden:]))
-    assert ok, (worst, strict)
+    assert r.ok, r
     # decode: the layer against the direct calls, from the same history
     slots = i32(np.array([2, 0, 1], dtype=np.int32))
     hist_d = hist.clone()

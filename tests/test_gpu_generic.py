@@ -82,9 +82,9 @@ def test_layer_2_3_grams_16_columns_hidden_2560(T):
     g = OG.gate(hf, k, lw.q_w, lw.k_w, mask_o[idx])
     out = OG.residual(hf, g, v, mask_o[idx])
     assert np.abs(gate.cpu().numpy()[idx] - g).max() <= GATE_ATOL
-    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v,
+    r = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v,
                                        dot_error_bound(e, W[:, w.hc * w.hidden:]))
-    assert ok, (worst, strict)
+    assert r.ok, r
 
 
 def _bf16_table(total, row_dim, seed):
@@ -164,6 +164,6 @@ def test_engram_27b_shaped_layer_with_80_dim_bf16_rows(T):
     g = OG.gate(hf, k, lw.q_w, lw.k_w, mask_o[idx])
     out = OG.residual(hf, g, v, mask_o[idx])
     assert np.abs(gate.cpu().numpy()[idx] - g).max() <= GATE_ATOL
-    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v,
+    r = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v,
                                        dot_error_bound(e, W[:, w.hc * w.hidden:]))
-    assert ok, (worst, strict)
+    assert r.ok, r

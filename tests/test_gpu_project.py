@@ -5,7 +5,7 @@ import torch
 
 import hashed_gram_conditional_gb300 as eg
 from gpu_util import (DEV, GATE_ATOL, bf16, bits, dot_error_bound, f32, i32, require_gpu, residual_close,
-                      status, u8)
+                      status, u8, v_flips_explained)
 from oracle import dequant as OD
 from oracle import gate as OG
 from workloads import bf16_bits_to_f64, normal_bf16_bits, uniform_f32
@@ -55,11 +55,12 @@ def test_project_partials_v_gate_residual(T, H, hc):
     partials, v_d = eg.engram_project(bf16(e), wp, h_d, f32(qw), f32(kw), status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    # v: fp32 accumulation then one bf16 rounding; the oracle rounds the exact value
+    # v: fp32 accumulation then one bf16 rounding; the oracle rounds the exact
+    # value.  Bit-equal except where the exact v is within the accumulation
+    # bound of a bf16 midpoint, and there one bf16 step away at most.
     vb = bf16_bits_to_f64(bits(v_d))
-    vr = OD.bf16_round(v)
     assert (np.abs(vb - v) <= 2.0 ** -8 * np.abs(v) + v_err).all()   # one bf16 rounding + fp32 sum
-    assert np.mean(vb == vr) > 0.9
+    v_flips_explained(bits(v_d), v, v_err)
     # partials per 256-column tile
     P = partials.cpu().numpy().astype(np.float64)
     ntile = H // 256
@@ -82,8 +83,8 @@ def test_project_partials_v_gate_residual(T, H, hc):
     assert (gg[mask] == 0).all()
     hb = bits(h_d)
     assert (hb[mask] == h[mask]).all()                     # masked rows bit-identical
-    ok, worst, strict = residual_close(bf16_bits_to_f64(hb), out, hf, g, v, v_err)
-    assert ok, (worst, strict)
+    r = residual_close(bf16_bits_to_f64(hb), out, hf, g, v, v_err)
+    assert r.ok, r
 
 
 def test_project_identity_selects_rows():
@@ -117,8 +118,8 @@ def test_project_large_m_tiles():
     idx = np.array([0, 1, 127, 128, 500, 1023])
     k, v, hf, g, out, k_err, v_err = _oracle(e[idx], w, h[idx], qw, kw, mask[idx], len(idx), H, hc)
     assert np.abs(gate.cpu().numpy()[idx] - g).max() <= GATE_ATOL
-    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
-    assert ok, (worst, strict)
+    r = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
+    assert r.ok, r
 
 
 def _assert_same_update(hu_bits, hb_bits, g_u, v_u, g_b=None, v_err=None):
@@ -165,8 +166,8 @@ def test_project_gate_fused(T, H, hc):
     assert (gf[mask] == 0).all()
     hb = bits(h_f)
     assert (hb[mask] == h[mask]).all()
-    ok, worst, strict = residual_close(bf16_bits_to_f64(hb), out, hf, g, v, v_err)
-    assert ok, (worst, strict)
+    r = residual_close(bf16_bits_to_f64(hb), out, hf, g, v, v_err)
+    assert r.ok, r
     # unfused kernels on the same inputs: gates agree to fp32 summation order
     h_u = bf16(h)
     g_u = torch.empty((T, hc), dtype=torch.float32, device=DEV)
@@ -192,8 +193,8 @@ def test_project_gate_fused_many_groups():
     idx = np.array([0, 3, 127, 128, 2047, 2048, 2049, 4095, 4096, 4131, 4132])
     k, v, hf, g, out, k_err, v_err = _oracle(e[idx], w, h[idx], qw, kw, mask[idx], len(idx), H, hc)
     assert np.abs(gate.cpu().numpy()[idx] - g).max() <= GATE_ATOL
-    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
-    assert ok, (worst, strict)
+    r = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
+    assert r.ok, r
     assert (bits(h_d)[mask] == h[mask]).all()
 
 
@@ -219,8 +220,8 @@ def test_project_gate_decode_shape(T, H):
     idx = np.unique(np.concatenate([np.arange(0, T, 16), [1, T - 2, T - 1]]))
     k, v, hf, g, out, k_err, v_err = _oracle(e[idx], w, h[idx], qw, kw, mask[idx], len(idx), H, hc)
     assert np.abs(gate.cpu().numpy()[idx] - g).max() <= GATE_ATOL
-    ok, worst, strict = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
-    assert ok, (worst, strict)
+    r = residual_close(bf16_bits_to_f64(bits(h_d)[idx]), out, hf, g, v, v_err)
+    assert r.ok, r
     assert (bits(h_d)[mask] == h[mask]).all()
     h_u = bf16(h)
     g_u = torch.empty((T, hc), dtype=torch.float32, device=DEV)
