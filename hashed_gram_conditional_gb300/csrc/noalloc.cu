@@ -15,6 +15,7 @@
 // share it, so calls that overlap on the GPU (on different streams, or from
 // different threads without ordering) race on it.  Each call writes every
 // scratch element it later reads, so nothing needs clearing between calls.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -35,21 +36,65 @@ __device__ __align__(256) unsigned char g_stage_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {nullptr};
+unsigned long long g_ctx_id[kMaxDevices] = {0};
 
-// Device address of g_stage_scratch on the current device, looked up once per
-// device (with that device current) on the first call made there.
+// Driver calls reached through the runtime's entry-point query, so the
+// library needs no link against libcuda.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+int driver_fn(const char* name, void** fn) {
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t err = cudaGetDriverEntryPointByVersion(name, fn, 12000, cudaEnableDefault, &q);
+  if (err != cudaSuccess || q != cudaDriverEntryPointSuccess || *fn == nullptr)
+    return fail(ENGRAM_E_CUDA, "%s entry point unavailable", name);
+  return ENGRAM_OK;
+}
+
+// Unique id of the current context (0 when none is current).  Ids are never
+// reused within a process, unlike CUcontext handle values.
+int current_ctx_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  if (get_current == nullptr || get_id == nullptr) {
+    void* a = nullptr;
+    void* b = nullptr;
+    int rc = driver_fn("cuCtxGetCurrent", &a);
+    if (rc == ENGRAM_OK) rc = driver_fn("cuCtxGetId", &b);
+    if (rc) return rc;
+    get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+    get_id = reinterpret_cast<CtxGetIdFn>(b);
+  }
+  CUcontext ctx = nullptr;
+  *id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS) return fail(ENGRAM_E_CUDA, "cuCtxGetCurrent failed");
+  if (ctx != nullptr && get_id(ctx, id) != CUDA_SUCCESS) return fail(ENGRAM_E_CUDA, "cuCtxGetId failed");
+  return ENGRAM_OK;
+}
+
+// Device address of g_stage_scratch on the current device.  It is looked up
+// (cudaGetSymbolAddress, with the device current) on the first call made on
+// a device, and again whenever that device's context has changed since
+// (cudaDeviceReset destroys the context and its module; the array may then
+// sit elsewhere in the new one).  The check costs two driver queries.
 int scratch_address(void** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
   if (dev < 0 || dev >= kMaxDevices) return fail(ENGRAM_E_DEVICE, "device index %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_addr[dev] == nullptr) {
+  unsigned long long id = 0;
+  int rc = current_ctx_id(&id);
+  if (rc) return rc;
+  if (g_addr[dev] == nullptr || id == 0 || id != g_ctx_id[dev]) {
     void* p = nullptr;
     err = cudaGetSymbolAddress(&p, g_stage_scratch);
     if (err != cudaSuccess || p == nullptr)
       return fail(ENGRAM_E_CUDA, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(err));
+    rc = current_ctx_id(&id);  // the lookup creates the primary context if none was current
+    if (rc) return rc;
     g_addr[dev] = p;
+    g_ctx_id[dev] = id;
   }
   *out = g_addr[dev];
   return ENGRAM_OK;
