@@ -26,6 +26,7 @@ __all__ = [
     "engram_pack_wkv", "engram_project", "engram_gate_add", "engram_fill_synthetic_table",
     "engram_selftest_mod", "engram_project_gate", "project_gate_workspace", "partials_shape", "EngramLayer",
     "library_path", "ST_BAD_TOKEN", "ST_BAD_ROW", "ST_BAD_SLOT", "ST_TIMEOUT", "DEAD", "ROW_BYTES", "DecodeGraph",
+    "set_kernel_options", "kernel_options",
 ]
 
 MAX_LAYERS = 8
@@ -125,6 +126,8 @@ _SIGS = {
     "engram_project_fp8": [_P, _P, _I64, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P],
     "engram_project_gate_fp8": [_P, _P, _I64, _I64, _P, _P, _I32, _I32, _P, _P, _P, _P, _F32, _F32, _F32, _P, _P,
                                 ctypes.c_size_t, _P, _P],
+    "engram_set_kernel_options": [_P],
+    "engram_get_kernel_options": [_P],
     "engram_short_conv_add": [_P, _P, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _I32, _I32, _F32, _P, _P,
                               _I64, _P, ctypes.c_size_t, _P, _P],
 }
@@ -193,6 +196,33 @@ def _need(t: torch.Tensor, name: str, dtype, device=None, numel=None):
         raise ValueError(f"{name} must be contiguous")
     if numel is not None and t.numel() != numel:
         raise ValueError(f"{name} must have {numel} elements, has {t.numel()}")
+
+
+class _KernelOptions(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int32) for name in
+                ("projection_cta", "gather_copy", "fp8_pair", "fp8_fused", "plain_launch")]
+
+
+def kernel_options() -> dict:
+    """The engram_kernel_options in force, as a dict (all zero: the library's own choice)."""
+    o = _KernelOptions()
+    _check(_load().engram_get_kernel_options(ctypes.byref(o)), "engram_get_kernel_options")
+    return {name: int(getattr(o, name)) for name, _ in _KernelOptions._fields_}
+
+
+def set_kernel_options(**opts) -> dict:
+    """Override the library's kernel choice process-wide (engram_set_kernel_options).
+
+    Keys: projection_cta (0 default, 1 single CTA, 2 CTA pair), gather_copy
+    (0 cp.async, 1 TMA bulk), fp8_pair, fp8_fused, plain_launch (0/1); keys
+    not given keep their current value.  Returns the previous options."""
+    prev = kernel_options()
+    unknown = set(opts) - set(prev)
+    if unknown:
+        raise ValueError(f"unknown kernel options {sorted(unknown)}")
+    o = _KernelOptions(**{**prev, **{k: int(v) for k, v in opts.items()}})
+    _check(_load().engram_set_kernel_options(ctypes.byref(o)), "engram_set_kernel_options")
+    return prev
 
 
 # --------------------------------------------------------------------------- layout

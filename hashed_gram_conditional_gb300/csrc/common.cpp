@@ -1,6 +1,7 @@
 // Error reporting, device checks and version queries of libengram.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -62,9 +63,47 @@ int check_launch(const char* what) {
   return ENGRAM_OK;
 }
 
+namespace {
+// Process-wide kernel options, one relaxed atomic per field.
+std::atomic<int32_t> g_opt_projection_cta{0}, g_opt_gather_copy{0}, g_opt_fp8_pair{0}, g_opt_fp8_fused{0},
+    g_opt_plain_launch{0};
+}  // namespace
+
+engram_kernel_options kernel_options() {
+  engram_kernel_options o;
+  o.projection_cta = g_opt_projection_cta.load(std::memory_order_relaxed);
+  o.gather_copy = g_opt_gather_copy.load(std::memory_order_relaxed);
+  o.fp8_pair = g_opt_fp8_pair.load(std::memory_order_relaxed);
+  o.fp8_fused = g_opt_fp8_fused.load(std::memory_order_relaxed);
+  o.plain_launch = g_opt_plain_launch.load(std::memory_order_relaxed);
+  return o;
+}
+
 }  // namespace engram
 
 extern "C" {
+
+int engram_set_kernel_options(const engram_kernel_options* opts) {
+  using namespace engram;
+  if (opts == nullptr) return fail(ENGRAM_E_INVALID, "null kernel options");
+  if (opts->projection_cta < 0 || opts->projection_cta > 2 || opts->gather_copy < 0 || opts->gather_copy > 1 ||
+      opts->fp8_pair < 0 || opts->fp8_pair > 1 || opts->fp8_fused < 0 || opts->fp8_fused > 1 ||
+      opts->plain_launch < 0 || opts->plain_launch > 1)
+    return fail(ENGRAM_E_INVALID, "kernel option out of range");
+  g_opt_projection_cta.store(opts->projection_cta, std::memory_order_relaxed);
+  g_opt_gather_copy.store(opts->gather_copy, std::memory_order_relaxed);
+  g_opt_fp8_pair.store(opts->fp8_pair, std::memory_order_relaxed);
+  g_opt_fp8_fused.store(opts->fp8_fused, std::memory_order_relaxed);
+  g_opt_plain_launch.store(opts->plain_launch, std::memory_order_relaxed);
+  return ENGRAM_OK;
+}
+
+int engram_get_kernel_options(engram_kernel_options* out) {
+  if (out == nullptr) return engram::fail(ENGRAM_E_INVALID, "null kernel options");
+  *out = engram::kernel_options();
+  return ENGRAM_OK;
+}
+
 
 const char* engram_last_error(void) { return engram::g_last_error.c_str(); }
 

@@ -20,6 +20,8 @@ int fail(int code, const char* fmt, ...);
 // Checks that the current device is an sm_103 GPU; fills the SM count.
 int check_device(int* sm_count);
 int check_launch(const char* what);
+// The engram_kernel_options in force (engram_set_kernel_options).
+engram_kernel_options kernel_options();
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

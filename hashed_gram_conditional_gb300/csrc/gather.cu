@@ -427,15 +427,10 @@ __global__ void fill_table_kernel(uint8_t* table, int64_t n_words, uint64_t seed
   }
 }
 
-// The cp.async row copies are the default; ENGRAM_GATHER=bulk selects one
-// bulk (TMA) copy per row instead.  Both measure the same on GB300.
-bool use_ldgsts() {
-  static const bool v = [] {
-    const char* e = std::getenv("ENGRAM_GATHER");
-    return !(e != nullptr && e[0] == 'b');
-  }();
-  return v;
-}
+// The cp.async row copies are the default; engram_kernel_options.gather_copy
+// = 1 selects one bulk (TMA) copy per row instead.  Both measure the same on
+// GB300.
+bool use_ldgsts() { return kernel_options().gather_copy == 0; }
 
 }  // namespace
 }  // namespace engram

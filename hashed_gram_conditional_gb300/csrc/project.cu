@@ -1755,14 +1755,11 @@ size_t project_smem_bytes(bool pair) {
 // 128 tokens (one 128-row block) runs the single-CTA kernel: the pair's second
 // CTA would hold no rows, and as 128 x 256 tiles the column tiles fill the SMs
 // in one wave where the pairs need two (GB300, hidden 5120, 128 tokens, after
-// writing a buffer larger than L2: 72 us single-CTA vs 87 us pair).  ENGRAM_SINGLE_CTA_MMA=1 selects
-// the single-CTA kernel and =0 the pair at every size (for comparisons).
+// writing a buffer larger than L2: 72 us single-CTA vs 87 us pair).
+// engram_kernel_options.projection_cta selects either kernel at every size.
 bool use_pair_kernel(int64_t n_tokens) {
-  static const int forced = [] {
-    const char* v = std::getenv("ENGRAM_SINGLE_CTA_MMA");
-    return v == nullptr ? -1 : (v[0] == '1' ? 1 : 0);
-  }();
-  if (forced >= 0) return forced == 0;
+  const int forced = kernel_options().projection_cta;
+  if (forced != 0) return forced == 2;
   return n_tokens > BM;
 }
 
@@ -1806,16 +1803,11 @@ int prepare(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint16_t* wk
   return ENGRAM_OK;
 }
 
-// Fused launches are cooperative unless ENGRAM_COOPERATIVE=0 (for profilers
-// that cannot replay a cooperative cluster launch).  The grid never exceeds
-// the resident capacity either way, and every in-kernel wait is bounded.
-bool use_cooperative() {
-  static const bool v = [] {
-    const char* e = std::getenv("ENGRAM_COOPERATIVE");
-    return !(e != nullptr && e[0] == '0');
-  }();
-  return v;
-}
+// Fused launches are cooperative unless engram_kernel_options.plain_launch
+// is set (for profilers that cannot replay a cooperative cluster launch).
+// The grid never exceeds the resident capacity either way, and every
+// in-kernel wait is bounded.
+bool use_cooperative() { return kernel_options().plain_launch == 0; }
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, ProjArgs);
 
@@ -1873,15 +1865,9 @@ int launch(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB
 // operand bytes per SM, but the per-SM MMA rate is the same (an M = 256 pair
 // MMA takes as many cycles as an M = 128 one), its two CTAs gate each other
 // at every k-block, and both keep a single accumulator: on 16,384 tokens the
-// two measure within 2 % of each other (1.94-1.98 ms).  ENGRAM_FP8_PAIR=1
-// selects the pair.
-bool use_fp8_pair() {
-  static const bool v = [] {
-    const char* e = std::getenv("ENGRAM_FP8_PAIR");
-    return e != nullptr && e[0] == '1';
-  }();
-  return v;
-}
+// two measure within 2 % of each other (1.94-1.98 ms).
+// engram_kernel_options.fp8_pair selects the pair.
+bool use_fp8_pair() { return kernel_options().fp8_pair != 0; }
 
 // Argument checks and set-up of the FP8 entry points.
 int prepare8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K, const uint8_t* w8_d,
@@ -2051,15 +2037,9 @@ constexpr int64_t kFusedMinK = 3200;
 // the scale factors), so its fused epilogue cannot overlap the next tile's
 // main loop; the two kernels are faster at every size measured (16,384
 // tokens, hidden 5120: 2.53 ms per layer step vs 3.22 ms fused).
-// ENGRAM_FP8_FUSED=1 selects the fused FP8 kernel above 1536 tokens (for
-// comparisons).
-bool use_fp8_fused() {
-  static const bool v = [] {
-    const char* e = std::getenv("ENGRAM_FP8_FUSED");
-    return e != nullptr && e[0] == '1';
-  }();
-  return v;
-}
+// engram_kernel_options.fp8_fused selects the fused FP8 kernel above 1536
+// tokens (for comparisons).
+bool use_fp8_fused() { return kernel_options().fp8_fused != 0; }
 
 struct FusedWs {
   size_t partials, counters_off, counter_words, gates_off, v_off, total;

@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define ENGRAM_ABI_VERSION 1
+#define ENGRAM_ABI_VERSION 2
 
 #define ENGRAM_MAX_LAYERS 8
 #define ENGRAM_MAX_NGRAM 4   /* n-gram orders 2..max_ngram; history depth max_ngram-1 */
@@ -420,7 +420,7 @@ int engram_project_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tok
  * It runs engram_project_fp8 and engram_gate_add inside the workspace: the
  * FP8 kernel keeps one accumulator buffer, so a fused epilogue would not
  * overlap the next tile's main loop, and the two kernels are faster at every
- * size measured.  (ENGRAM_FP8_FUSED=1 in the environment selects the fused
+ * size measured.  (engram_kernel_options.fp8_fused = 1 selects the fused
  * FP8 kernel above 1536 tokens, for comparisons.) */
 int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K,
                             const uint8_t* w8_packed_d, const uint32_t* sfb_d, int32_t hidden, int32_t hc,
@@ -571,7 +571,9 @@ int engram_project_gate(const uint16_t* e_d, int64_t n_tokens, int64_t K, const 
  * The array is part of the library image, so every GPU that loads the
  * library holds it until the process exits.  The first call on each device
  * looks up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  All calls share
+ * current, and a call looks it up again when the device's context is not the
+ * one of the last lookup (after cudaDeviceReset); make the first call on a
+ * device, and the first after a reset, before any stream capture.  All calls share
  * the array: calls that overlap on the GPU race on it.  Each call writes
  * every scratch element it reads, so no clearing is needed between calls. */
 int engram_project_gate_add_noalloc(const uint16_t* e_d, int64_t n_tokens, int64_t K,
@@ -579,6 +581,44 @@ int engram_project_gate_add_noalloc(const uint16_t* e_d, int64_t n_tokens, int64
                                     uint16_t* h_d, const float* q_w_d, const float* k_w_d,
                                     const uint8_t* mask_d, float eps, float clamp, float score_scale,
                                     float* gate_out_d, int32_t* status_d, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Kernel selection                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Alternative kernels, for comparisons and profiling; the pages have no
+ * counterpart.  The library picks its kernels by itself; these options
+ * override that choice process-wide (every device and thread) from the next
+ * call on.  All fields zero is the default choice.
+ *   projection_cta  bf16 projection (engram_project, engram_project_gate):
+ *                   0 single CTA up to 128 tokens and the CTA pair above,
+ *                   1 the single-CTA kernel at every size, 2 the CTA pair at
+ *                   every size
+ *   gather_copy     row copies of the E4M3 + E8M0 gathers: 0 16-byte cp.async
+ *                   copies, 1 one TMA bulk copy per row
+ *   fp8_pair        block-FP8 projection: 0 single CTA, 1 CTA pair
+ *   fp8_fused       engram_project_gate_fp8 above 1536 tokens: 0 projection
+ *                   kernel then the gate kernel, 1 the fused kernel
+ *   plain_launch    fused projection + gate kernels: 0 cooperative launch
+ *                   (every CTA guaranteed resident), 1 plain launch, for
+ *                   profilers that cannot replay a cooperative launch.  The
+ *                   fused kernels' value tiles wait for gates that other CTAs
+ *                   compute, so a plain launch is correct only while nothing
+ *                   else runs on the GPU; otherwise such a wait may run out
+ *                   and set ENGRAM_ST_TIMEOUT (no hang, no trap). */
+typedef struct engram_kernel_options {
+  int32_t projection_cta;
+  int32_t gather_copy;
+  int32_t fp8_pair;
+  int32_t fp8_fused;
+  int32_t plain_launch;
+} engram_kernel_options;
+
+/* Sets the options; ENGRAM_E_INVALID (nothing changed) for a null pointer or
+ * a field out of range. */
+int engram_set_kernel_options(const engram_kernel_options* opts);
+/* Copies the options in force into *out. */
+int engram_get_kernel_options(engram_kernel_options* out);
 
 /* ------------------------------------------------------------------------ */
 /* Test-data and diagnostics                                                  */

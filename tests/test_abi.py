@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_struct_sizes_match(lib):
     assert lib.engram_layout_size() == ctypes.sizeof(eg._Layout)
     assert lib.engram_layout_params_size() == ctypes.sizeof(eg._LayoutParams)
-    assert lib.engram_abi_version() == 1
+    assert lib.engram_abi_version() == 2
 
 
 @pytest.mark.parametrize("vocab,base,layers", [(1000, 4099, [1]), (99092, 2_000_000, [1]),
@@ -155,3 +155,24 @@ def test_host_side_argument_checks_of_the_wider_path(lib):
     # host gather: sizes and pointers
     assert lib.engram_host_gather(None, 10, None, 5, None, 0, None) == E_INVALID
     assert lib.engram_host_gather(None, -1, None, 0, None, 0, None) == E_INVALID
+
+
+def test_kernel_options_round_trip_and_range_checks(lib):
+    """engram_set/get_kernel_options: host-only, no device needed."""
+    prev = eg.kernel_options()
+    assert prev == dict(projection_cta=0, gather_copy=0, fp8_pair=0, fp8_fused=0, plain_launch=0)
+    try:
+        eg.set_kernel_options(projection_cta=2, plain_launch=1)
+        assert eg.kernel_options() == dict(projection_cta=2, gather_copy=0, fp8_pair=0, fp8_fused=0, plain_launch=1)
+        with pytest.raises(eg.EngramError):
+            eg.set_kernel_options(projection_cta=3)
+        with pytest.raises(eg.EngramError):
+            eg.set_kernel_options(gather_copy=-1)
+        # a rejected call changes nothing
+        assert eg.kernel_options()["projection_cta"] == 2
+        with pytest.raises(ValueError):
+            eg.set_kernel_options(no_such_option=1)
+        assert lib.engram_set_kernel_options(None) == -1
+    finally:
+        eg.set_kernel_options(**prev)
+    assert eg.kernel_options() == prev

@@ -1,13 +1,15 @@
-"""The alternative projection kernels pass the same parity tests as the
-defaults: the single-CTA bf16 kernels at every size (ENGRAM_SINGLE_CTA_MMA=1),
-the CTA-pair bf16 kernels at every size (=0; by default batches of at most
-128 tokens take the single-CTA kernel), the CTA-pair block-FP8 kernels
-(ENGRAM_FP8_PAIR=1), the fused block-FP8 kernels (ENGRAM_FP8_FUSED=1; by
-default the FP8 gate runs as a separate kernel), the TMA bulk-copy gather
-(ENGRAM_GATHER=bulk) and the fused projection launched without the
-cooperative attribute (ENGRAM_COOPERATIVE=0, the mode profilers need).
+"""The alternative kernels pass the same parity tests as the defaults.
 
-The selection is read once per process, so the tests run in a child process.
+engram_kernel_options selects them: the single-CTA bf16 kernels at every
+size (projection_cta = 1), the CTA-pair bf16 kernels at every size (= 2; by
+default batches of at most 128 tokens take the single-CTA kernel), the
+CTA-pair block-FP8 kernels (fp8_pair), the fused block-FP8 kernels
+(fp8_fused; by default the FP8 gate runs as a separate kernel), the TMA
+bulk-copy gather (gather_copy = 1) and the fused projection launched without
+the cooperative attribute (plain_launch, the mode profilers need).
+
+Each case reruns a parity test file in a child process with the options set
+for the whole run (--kernel-options), so the defaults stay in force here.
 """
 import os
 import subprocess
@@ -19,51 +21,21 @@ from gpu_util import require_gpu
 
 pytestmark = pytest.mark.gpu
 
+HERE = os.path.dirname(os.path.abspath(__file__))
 
-def test_single_cta_kernels_pass_projection_parity():
+
+@pytest.mark.parametrize("options,test_file", [
+    ("projection_cta=1", "test_gpu_project.py"),
+    ("projection_cta=2", "test_gpu_project.py"),
+    ("fp8_pair=1", "test_gpu_fp8.py"),
+    ("fp8_fused=1,fp8_pair=0", "test_gpu_fp8.py"),
+    ("fp8_fused=1,fp8_pair=1", "test_gpu_fp8.py"),
+    ("gather_copy=1", "test_gpu_gather.py"),
+    ("plain_launch=1", "test_gpu_project.py"),
+])
+def test_alternative_kernels_pass_parity(options, test_file):
     require_gpu()
-    here = os.path.dirname(os.path.abspath(__file__))
-    env = dict(os.environ, ENGRAM_SINGLE_CTA_MMA="1")
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_project.py"), "-m", "gpu", "-q",
-                        "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
-
-
-def test_fp8_pair_kernels_pass_fp8_parity():
-    require_gpu()
-    here = os.path.dirname(os.path.abspath(__file__))
-    env = dict(os.environ, ENGRAM_FP8_PAIR="1")
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_fp8.py"), "-m", "gpu", "-q",
-                        "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
-
-
-
-def test_pair_kernels_at_every_size_pass_projection_parity():
-    require_gpu()
-    here = os.path.dirname(os.path.abspath(__file__))
-    env = dict(os.environ, ENGRAM_SINGLE_CTA_MMA="0")
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_project.py"), "-m", "gpu", "-q",
-                        "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
-
-
-@pytest.mark.parametrize("pair", ["0", "1"])
-def test_fused_fp8_kernels_pass_fp8_parity(pair):
-    require_gpu()
-    here = os.path.dirname(os.path.abspath(__file__))
-    env = dict(os.environ, ENGRAM_FP8_FUSED="1", ENGRAM_FP8_PAIR=pair)
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_fp8.py"), "-m", "gpu", "-q",
-                        "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
-
-
-@pytest.mark.parametrize("env_var,value,test_file", [("ENGRAM_GATHER", "bulk", "test_gpu_gather.py"),
-                                                     ("ENGRAM_COOPERATIVE", "0", "test_gpu_project.py")])
-def test_alternative_launch_modes_pass_parity(env_var, value, test_file):
-    require_gpu()
-    here = os.path.dirname(os.path.abspath(__file__))
-    env = dict(os.environ, **{env_var: value})
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, test_file), "-m", "gpu", "-q",
-                        "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(HERE, test_file), "-m", "gpu", "-q",
+                        "-p", "no:cacheprovider", f"--kernel-options={options}"],
+                       capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
