@@ -88,6 +88,10 @@ def parse():
     p.add_argument("--cpu-sample", type=int, default=8192, help="tokens of the oracle CPU baseline sample")
     p.add_argument("--ref-sample", type=int, default=128, help="tokens per reference-arm step")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sustained-s", type=float, default=3.0,
+                   help="seconds of back-to-back layer steps after the timed region (projection under the power cap)")
+    p.add_argument("--plain-launch", action="store_true",
+                   help="launch the fused kernels without the cooperative attribute (for ncu; GPU must be exclusive)")
     return p.parse_args()
 
 
@@ -249,6 +253,8 @@ def run_ours(args, rank, world, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.plain_launch:
+        eg.set_kernel_options(plain_launch=1)
     w = WORKLOADS[args.workload]
     inp = make_inputs(w, rank_seed(w.seed, rank), dev)
     layer, b = inp["layer"], inp["batch"]
@@ -334,6 +340,8 @@ def run_ours(args, rank, world, local):
     host = host_table_bench(args, w, inp, layer, flush, dev, statistics.mean(step_ms)) \
         if side and args.host_steps > 0 else None
     full = fullscale_bench(args, inp, layer, dev) if side and args.fullscale_passes > 0 else None
+    # last, so that the heat of a seconds-long loop does not reach the other legs
+    sus = sustained_loop(args.sustained_s, step, flush, gpu_id) if side and args.sustained_s > 0 else None
 
     if rank != 0:
         return None
@@ -389,6 +397,59 @@ def run_ours(args, rank, world, local):
               "traffic": traffic.get(gather_kernel),
               "algorithmic_per_launch": f"{gbytes} B ({GATHER_BYTES_PER_TOKEN} B/token, T={T})",
               "peak_source": f"{peak_src} hbm_gbs"}
+    # the gather half of the metric, nested in the roofline record: the fused
+    # hash + gather inside the timed step and the 65,536-token microbench
+    roof["hash_gather"] = {
+        "in_step": {k: roof_g[k] for k in ("kernel", "achieved", "peak", "unit", "frac", "traffic",
+                                            "algorithmic_per_launch", "peak_source")},
+    }
+    roof["hash_gather"]["in_step"]["ms"] = gat_s * 1e3
+    if micro is not None:
+        Tm = micro["algorithmic_bytes"] // GATHER_BYTES_PER_TOKEN
+        for key, kern in (("microbench_fused", "fused"), ("microbench", "gather")):
+            if key == "microbench_fused" and "fused_gather_gbs" not in micro:
+                continue
+            gbs = micro["fused_gather_gbs"] if key == "microbench_fused" else micro["gather_gbs"]
+            roof["hash_gather"][key] = {
+                "kernel": ("gather_ldgsts_kernel<HashedRows> (hash fused into the gather)" if kern == "fused"
+                           else "gather_ldgsts_kernel<IdRows> (engram_gather_dequant after engram_hash)"),
+                "tokens": Tm, "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"],
+                "algorithmic_per_launch": f"{micro['algorithmic_bytes']} B ({GATHER_BYTES_PER_TOKEN} B/token)",
+                "traffic": traffic.get(f"{gather_kernel}_microbench" if kern == "gather"
+                                       else f"{gather_kernel}_microbench_fused"),
+                "uniform_tokens_frac": (micro["uniform_control"]["fused_gather_gbs"] if kern == "fused"
+                                        else micro["uniform_control"]["gather_gbs"]) / peaks["hbm_gbs"]
+                if (kern == "gather" or "fused_gather_gbs" in micro["uniform_control"]) else None,
+                "peak_source": f"{peak_src} hbm_gbs"}
+    if full is not None and "hash_gather_gbs" in full:
+        roof["hash_gather"]["full_scale"] = {
+            "kernel": "gather_ldgsts_kernel<HashedRows>, 101.4 GB table, 16,384-token chunks",
+            "achieved": full["hash_gather_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": full["hash_gather_gbs"] / peaks["hbm_gbs"]}
+    if gen is not None:
+        roof["hash_gather"]["generic_27b_shape"] = {
+            "kernel": gen.get("kernels", "bf16-row gather"), "achieved": gen["hash_gather_gbs"],
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gen["hash_gather_gbs"] / peaks["hbm_gbs"]}
+    if dec is not None:
+        roof["decode_wkv"] = {"kernel": "projection at 256 tokens (wkv streamed from HBM)",
+                              "achieved": dec["wkv_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": dec["wkv_gbs"] / peaks["hbm_gbs"], "step_ms": dec.get("step_ms"),
+                              "project_gate_ms": dec.get("project_gate_ms")}
+    roof["frac_vs_sustained"] = flops / proj_s / 1e12 / peaks["bf16_tflops_sustained"]
+    if clocks.get("sm_mhz"):
+        roof["sm_mhz_median_timed"] = clocks["sm_mhz"]
+    if sus is not None:
+        tf = flops / (sus["project_gate_ms"] / 1e3) / 1e12
+        roof["sustained_loop"] = {
+            "seconds": sus["wall_s"], "steps": sus["steps"], "project_gate_ms": sus["project_gate_ms"],
+            "achieved": tf, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": tf / peaks["bf16_tflops_sustained"], "frac_vs_burst": tf / peaks["bf16_tflops"],
+            "sm_mhz_median": sus["clocks"].get("sm_mhz"), "power_w_max": sus["clocks"].get("power_w_max"),
+            "reasons": sus["clocks"].get("reasons"), "clock_samples": sus["clocks"].get("samples"),
+            "tflops_per_ghz": (tf / (sus["clocks"]["sm_mhz"] / 1e3)) if sus["clocks"].get("sm_mhz") else None,
+            "peak_source": f"{peak_src} bf16_tflops_sustained (sm_mhz_median "
+                           f"{peaks.get('clocks_under_load', {}).get('sm_mhz_median')})"}
     out = {
         "metric": METRIC,
         "value": aggregate_value(T, args.steps, world, total_s),
@@ -424,6 +485,32 @@ def run_ours(args, rank, world, local):
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_sample)
     return out
+
+
+def sustained_loop(seconds, step, flush, gpu_id):
+    """Layer steps back to back for ``seconds`` after the timed region, with
+    the SM clocks sampled meanwhile: the projection's rate under the power
+    cap, comparable with the driver's sustained GEMM peak (also a
+    seconds-long loop).  Same step and L2 flush as the timed region."""
+    import torch
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    evs = []
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        batch = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(50)]
+        for ev in batch:
+            flush()
+            step(ev)
+        torch.cuda.synchronize()
+        evs.extend(batch)
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    return {"steps": len(evs), "wall_s": wall,
+            "project_gate_ms": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs),
+            "hash_gather_ms": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
+            "step_ms": statistics.mean(ev[0].elapsed_time(ev[2]) for ev in evs), "clocks": clocks}
 
 
 def e2e_pipeline(args, b, h0, layer, hist, status, dev, world):
@@ -662,11 +749,35 @@ def microbench(args, w, inp, layer, flush, dev):
         run(evu[k])
     torch.cuda.synchronize()
     gat_u = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evu) / 1e3
+
+    # the product path: hash fused into the gather (one kernel), Zipf then uniform tokens
+    def fused(raw_ids, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        eg.engram_hash_gather(layer.layout, 0, raw_ids, cu, layer.token_map, layer.table, None, e, mask)
+        if ev is not None:
+            ev[1].record(stream)
+
+    fused_s = {}
+    for name, raw_ids in (("zipf", torch.from_numpy(bm.raw_ids).to(dev)), ("uniform", raw)):
+        for _ in range(3):
+            flush()
+            fused(raw_ids)
+        evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.micro_steps)]
+        for k in range(args.micro_steps):
+            flush()
+            fused(raw_ids, evf[k])
+        torch.cuda.synchronize()
+        fused_s[name] = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evf) / 1e3
     return {"workload": f"microbench: 1 x {T} Zipf(1.1) tokens, same 12.67 GB table", "steps": args.micro_steps,
             "hash_gather_tokens_per_s": T / step, "hash_ms": (step - gat) * 1e3, "gather_ms": gat * 1e3,
             "gather_gbs": gbytes / gat / 1e9, "algorithmic_bytes": gbytes,
+            "fused_hash_gather_ms": fused_s["zipf"] * 1e3, "fused_gather_gbs": gbytes / fused_s["zipf"] / 1e9,
+            "fused_tokens_per_s": T / fused_s["zipf"],
             "uniform_control": {"tokens": "uniform over the raw vocabulary", "gather_ms": gat_u * 1e3,
-                                "gather_gbs": gbytes / gat_u / 1e9}}
+                                "gather_gbs": gbytes / gat_u / 1e9,
+                                "fused_hash_gather_ms": fused_s["uniform"] * 1e3,
+                                "fused_gather_gbs": gbytes / fused_s["uniform"] / 1e9}}
 
 
 def decode_bench(args, w, inp, layer, flush, dev):
