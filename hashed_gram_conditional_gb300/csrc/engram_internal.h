@@ -34,6 +34,17 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 // and the kernel then records ENGRAM_ST_TIMEOUT and unwinds instead of hanging.
 constexpr long long kWaitBudgetCycles = 1LL << 31;
 
+// Programmatic dependent launch: a kernel launched right after this one with
+// programmatic stream serialization may be scheduled once every CTA of this
+// grid has issued this (its griddepcontrol.wait still waits for the whole
+// grid to finish and its writes to be visible).
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits for the grids this one depends on programmatically (a no-op when the
+// launch had no such dependency).
+__device__ __forceinline__ void wait_prior_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

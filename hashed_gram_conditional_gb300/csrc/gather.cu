@@ -85,6 +85,7 @@ __device__ __forceinline__ uint4 dequant8(uint2 w, uint32_t sbyte) {
 
 __global__ void __launch_bounds__(kWarps * 32, 1) gather_dequant_kernel(GatherArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  allow_dependent_launch();  // a following history commit may load its inputs meanwhile
   const int w = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const uint32_t stage_bytes = static_cast<uint32_t>(a.n_cols) * kSlot;
@@ -322,6 +323,7 @@ struct Fp8Out {
 template <class RowSource, class Out>
 __global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArgs a, RowSource src, Out store) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  allow_dependent_launch();  // a following history commit may load its inputs meanwhile
   const int w = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const uint32_t stage_bytes = static_cast<uint32_t>(a.n_cols) * kSlot;

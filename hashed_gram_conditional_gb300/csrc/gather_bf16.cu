@@ -20,7 +20,7 @@ namespace engram {
 namespace {
 
 constexpr int kWarpsB = 8;   // warps per block
-constexpr int kUnrollB = 4;  // 16-byte pieces in flight per lane per round
+constexpr int kUnrollB = 5;  // 16-byte pieces in flight per lane per round: one round for 16 rows of 80
 
 template <bool kHash>
 __global__ void __launch_bounds__(kWarpsB * 32) gather_rows_bf16_kernel(
@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kWarpsB * 32) gather_rows_bf16_kernel(
     int64_t n_tokens, int32_t n_cols, uint16_t* __restrict__ e, int32_t* status, hashdev::HashConsts c,
     const int32_t* __restrict__ raw, const int64_t* __restrict__ cu, int32_t n_seqs,
     const int32_t* __restrict__ tmap, const int32_t* __restrict__ hist, int32_t* rows_out, uint8_t* mask) {
+  allow_dependent_launch();  // a following history commit may load its inputs meanwhile
   const uint32_t lane = lane_id();
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;

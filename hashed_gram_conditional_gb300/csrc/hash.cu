@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(256) hash_prefill_kernel(
     const int64_t* __restrict__ cu, int32_t n_seqs, const int32_t* __restrict__ tmap,
     const int32_t* __restrict__ hist, int32_t* __restrict__ rows, uint8_t* __restrict__ mask,
     int32_t* status) {
+  allow_dependent_launch();  // the history commit may load its inputs meanwhile
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
        t < n_tokens; t += warps) {
@@ -48,6 +49,7 @@ __global__ void __launch_bounds__(256) hash_all_layers_kernel(
     int32_t n_seqs, const int32_t* __restrict__ tmap, const int32_t* __restrict__ hist,
     int32_t* __restrict__ rows, uint8_t* __restrict__ mask, int32_t* status) {
   const HashConsts& c = ca.l[0];
+  allow_dependent_launch();  // the history commit may load its inputs meanwhile
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; t < n_tokens;
        t += warps) {
@@ -60,6 +62,9 @@ __global__ void __launch_bounds__(256) hash_all_layers_kernel(
 // History after a chunk: the last `depth` compressed ids of each sequence,
 // most recent first, falling back to the previous history for short chunks.
 // One thread per sequence reads all it needs before writing its own row.
+// It is launched as a programmatic dependent of the kernel that hashed the
+// chunk: that kernel writes none of what is read here, only reads the old
+// history, so the loads run early and only the writes wait for it.
 __global__ void hash_commit_kernel(HashConsts c, const int32_t* __restrict__ raw,
                                    const int64_t* __restrict__ cu, int32_t n_seqs,
                                    const int32_t* __restrict__ tmap, int32_t* hist,
@@ -80,6 +85,7 @@ __global__ void hash_commit_kernel(HashConsts c, const int32_t* __restrict__ raw
       nh[i] = hist[static_cast<int64_t>(s) * depth + (i - len)];
     }
   }
+  wait_prior_grids();  // every position of the chunk has read the old history
 #pragma unroll
   for (int i = 0; i < ENGRAM_MAX_NGRAM - 1; ++i) {
     if (i >= depth) break;
@@ -119,7 +125,17 @@ __global__ void selftest_mod_kernel(HashConsts c, const uint64_t* __restrict__ x
 
 int hashdev::launch_hist_commit(const HashConsts& c, const int32_t* raw, const int64_t* cu, int32_t n_seqs,
                                 const int32_t* tmap, int32_t* hist, int32_t* status, cudaStream_t st) {
-  hash_commit_kernel<<<(n_seqs + 127) / 128, 128, 0, st>>>(c, raw, cu, n_seqs, tmap, hist, status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((n_seqs + 127) / 128));
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, hash_commit_kernel, c, raw, cu, n_seqs, tmap, hist, status);
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "hash_commit_kernel launch: %s", cudaGetErrorString(err));
   return check_launch("hash_commit_kernel");
 }
 
@@ -150,11 +166,8 @@ extern "C" int engram_hash(const engram_layout* layout, int32_t layer, const int
                                                     status_d);
     if ((rc = check_launch("hash_prefill_kernel"))) return rc;
   }
-  if (hist_d != nullptr) {
-    hash_commit_kernel<<<(n_seqs + 127) / 128, 128, 0, st>>>(c, raw_ids_d, cu_seqlens_d, n_seqs,
-                                                            token_map_d, hist_d, status_d);
-    if ((rc = check_launch("hash_commit_kernel"))) return rc;
-  }
+  if (hist_d != nullptr)
+    return launch_hist_commit(c, raw_ids_d, cu_seqlens_d, n_seqs, token_map_d, hist_d, status_d, st);
   return ENGRAM_OK;
 }
 
@@ -217,10 +230,7 @@ extern "C" int engram_hash_all_layers(const engram_layout* layout, const int32_t
                                                    hist_d, row_ids_d, mask_d, status_d);
     if ((rc = check_launch("hash_all_layers_kernel"))) return rc;
   }
-  if (hist_d != nullptr) {
-    hash_commit_kernel<<<(n_seqs + 127) / 128, 128, 0, st>>>(ca.l[0], raw_ids_d, cu_seqlens_d, n_seqs,
-                                                            token_map_d, hist_d, status_d);
-    if ((rc = check_launch("hash_commit_kernel"))) return rc;
-  }
+  if (hist_d != nullptr)
+    return launch_hist_commit(ca.l[0], raw_ids_d, cu_seqlens_d, n_seqs, token_map_d, hist_d, status_d, st);
   return ENGRAM_OK;
 }
