@@ -54,6 +54,10 @@ KERNEL_SOURCES = {
     "conv_prep_kernel": ["shortconv.cu", "engram_internal.h"],
     "conv_add_kernel": ["shortconv.cu", "engram_internal.h"],
     "conv_state_kernel": ["shortconv.cu", "engram_internal.h"],
+    "gather_ldgsts_kernel_microbench": ["gather.cu", "hash_device.cuh", "engram_internal.h"],
+    "gather_ldgsts_kernel_microbench_fused": ["gather.cu", "hash_device.cuh", "engram_internal.h"],
+    "gather_ldgsts_kernel_fp8": ["gather.cu", "hash_device.cuh", "engram_internal.h"],
+    "gather_rows_bf16_kernel": ["gather_bf16.cu", "hash_device.cuh", "engram_internal.h"],
 }
 
 
@@ -429,8 +433,9 @@ def run_ours(args, rank, world, local):
             "frac": full["hash_gather_gbs"] / peaks["hbm_gbs"]}
     if gen is not None:
         roof["hash_gather"]["generic_27b_shape"] = {
-            "kernel": gen.get("kernels", "bf16-row gather"), "achieved": gen["hash_gather_gbs"],
-            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gen["hash_gather_gbs"] / peaks["hbm_gbs"]}
+            "kernel": "gather_rows_bf16_kernel<hashed> + the history commit", "achieved": gen["hash_gather_gbs"],
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gen["hash_gather_gbs"] / peaks["hbm_gbs"],
+            "traffic": traffic.get("gather_rows_bf16_kernel")}
     if dec is not None:
         roof["decode_wkv"] = {"kernel": "projection at 256 tokens (wkv streamed from HBM)",
                               "achieved": dec["wkv_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
