@@ -166,3 +166,26 @@ def test_hash_step_bad_slot():
     torch.cuda.synchronize()
     assert int(st.item()) & eg.ST_BAD_SLOT
     assert list(mask.cpu().numpy()) == [0, 1]
+
+
+def test_hash_zero_tokens_keeps_history():
+    """A call with no tokens still runs the history commit on its own (as a
+    programmatic dependent of whatever the stream ran last): every sequence
+    is empty, so each history row comes back unchanged, DEAD slots included."""
+    w, tm, lay_o, lay = setup("tiny")
+    rng = np.random.default_rng(11)
+    hist0 = rng.integers(0, w.v, size=(5, 3)).astype(np.int32)
+    hist0[1, 2] = DEAD
+    hist_d = i32(hist0)
+    cu = np.zeros(6, dtype=np.int64)
+    st = status()
+    # something on the stream first: a real hash call whose kernel allows early dependent launch
+    b = prefill_batch(w)
+    eg.engram_hash(lay, 0, i32(b.raw_ids), i64(b.cu_seqlens), i32(tm), status=st)
+    rows, mask = eg.engram_hash(lay, 0, i32(np.zeros(0, dtype=np.int32)), i64(cu), i32(tm), hist_d, status=st)
+    torch.cuda.synchronize()
+    assert rows.shape[0] == 0
+    assert int(st.item()) == 0
+    assert (hist_d.cpu().numpy() == hist0).all()
+    _, _, hist_o = OH.hash_prefill(np.zeros(0, dtype=np.int32), cu, tm, lay_o, 0, hist=hist0.astype(np.int64))
+    assert (hist_o == hist0).all()
