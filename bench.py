@@ -143,20 +143,25 @@ def profiled_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle-reason sampling around a timed region.
+
+    Samples every `interval_ms` with nvidia-smi's own timestamp; stop(t0, t1)
+    keeps only the samples taken between the wall-clock times t0 and t1 (the
+    timed region), and says how many that was."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id: str):
+    def __init__(self, gpu_id: str, interval_ms: int = 10):
         self.gpu_id = gpu_id
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines = []
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-lms", "100", "-i", self.gpu_id], stdout=subprocess.PIPE,
+                                          "-lms", str(self.interval_ms), "-i", self.gpu_id], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -167,32 +172,62 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    @staticmethod
+    def _epoch(stamp: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, t0=None, t1=None):
+        """Summary of the samples; with t0, t1 (time.time()) only those inside
+        [t0, t1], widened by 50 ms steps (up to 250 ms) while none falls inside."""
+        out = self._summary(t0, t1)
+        pad = 0.0
+        while t0 is not None and out["samples"] == 0 and pad < 0.25:
+            pad += 0.05
+            out = self._summary(t0 - pad, t1 + pad)
+            out["window_widened_ms"] = round(pad * 1e3)
+        return out
+
+    def _summary(self, t0, t1):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.thread.join(timeout=2)
+        if self.proc.poll() is None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        total = 0
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
+            total += 1
+            if t0 is not None:
+                ts = self._epoch(parts[0])
+                if ts is None or ts < t0 or ts > t1:
+                    continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+                power.append(float(parts[4]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(names, parts[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+               "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm),
+               "interval_ms": self.interval_ms}
+        if t0 is not None:
+            out["samples_outside_region"] = total - len(sm)
+        return out
 
 
 # ------------------------------------------------------------------------- ranks
@@ -303,15 +338,18 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)  # let the sampler's first reading land
+    epoch0 = time.time()
     wall0 = time.perf_counter()
     for k in range(args.steps):
         flush()
         step(events[k])
     torch.cuda.synchronize()
     wall1 = time.perf_counter()
+    epoch1 = time.time()
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
+    time.sleep(0.05)  # the sampler's last readings of the region
+    clocks = sampler.stop(epoch0, epoch1)
     st = int(status.item())
 
     def ms(k, i, j):
@@ -498,9 +536,10 @@ def sustained_loop(seconds, step, flush, gpu_id):
     cap, comparable with the driver's sustained GEMM peak (also a
     seconds-long loop).  Same step and L2 flush as the timed region."""
     import torch
-    sampler = ClockSampler(gpu_id)
+    sampler = ClockSampler(gpu_id, interval_ms=50)
     sampler.start()
     time.sleep(0.3)
+    e0 = time.time()
     evs = []
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < seconds:
@@ -511,7 +550,7 @@ def sustained_loop(seconds, step, flush, gpu_id):
         torch.cuda.synchronize()
         evs.extend(batch)
     wall = time.perf_counter() - t0
-    clocks = sampler.stop()
+    clocks = sampler.stop(e0, time.time())
     return {"steps": len(evs), "wall_s": wall,
             "project_gate_ms": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs),
             "hash_gather_ms": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),

@@ -58,3 +58,29 @@ def test_algorithmic_bytes_per_token():
     assert bench.GATE_BYTES_PER_TOKEN(4, 5120) == 2 * 4 * 5120 * 2 + 5120 * 2 + 4 * 20 * 16 + 1
     # h read and written, v read once, the gates
     assert bench.CONV_BYTES_PER_TOKEN(4, 5120) == 92_176
+
+
+def test_clock_sampler_keeps_only_the_timed_region():
+    """The clock record counts only nvidia-smi samples taken inside the timed
+    region, widening the window in 50 ms steps only while none falls inside."""
+    import datetime
+    import time
+
+    import bench
+
+    c = bench.ClockSampler("0")
+    c.proc = type("Done", (), {"poll": lambda self: 0})()  # no process to stop
+    now = time.time()
+
+    def line(dt, mhz, watts, cap):
+        stamp = datetime.datetime.fromtimestamp(now + dt).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{stamp}, 0, {mhz}, 2070, {watts}, 0x0, Not Active, Not Active, Not Active, {cap}"
+
+    c.lines = [line(-0.2, 345, 90, "Not Active"), line(0.01, 2070, 900, "Not Active"),
+               line(0.03, 1980, 1200, "Active"), line(0.3, 1500, 300, "Not Active")]
+    inside = c.stop(now, now + 0.05)
+    assert inside["samples"] == 2 and inside["samples_outside_region"] == 2
+    assert inside["sm_mhz"] == (2070 + 1980) / 2 and inside["power_w_max"] == 1200
+    assert inside["reasons"] == ["sw_power_cap"] and "window_widened_ms" not in inside
+    widened = c.stop(now + 0.1, now + 0.12)  # nothing inside: widened until the two samples before it
+    assert widened["samples"] == 2 and widened["window_widened_ms"] == 100
