@@ -75,6 +75,9 @@ __global__ void __launch_bounds__(256) gate_add_kernel(
     float clamp, float score_scale, float* __restrict__ gate_out, int pos_per_cta) {
   __shared__ float gs[kPosPerCta][kMaxHc];
   __shared__ uint8_t live[kPosPerCta];
+  // launched as a programmatic dependent: the partial sums, v and h are read
+  // only after the previous kernel (the projection) has finished
+  wait_prior_grids();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntile = hidden / 256;
   const int nvec = hidden / 8;  // 16-byte vectors per stream row
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(256) gates_kernel(const float4* __restrict__ p
                                                     const uint8_t* __restrict__ mask, int64_t n_tokens,
                                                     int hidden, int hc, float eps, float clamp, float score_scale,
                                                     float* __restrict__ gate_out) {
+  wait_prior_grids();  // as gate_add_kernel
   const int lane = threadIdx.x & 31;
   const int ntile = hidden / 256;
   const float inv_h = 1.0f / static_cast<float>(hidden);
@@ -143,6 +147,20 @@ __global__ void __launch_bounds__(256) gates_kernel(const float4* __restrict__ p
       if (lane == 0) gate_out[t * hc + m] = g;
     }
   }
+}
+
+// 256-thread launch configuration on `st`; set_pdl makes it a programmatic
+// dependent of the previous kernel in the stream.
+cudaLaunchConfig_t pdl_config(int blocks, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  return cfg;
+}
+void set_pdl(cudaLaunchAttribute* attr) {
+  attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr->val.programmaticStreamSerializationAllowed = 1;
 }
 
 }  // namespace
@@ -169,9 +187,14 @@ extern "C" int engram_gate_add(const float* partials_d, const uint16_t* v_d, uin
   if (h_d == nullptr) {  // gates only
     const int64_t cap = static_cast<int64_t>(sms) * 16;
     const int64_t need = (n_tokens + 7) / 8;
-    gates_kernel<<<static_cast<int>(need < cap ? need : cap), 256, 0, as_stream(stream)>>>(
-        reinterpret_cast<const float4*>(partials_d), mask_d, n_tokens, hidden, hc, eps, clamp, score_scale,
-        gate_out_d);
+    cudaLaunchConfig_t cfg = pdl_config(static_cast<int>(need < cap ? need : cap), as_stream(stream));
+    cudaLaunchAttribute attr;
+    cfg.attrs = &attr;
+    set_pdl(&attr);
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, gates_kernel, reinterpret_cast<const float4*>(partials_d),
+                                               mask_d, n_tokens, hidden, hc, eps, clamp, score_scale, gate_out_d);
+    if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "gates_kernel launch: %s", cudaGetErrorString(err));
     return check_launch("gates_kernel");
   }
   // positions per CTA: 8 when there are enough positions for 4 CTAs per SM
@@ -180,9 +203,14 @@ extern "C" int engram_gate_add(const float* partials_d, const uint16_t* v_d, uin
   const int64_t cap = static_cast<int64_t>(sms) * 8;
   const int64_t need = (n_tokens + P - 1) / P;
   const int blocks = static_cast<int>(need < cap ? need : cap);
-  gate_add_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
-      reinterpret_cast<const float4*>(partials_d), reinterpret_cast<const uint4*>(v_d),
-      reinterpret_cast<uint4*>(h_d), mask_d, n_tokens, hidden, hc, eps, clamp, score_scale,
-      gate_out_d, P);
+  cudaLaunchConfig_t cfg = pdl_config(blocks, as_stream(stream));
+  cudaLaunchAttribute attr;
+  cfg.attrs = &attr;
+  set_pdl(&attr);
+  cfg.numAttrs = 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, gate_add_kernel, reinterpret_cast<const float4*>(partials_d),
+                                             reinterpret_cast<const uint4*>(v_d), reinterpret_cast<uint4*>(h_d),
+                                             mask_d, n_tokens, hidden, hc, eps, clamp, score_scale, gate_out_d, P);
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "gate_add_kernel launch: %s", cudaGetErrorString(err));
   return check_launch("gate_add_kernel");
 }

@@ -599,6 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  // Launched as a programmatic dependent (unfused form): the set-up above
+  // overlaps the previous kernel's tail; e, the mask and h are read only
+  // after it has finished.
+  if (!kFuse) wait_prior_grids();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -753,6 +757,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  // Launched as a programmatic dependent (unfused form): the set-up above
+  // overlaps the previous kernel's tail; e, the mask and h are read only
+  // after it has finished.
+  if (!kFuse) wait_prior_grids();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1850,6 +1858,11 @@ int launch(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB
   if (fused && use_cooperative()) {
     attr[nattr].id = cudaLaunchAttributeCooperative;
     attr[nattr].val.cooperative = 1;
+    ++nattr;
+  }
+  if (!fused) {  // the unfused kernels wait for the previous grid in-kernel
+    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
     ++nattr;
   }
   const int n = a.num_tiles < units ? a.num_tiles : units;
