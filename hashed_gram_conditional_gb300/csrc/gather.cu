@@ -85,7 +85,12 @@ __device__ __forceinline__ uint4 dequant8(uint2 w, uint32_t sbyte) {
 
 __global__ void __launch_bounds__(kWarps * 32, 1) gather_dequant_kernel(GatherArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  allow_dependent_launch();  // a following history commit may load its inputs meanwhile
+  // Launched as a programmatic dependent: nothing is read before the
+  // previous kernel has finished, and a following history commit may start
+  // (and load its inputs) only after that, never ahead of this kernel's own
+  // predecessor.
+  wait_prior_grids();
+  allow_dependent_launch();
   const int w = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const uint32_t stage_bytes = static_cast<uint32_t>(a.n_cols) * kSlot;
@@ -323,7 +328,12 @@ struct Fp8Out {
 template <class RowSource, class Out>
 __global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArgs a, RowSource src, Out store) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  allow_dependent_launch();  // a following history commit may load its inputs meanwhile
+  // Launched as a programmatic dependent: nothing is read before the
+  // previous kernel has finished, and a following history commit may start
+  // (and load its inputs) only after that, never ahead of this kernel's own
+  // predecessor.
+  wait_prior_grids();
+  allow_dependent_launch();
   const int w = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const uint32_t stage_bytes = static_cast<uint32_t>(a.n_cols) * kSlot;
@@ -462,7 +472,18 @@ int launch_ldgsts(const GatherArgs& a, const RowSource& src, const Out& out, siz
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaFuncSetAttribute(gather): %s", cudaGetErrorString(err));
   // one CTA per SM, or one per position when there are fewer positions
   const int blocks = static_cast<int>(a.n_tokens < sms ? a.n_tokens : sms);
-  gather_ldgsts_kernel<RowSource, Out><<<blocks, kWarps * 32, smem, st>>>(a, src, out);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;  // the launch overlaps the previous kernel's tail
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, gather_ldgsts_kernel<RowSource, Out>, a, src, out);
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "gather_ldgsts_kernel launch: %s", cudaGetErrorString(err));
   return check_launch("gather_ldgsts_kernel");
 }
 

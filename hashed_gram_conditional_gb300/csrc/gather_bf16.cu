@@ -28,7 +28,12 @@ __global__ void __launch_bounds__(kWarpsB * 32) gather_rows_bf16_kernel(
     int64_t n_tokens, int32_t n_cols, uint16_t* __restrict__ e, int32_t* status, hashdev::HashConsts c,
     const int32_t* __restrict__ raw, const int64_t* __restrict__ cu, int32_t n_seqs,
     const int32_t* __restrict__ tmap, const int32_t* __restrict__ hist, int32_t* rows_out, uint8_t* mask) {
-  allow_dependent_launch();  // a following history commit may load its inputs meanwhile
+  // Launched as a programmatic dependent: nothing is read before the
+  // previous kernel has finished, and a following history commit may start
+  // (and load its inputs) only after that, never ahead of this kernel's own
+  // predecessor.
+  wait_prior_grids();
+  allow_dependent_launch();
   const uint32_t lane = lane_id();
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -106,14 +111,27 @@ int launch_rows_bf16(bool hash, const uint16_t* table_d, int64_t total_rows, int
   const int64_t want = (n_tokens + kWarpsB - 1) / kWarpsB;
   const int64_t cap = static_cast<int64_t>(sms) * 8;  // 64 warps per SM
   const int blocks = static_cast<int>(want < cap ? want : cap);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kWarpsB * 32);
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;  // the launch overlaps the previous kernel's tail
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cudaError_t err;
   if (hash)
-    gather_rows_bf16_kernel<true><<<blocks, kWarpsB * 32, 0, st>>>(table_d, total_rows, row_dim, nullptr, n_tokens,
-                                                                  n_cols, e_d, status_d, c, raw, cu, n_seqs, tmap,
-                                                                  hist, rows_out, mask);
+    err = cudaLaunchKernelEx(&cfg, gather_rows_bf16_kernel<true>, table_d, total_rows, row_dim,
+                             static_cast<const int32_t*>(nullptr), n_tokens, n_cols, e_d, status_d, c, raw, cu,
+                             n_seqs, tmap, hist, rows_out, mask);
   else
-    gather_rows_bf16_kernel<false><<<blocks, kWarpsB * 32, 0, st>>>(table_d, total_rows, row_dim, row_ids_d,
-                                                                   n_tokens, n_cols, e_d, status_d, c, nullptr,
-                                                                   nullptr, 0, nullptr, nullptr, nullptr, nullptr);
+    err = cudaLaunchKernelEx(&cfg, gather_rows_bf16_kernel<false>, table_d, total_rows, row_dim, row_ids_d, n_tokens,
+                             n_cols, e_d, status_d, c, static_cast<const int32_t*>(nullptr),
+                             static_cast<const int64_t*>(nullptr), 0, static_cast<const int32_t*>(nullptr),
+                             static_cast<const int32_t*>(nullptr), static_cast<int32_t*>(nullptr),
+                             static_cast<uint8_t*>(nullptr));
+  if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "gather_rows_bf16_kernel launch: %s", cudaGetErrorString(err));
   return check_launch("gather_rows_bf16_kernel");
 }
 

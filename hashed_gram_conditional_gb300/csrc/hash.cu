@@ -63,29 +63,34 @@ __global__ void __launch_bounds__(256) hash_all_layers_kernel(
 // most recent first, falling back to the previous history for short chunks.
 // One thread per sequence reads all it needs before writing its own row.
 // It is launched as a programmatic dependent of the kernel that hashed the
-// chunk: that kernel writes none of what is read here, only reads the old
-// history, so the loads run early and only the writes wait for it.
+// chunk.  No kernel of the path writes the raw ids, the sequence bounds or the
+// token map, so those loads run early; the old history is read, and the new
+// one written, only once that kernel has finished (it reads the old history,
+// and a decode-step gather before it would be writing it).
 __global__ void hash_commit_kernel(HashConsts c, const int32_t* __restrict__ raw,
                                    const int64_t* __restrict__ cu, int32_t n_seqs,
                                    const int32_t* __restrict__ tmap, int32_t* hist,
                                    int32_t* status) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
-  if (s >= n_seqs) return;
+  const bool live = s < n_seqs;
   const int depth = c.max_ngram - 1;
-  const int64_t start = cu[s], end = cu[s + 1];
+  const int64_t start = live ? cu[s] : 0, end = live ? cu[s + 1] : 0;
   const int64_t len = end - start;
   int32_t nh[ENGRAM_MAX_NGRAM - 1];
 #pragma unroll
   for (int i = 0; i < ENGRAM_MAX_NGRAM - 1; ++i) {
     if (i >= depth) break;
     const int64_t pos = end - 1 - i;
-    if (pos >= start) {
-      nh[i] = compress_id(raw[pos], tmap, c, nullptr);  // errors already reported by the hash
-    } else {
-      nh[i] = hist[static_cast<int64_t>(s) * depth + (i - len)];
-    }
+    if (live && pos >= start) nh[i] = compress_id(raw[pos], tmap, c, nullptr);  // errors reported by the hash
   }
   wait_prior_grids();  // every position of the chunk has read the old history
+  if (!live) return;
+#pragma unroll
+  for (int i = 0; i < ENGRAM_MAX_NGRAM - 1; ++i) {
+    if (i >= depth) break;
+    const int64_t pos = end - 1 - i;
+    if (pos < start) nh[i] = hist[static_cast<int64_t>(s) * depth + (i - len)];
+  }
 #pragma unroll
   for (int i = 0; i < ENGRAM_MAX_NGRAM - 1; ++i) {
     if (i >= depth) break;

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import hashed_gram_conditional_gb300 as eg
-from gpu_util import DEV, i32, i64, require_gpu, setup, status
+from gpu_util import DEV, device_table, i32, i64, require_gpu, setup, status
 from oracle import hashing as OH
 from oracle import layout as OL
 from workloads import DEAD, WORKLOADS, decode_workload, prefill_batch, zipf_tokens
@@ -189,3 +189,31 @@ def test_hash_zero_tokens_keeps_history():
     assert (hist_d.cpu().numpy() == hist0).all()
     _, _, hist_o = OH.hash_prefill(np.zeros(0, dtype=np.int32), cu, tm, lay_o, 0, hist=hist0.astype(np.int64))
     assert (hist_o == hist0).all()
+
+
+def test_history_commit_after_a_decode_step():
+    """A decode step (which rolls the history inside its gather kernel) and,
+    straight after it on the stream, prefill chunks of one token per sequence:
+    the chunk's history commit must build on the step's history, not on the
+    one before it."""
+    w, tm, lay_o, lay = setup("tiny")
+    table = device_table(lay_o.layers[0].total_rows, w.seed)
+    S = 6
+    rng = np.random.default_rng(5)
+    hist0 = rng.integers(0, w.v, size=(S, 3)).astype(np.int32)
+    step_raw = rng.integers(0, w.v_raw, size=S).astype(np.int32)
+    chunk_raw = rng.integers(0, w.v_raw, size=S).astype(np.int32)
+    slots = np.arange(S, dtype=np.int32)
+    _, _, h1 = OH.hash_step(step_raw, slots, hist0.astype(np.int64), tm, lay_o, 0)
+    cu = np.arange(S + 1, dtype=np.int64)
+    _, _, h2 = OH.hash_prefill(chunk_raw, cu, tm, lay_o, 0, hist=h1)
+    for _ in range(3):  # back to back, several times
+        hist_d = i32(hist0)
+        st = status()
+        eg.engram_hash_gather_step(lay, 0, i32(step_raw), i32(slots), i32(tm), table, hist_d, status=st)
+        eg.engram_hash(lay, 0, i32(chunk_raw), i64(cu), i32(tm), hist_d, status=st)
+        eg.engram_hash(lay, 0, i32(np.zeros(0, dtype=np.int32)), i64(np.zeros(S + 1, dtype=np.int64)), i32(tm),
+                       hist_d, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert (hist_d.cpu().numpy() == h2).all()
