@@ -213,19 +213,28 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Where the row ids of a position come from: read from memory (or the
-// identity t * n_cols + j for contiguous rows) ...
+// Where the row ids of a position come from.  A warp takes its positions t0,
+// t0 + stride, ... in order; fetch() loads the source words of a batch of
+// batch() consecutive ones in one warp load, and operator() turns the words
+// into position k's row id of column `lane` (warp-collective).  The kernel
+// fetches the next batch while the current one's copies are in flight.
+//
+// Row ids read from memory (or the identity t * n_cols + j for contiguous
+// rows), one position per batch ...
 struct IdRows {
   const int32_t* rows;
-  __device__ __forceinline__ int32_t operator()(int64_t t, uint32_t lane, int n_cols) const {
-    if (lane >= static_cast<uint32_t>(n_cols)) return -1;
-    return rows != nullptr ? __ldg(rows + t * n_cols + lane) : static_cast<int32_t>(t * n_cols + lane);
+  __device__ __forceinline__ int batch() const { return 1; }
+  __device__ __forceinline__ int32_t fetch(int64_t t0, int64_t, int64_t n_tokens, uint32_t lane, int n_cols) const {
+    if (t0 >= n_tokens || lane >= static_cast<uint32_t>(n_cols)) return -1;
+    return rows != nullptr ? __ldg(rows + t0 * n_cols + lane) : static_cast<int32_t>(t0 * n_cols + lane);
   }
+  __device__ __forceinline__ int32_t operator()(int32_t word, int, int64_t, uint32_t, int) const { return word; }
 };
 
 // ... or computed in the warp from the position's token window (the fused
 // hash + gather: the row ids need not round-trip through memory; they and
-// the mask are still written when asked for).
+// the mask are still written when asked for).  One fetch loads the window
+// slots of 32 / max_ngram positions.
 struct HashedRows {
   hashdev::HashConsts c;
   const int32_t* raw;
@@ -236,10 +245,13 @@ struct HashedRows {
   int32_t* rows_out;  // or null
   uint8_t* mask;
   int32_t* status;
-  __device__ __forceinline__ int32_t operator()(int64_t t, uint32_t lane, int n_cols) const {
-    const int32_t slot = hashdev::prefill_slot(c, t, raw, cu, n_seqs, tmap, hist, status);
+  __device__ __forceinline__ int batch() const { return 32 / c.max_ngram; }
+  __device__ __forceinline__ int32_t fetch(int64_t t0, int64_t stride, int64_t n_tokens, uint32_t, int) const {
+    return hashdev::prefill_slot_batch(c, t0, stride, n_tokens, raw, cu, n_seqs, tmap, hist, status);
+  }
+  __device__ __forceinline__ int32_t operator()(int32_t word, int k, int64_t t, uint32_t lane, int n_cols) const {
     int32_t row;
-    const bool dead = hashdev::window_rows(slot, c, &row);
+    const bool dead = hashdev::window_rows(word, c, &row, k * c.max_ngram);
     if (rows_out != nullptr && lane < static_cast<uint32_t>(n_cols)) rows_out[t * n_cols + lane] = row;
     if (lane == 0) mask[t] = dead ? 1 : 0;
     return row;
@@ -248,7 +260,8 @@ struct HashedRows {
 
 // ... or computed from a decode entry's new id and its carried history, the
 // history rolled in the same warp once every lane has read its slot (entries
-// of one call name distinct slots, so no other warp touches it).
+// of one call name distinct slots, so no other warp touches it).  Nothing is
+// fetched ahead: the entry reads its slot's history when it is issued.
 struct StepRows {
   hashdev::HashConsts c;
   const int32_t* raw;
@@ -259,7 +272,9 @@ struct StepRows {
   int32_t* rows_out;  // or null
   uint8_t* mask;
   int32_t* status;
-  __device__ __forceinline__ int32_t operator()(int64_t b, uint32_t lane, int n_cols) const {
+  __device__ __forceinline__ int batch() const { return 1; }
+  __device__ __forceinline__ int32_t fetch(int64_t, int64_t, int64_t, uint32_t, int) const { return 0; }
+  __device__ __forceinline__ int32_t operator()(int32_t, int, int64_t b, uint32_t lane, int n_cols) const {
     bool pad_row;
     int32_t xnew;
     const int32_t slot = hashdev::step_slot(c, b, raw, slots, tmap, hist, n_slots, status, &pad_row, &xnew);
@@ -355,8 +370,21 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArg
   const int n_cols = a.n_cols;
   const int pieces = n_cols * 17;
 
-  auto issue = [&](int64_t t, int s) {
-    const int32_t r = src(t, lane, n_cols);  // warp-collective
+  // the source words of the batch holding the next position to issue, and
+  // of the batch after it (fetched once that batch's first copies are out)
+  const int B = src.batch();
+  int64_t qb = 0;  // the current batch's first position, counted per warp
+  int32_t cur = src.fetch(gw, nw, a.n_tokens, lane, n_cols);
+  int32_t nxt = 0;
+
+  // issues the copies of the warp's position q (t = gw + q * nw) into stage s
+  auto issue = [&](int64_t q, int s) {
+    if (q == qb + B) {
+      cur = nxt;
+      qb += B;
+    }
+    const int64_t t = gw + q * nw;
+    const int32_t r = src(cur, static_cast<int>(q - qb), t, lane, n_cols);  // warp-collective
     bool valid = false;
     if (lane < static_cast<uint32_t>(n_cols)) {
       valid = r >= 0 && static_cast<int64_t>(r) < a.total_rows;
@@ -379,19 +407,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArg
       const int piece = p - 17 * row;
       const int rr = __shfl_sync(0xffffffffu, r, row < 32 ? row : 0);
       if (p < pieces && ((vmask >> row) & 1u)) {
-        const uint8_t* src = a.table + ((static_cast<int64_t>(rr) * kRowBytes) & ~int64_t(15)) + piece * 16;
+        const uint8_t* from = a.table + ((static_cast<int64_t>(rr) * kRowBytes) & ~int64_t(15)) + piece * 16;
         const uint32_t dst = sbase + row * kSlot + piece * 16;
-        if (piece == 16 && ((tmask >> row) & 1u)) cp_async8(dst, src);
-        else cp_async16(dst, src);
+        if (piece == 16 && ((tmask >> row) & 1u)) cp_async8(dst, from);
+        else cp_async16(dst, from);
       }
     }
     cp_async_arrive(smem_u32(&bars[s]));
+    if (q == qb) nxt = src.fetch(gw + (qb + B) * nw, nw, a.n_tokens, lane, n_cols);
   };
 
-  for (int s = 0; s < S; ++s) {
-    const int64_t t = gw + s * nw;
-    if (t < a.n_tokens) issue(t, s);
-  }
+  for (int s = 0; s < S; ++s)
+    if (gw + s * nw < a.n_tokens) issue(s, s);
 
   int64_t k = 0;
   bool timed_out = false;
@@ -406,8 +433,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) gather_ldgsts_kernel(GatherArg
     }
     store(wbuf + static_cast<size_t>(s) * stage_bytes, masks[2 * s], masks[2 * s + 1], t, n_cols, lane);
     __syncwarp();
-    const int64_t t2 = t + static_cast<int64_t>(S) * nw;
-    if (t2 < a.n_tokens) issue(t2, s);
+    if (t + static_cast<int64_t>(S) * nw < a.n_tokens) issue(k + S, s);
   }
   if (timed_out) {
     if (lane == 0 && a.status) atomicOr(a.status, static_cast<int>(ENGRAM_ST_TIMEOUT));

@@ -97,11 +97,11 @@ __device__ __forceinline__ int32_t check_hist(int32_t x, const HashConsts& c, in
   return x;
 }
 
-// Given the window slot held by lane i < max_ngram (slot i = x'_{t-i}),
-// applies the DEAD cascade and forms the mixes; lane j < n_cols gets the row
-// id of column j (other lanes -1).  Returns whether the position itself is
-// DEAD.  All 32 lanes call it.
-__device__ __forceinline__ bool window_rows(int32_t my_slot, const HashConsts& c, int32_t* row) {
+// Given the window slot held by lane base + i, i < max_ngram (slot i =
+// x'_{t-i}), applies the DEAD cascade and forms the mixes; lane j < n_cols
+// gets the row id of column j (other lanes -1).  Returns whether the position
+// itself is DEAD.  All 32 lanes call it.
+__device__ __forceinline__ bool window_rows(int32_t my_slot, const HashConsts& c, int32_t* row, int base = 0) {
   const uint32_t lane = lane_id();
   // [P-V41] image tokens / [P-LMNT] §多模态细节: looking back, the first DEAD
   // slot and every slot farther back count as pad.
@@ -110,7 +110,7 @@ __device__ __forceinline__ bool window_rows(int32_t my_slot, const HashConsts& c
   bool self_dead = false;
 #pragma unroll
   for (int i = 0; i < ENGRAM_MAX_NGRAM; ++i) {
-    int32_t v = __shfl_sync(0xffffffffu, my_slot, i);
+    int32_t v = __shfl_sync(0xffffffffu, my_slot, (base + i) & 31);
     if (i < c.max_ngram) {
       if (v == kDead) {
         dead_seen = true;
@@ -147,14 +147,13 @@ __device__ __forceinline__ void hash_window(int32_t my_slot, const HashConsts& c
   if (lane == 0) *mask_out = (self_dead || force_mask) ? 1 : 0;
 }
 
-// The window slot of lane i < max_ngram for prefill position t of packed
-// sequences (x'_{t-i}, or carried history / pad before the sequence start);
-// other lanes return pad.  Also returns the sequence index.
-__device__ __forceinline__ int32_t prefill_slot(const HashConsts& c, int64_t t, const int32_t* __restrict__ raw,
-                                                const int64_t* __restrict__ cu, int32_t n_seqs,
-                                                const int32_t* __restrict__ tmap, const int32_t* __restrict__ hist,
-                                                int32_t* status) {
-  const uint32_t lane = lane_id();
+// Window slot i of prefill position t of packed sequences: x'_{t-i}, or the
+// carried history (most recent first) / pad before the sequence start.  Any
+// lane may ask for any (t, i).
+__device__ __forceinline__ int32_t prefill_slot_at(const HashConsts& c, int64_t t, int i,
+                                                   const int32_t* __restrict__ raw, const int64_t* __restrict__ cu,
+                                                   int32_t n_seqs, const int32_t* __restrict__ tmap,
+                                                   const int32_t* __restrict__ hist, int32_t* status) {
   const int depth = c.max_ngram - 1;
   // sequence of position t: largest s with cu[s] <= t
   int lo = 0, hi = n_seqs - 1;
@@ -163,18 +162,41 @@ __device__ __forceinline__ int32_t prefill_slot(const HashConsts& c, int64_t t, 
     if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
   }
   const int64_t start = __ldg(cu + lo);
-  int32_t slot = c.pad_id;
-  if (lane < static_cast<uint32_t>(c.max_ngram)) {
-    const int64_t src = t - static_cast<int64_t>(lane);
-    if (src >= start) {
-      slot = compress_id(__ldg(raw + src), tmap, c, status);
-    } else if (hist != nullptr) {
-      // before the chunk start: carried history, most recent first
-      const int64_t hidx = static_cast<int64_t>(lane) - 1 - (t - start);
-      slot = check_hist(__ldg(hist + static_cast<int64_t>(lo) * depth + hidx), c, status);
-    }
+  const int64_t src = t - static_cast<int64_t>(i);
+  if (src >= start) return compress_id(__ldg(raw + src), tmap, c, status);
+  if (hist != nullptr) {
+    const int64_t hidx = static_cast<int64_t>(i) - 1 - (t - start);
+    return check_hist(__ldg(hist + static_cast<int64_t>(lo) * depth + hidx), c, status);
   }
-  return slot;
+  return c.pad_id;
+}
+
+// The window slot of lane i < max_ngram for prefill position t (other lanes
+// return pad).
+__device__ __forceinline__ int32_t prefill_slot(const HashConsts& c, int64_t t, const int32_t* __restrict__ raw,
+                                                const int64_t* __restrict__ cu, int32_t n_seqs,
+                                                const int32_t* __restrict__ tmap, const int32_t* __restrict__ hist,
+                                                int32_t* status) {
+  const uint32_t lane = lane_id();
+  if (lane >= static_cast<uint32_t>(c.max_ngram)) return c.pad_id;
+  return prefill_slot_at(c, t, static_cast<int>(lane), raw, cu, n_seqs, tmap, hist, status);
+}
+
+// The window slots of a batch of prefill positions t0 + k * stride, k <
+// 32 / max_ngram, in one warp load: lane k * max_ngram + i holds slot i of
+// position k (pad past n_tokens and on the lanes left over).  window_rows
+// with base k * max_ngram then forms position k's row ids.
+__device__ __forceinline__ int32_t prefill_slot_batch(const HashConsts& c, int64_t t0, int64_t stride,
+                                                      int64_t n_tokens, const int32_t* __restrict__ raw,
+                                                      const int64_t* __restrict__ cu, int32_t n_seqs,
+                                                      const int32_t* __restrict__ tmap,
+                                                      const int32_t* __restrict__ hist, int32_t* status) {
+  const int lane = static_cast<int>(lane_id());
+  const int k = lane / c.max_ngram;
+  const int i = lane - k * c.max_ngram;
+  const int64_t t = t0 + static_cast<int64_t>(k) * stride;
+  if (k >= 32 / c.max_ngram || t >= n_tokens) return c.pad_id;
+  return prefill_slot_at(c, t, i, raw, cu, n_seqs, tmap, hist, status);
 }
 
 // The window slot of lane i < max_ngram for decode entry b: lane 0 the new
