@@ -909,7 +909,7 @@ def decode_bench(args, w, inp, layer, flush, dev):
     eg.engram_hash(layer.layout, 0, torch.from_numpy(dw.prefix.raw_ids).to(dev),
                    torch.from_numpy(dw.prefix.cu_seqlens).to(dev), layer.token_map, hist)
     e8 = torch.empty((B, 6144), dtype=torch.uint8, device=dev)
-    sfa = torch.empty((48, B), dtype=torch.int32, device=dev)
+    sfa = torch.empty((48, eg.sf_cols(B)), dtype=torch.int32, device=dev)
 
     def run8(k, ev=None):
         if ev is not None:
@@ -1054,7 +1054,7 @@ def fp8_bench(args, w, inp, layer, flush, dev):
     h = inp["bf16"](inp["h_bits"])
     hist = torch.full((w.n_seqs, 3), layer.layout.pad_id, dtype=torch.int32, device=dev)
     e8 = torch.empty((T, K), dtype=torch.uint8, device=dev)
-    sfa = torch.empty((2 * 24, T), dtype=torch.int32, device=dev)
+    sfa = torch.empty((2 * 24, eg.sf_cols(T)), dtype=torch.int32, device=dev)
     mask = torch.empty(T, dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)

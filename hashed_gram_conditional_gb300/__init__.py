@@ -26,7 +26,7 @@ __all__ = [
     "engram_pack_wkv", "engram_project", "engram_gate_add", "engram_fill_synthetic_table",
     "engram_selftest_mod", "engram_project_gate", "project_gate_workspace", "partials_shape", "EngramLayer",
     "library_path", "ST_BAD_TOKEN", "ST_BAD_ROW", "ST_BAD_SLOT", "ST_TIMEOUT", "DEAD", "ROW_BYTES", "DecodeGraph",
-    "set_kernel_options", "kernel_options",
+    "set_kernel_options", "kernel_options", "sf_cols", "sf_word_index",
 ]
 
 MAX_LAYERS = 8
@@ -35,6 +35,19 @@ MAX_COLS = 32
 DEAD = -1
 ROW_BYTES = 264
 HEAD_DIM = 256
+
+
+def sf_cols(n_tokens: int) -> int:
+    """Words per k-block row of a block-FP8 scale array for n_tokens positions:
+    n_tokens rounded up to a multiple of 128."""
+    return (n_tokens + 127) // 128 * 128
+
+
+def sf_word_index(i):
+    """Word of position (or wkv column) i within a k-block row of a block-FP8
+    scale array: the 16 bytes at word 4 r of each 128-word block hold rows r,
+    r + 32, r + 64 and r + 96 (the image the tensor cores' scale copy reads)."""
+    return (i & ~127) | ((i & 31) << 2) | ((i >> 5) & 3)
 ST_BAD_TOKEN, ST_BAD_ROW, ST_BAD_SLOT, ST_TIMEOUT = 1, 2, 4, 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -447,9 +460,9 @@ def engram_hash_gather_step_fp8(layout: Layout, layer: int, raw_ids: torch.Tenso
     if e8 is None:
         e8 = torch.empty((B, C * HEAD_DIM), dtype=torch.uint8, device=dev)
     if sf is None:
-        sf = torch.empty((2 * C, B), dtype=torch.int32, device=dev)
+        sf = torch.empty((2 * C, sf_cols(B)), dtype=torch.int32, device=dev)
     _need(e8, "e8", torch.uint8, dev, B * C * HEAD_DIM)
-    _need(sf, "sf", torch.int32, dev, 2 * C * B)
+    _need(sf, "sf", torch.int32, dev, 2 * C * sf_cols(B))
     _check(L.engram_hash_gather_step_fp8(layout.ref, layer, _ptr(raw_ids), _ptr(slots), B, _ptr(token_map),
                                          token_map.numel(), _ptr(hist), n_slots, _ptr(table), table.numel(),
                                          _ptr(e8), _ptr(sf), _ptr(mask), _ptr(row_ids), _ptr(status), _stream(dev)),
@@ -513,7 +526,8 @@ def engram_hash_gather(layout: Layout, layer: int, raw_ids: torch.Tensor, cu_seq
 def engram_gather_fp8(table: torch.Tensor, total_rows: int, row_ids: torch.Tensor,
                       e8: Optional[torch.Tensor] = None, sf: Optional[torch.Tensor] = None,
                       status: Optional[torch.Tensor] = None):
-    """Gather without dequantising: (e8 uint8 [T][n_cols*256], sf int32 [n_cols*2][T] words of 4 E8M0 scales)."""
+    """Gather without dequantising: (e8 uint8 [T][n_cols*256], sf int32 [n_cols*2][sf_cols(T)] words of 4 E8M0
+    scales, positions in sf_word_index order)."""
     L = _load()
     dev = row_ids.device
     _need(table, "table", torch.uint8, dev)
@@ -522,9 +536,9 @@ def engram_gather_fp8(table: torch.Tensor, total_rows: int, row_ids: torch.Tenso
     if e8 is None:
         e8 = torch.empty((T, C * HEAD_DIM), dtype=torch.uint8, device=dev)
     if sf is None:
-        sf = torch.empty((2 * C, T), dtype=torch.int32, device=dev)
+        sf = torch.empty((2 * C, sf_cols(T)), dtype=torch.int32, device=dev)
     _need(e8, "e8", torch.uint8, dev, T * C * HEAD_DIM)
-    _need(sf, "sf", torch.int32, dev, 2 * C * T)
+    _need(sf, "sf", torch.int32, dev, 2 * C * sf_cols(T))
     _check(L.engram_gather_fp8(_ptr(table), total_rows, table.numel(), _ptr(row_ids), T, C, _ptr(e8), _ptr(sf),
                                _ptr(status), _stream(dev)), "engram_gather_fp8")
     return e8, sf
@@ -550,11 +564,11 @@ def engram_hash_gather_fp8(layout: Layout, layer: int, raw_ids: torch.Tensor, cu
     if e8 is None:
         e8 = torch.empty((T, C * HEAD_DIM), dtype=torch.uint8, device=dev)
     if sf is None:
-        sf = torch.empty((2 * C, T), dtype=torch.int32, device=dev)
+        sf = torch.empty((2 * C, sf_cols(T)), dtype=torch.int32, device=dev)
     if mask is None:
         mask = torch.empty(T, dtype=torch.uint8, device=dev)
     _need(e8, "e8", torch.uint8, dev, T * C * HEAD_DIM)
-    _need(sf, "sf", torch.int32, dev, 2 * C * T)
+    _need(sf, "sf", torch.int32, dev, 2 * C * sf_cols(T))
     _need(mask, "mask", torch.uint8, dev, T)
     if row_ids is not None:
         _need(row_ids, "row_ids", torch.int32, dev, T * C)
@@ -565,7 +579,8 @@ def engram_hash_gather_fp8(layout: Layout, layer: int, raw_ids: torch.Tensor, cu
 
 
 def engram_pack_wkv_fp8(w8: torch.Tensor, sf: torch.Tensor):
-    """Block-FP8 wkv (codes uint8 [K][N], scales uint8 [K/32][N]) -> (packed codes, packed scale words)."""
+    """Block-FP8 wkv (codes uint8 [K][N], scales uint8 [K/32][N]) -> (packed codes, packed scale words
+    [K/128][N], the columns of each 128 in sf_word_index order)."""
     L = _load()
     dev = w8.device
     K, N = w8.shape
@@ -588,7 +603,7 @@ def engram_project_fp8(e8: torch.Tensor, sfa: torch.Tensor, w8p: torch.Tensor, s
     T, K = e8.shape
     _need(h, "h", torch.bfloat16, dev)
     _, hc, H = h.shape
-    _need(sfa, "sfa", torch.int32, dev, (K // 128) * T)
+    _need(sfa, "sfa", torch.int32, dev, (K // 128) * sf_cols(T))
     _need(w8p, "w8p", torch.uint8, dev, K * (hc + 1) * H)
     _need(sfb, "sfb", torch.int32, dev, (K // 128) * (hc + 1) * H)
     if partials is None:
@@ -614,7 +629,7 @@ def engram_project_gate_fp8(e8: torch.Tensor, sfa: torch.Tensor, w8p: torch.Tens
     T, K = e8.shape
     _need(h, "h", torch.bfloat16, dev)
     _, hc, H = h.shape
-    _need(sfa, "sfa", torch.int32, dev, (K // 128) * T)
+    _need(sfa, "sfa", torch.int32, dev, (K // 128) * sf_cols(T))
     _need(w8p, "w8p", torch.uint8, dev, K * (hc + 1) * H)
     _need(sfb, "sfb", torch.int32, dev, (K // 128) * (hc + 1) * H)
     if mask is not None:
@@ -1017,7 +1032,8 @@ class EngramLayer:
                 mask=torch.empty(T, dtype=torch.uint8, device=device),
                 e=torch.empty((T, self.e_dim), dtype=torch.bfloat16, device=device) if not self.fp8 else None,
                 e8=torch.empty((T, self.e_dim), dtype=torch.uint8, device=device) if self.fp8 else None,
-                sf=torch.empty((2 * self.layout.n_cols, T), dtype=torch.int32, device=device) if self.fp8 else None,
+                sf=torch.empty((2 * self.layout.n_cols, sf_cols(T)), dtype=torch.int32, device=device)
+                if self.fp8 else None,
                 partials=torch.empty(partials_shape(T, self.hidden, self.hc), dtype=torch.float32, device=device),
                 v=torch.empty((T, self.hidden), dtype=torch.bfloat16, device=device),
                 work=project_gate_workspace(T, self.hidden, self.hc, device),
@@ -1063,7 +1079,7 @@ class EngramLayer:
                 mask=torch.empty(T, dtype=torch.uint8, device=device),
                 e=torch.empty((T, C * HEAD_DIM), dtype=torch.bfloat16, device=device) if not fp8 else None,
                 e8=torch.empty((T, C * HEAD_DIM), dtype=torch.uint8, device=device) if fp8 else None,
-                sf=torch.empty((2 * C, T), dtype=torch.int32, device=device) if fp8 else None,
+                sf=torch.empty((2 * C, sf_cols(T)), dtype=torch.int32, device=device) if fp8 else None,
                 # the staged rows in order: row t*C + j of the staging buffer is column j of position t
                 staged_ids=(torch.arange(T * C, dtype=torch.int32, device=device).view(T, C)
                             if fp8 and host else None),

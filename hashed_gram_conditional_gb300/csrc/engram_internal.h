@@ -26,6 +26,18 @@ engram_kernel_options kernel_options();
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Word of row (or column) i within a k-block row of a block-FP8 scale array:
+// the words of each 128 consecutive rows are stored so that the 16 bytes at
+// word 4 r hold rows r, r + 32, r + 64 and r + 96 -- the 32-row x 128-bit
+// image that tcgen05.cp.32x128b.warpx4 spreads over the four TMEM lane
+// quarters, in the layout the block-scaled MMA reads.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline int64_t sf_word_index(int64_t i) {
+  return (i & ~int64_t(127)) | ((i & 31) << 2) | ((i >> 5) & 3);
+}
+
 // ------------------------------------------------------------- device side
 #ifdef __CUDACC__
 

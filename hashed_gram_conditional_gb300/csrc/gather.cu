@@ -311,12 +311,15 @@ struct Bf16Out {
 
 // ... or the rows as they are, for the block-scaled FP8 projection: the E4M3
 // bytes concatenated, e8[t][256 j + c], and the E8M0 scales grouped by
-// 128-element k-block, sf[(2 j + b / 4) * T + t] byte b % 4 (so the four
-// scales of one k-block of consecutive positions are contiguous).  A bad row
-// becomes zero bytes with scale 127 (the value 0).
+// 128-element k-block: row kb = 2 j + b / 4 of sf holds T128 words (T rounded
+// up to a multiple of 128), byte b % 4 of position t's word the scale of its
+// 32-element block b of row j, positions in sf_word_index order (so a
+// k-block's scales of 128 positions form the 512-byte image the projection
+// copies to TMEM as it is).  A bad row becomes zero bytes with scale 127 (the
+// value 0); positions T .. T128 - 1 hold scale 127 too.
 struct Fp8Out {
   uint8_t* e8;    // [T][n_cols * 256]
-  uint32_t* sf;   // [n_cols * 2][T] words of four E8M0 bytes
+  uint32_t* sf;   // [n_cols * 2][T128] words of four E8M0 bytes
   int64_t n_tokens;
   __device__ __forceinline__ void operator()(const uint8_t* sb, uint32_t odd, uint32_t vm, int64_t t, int n_cols,
                                              uint32_t lane) const {
@@ -328,10 +331,17 @@ struct Fp8Out {
       *reinterpret_cast<uint2*>(out + j * ENGRAM_HEAD_DIM + lane * 8) = wv;
     }
     if (lane < static_cast<uint32_t>(n_cols)) {
+      const int64_t ld = (n_tokens + 127) & ~int64_t(127);
+      uint32_t* s0 = sf + 2 * static_cast<int64_t>(lane) * ld;
       const uint8_t* row = sb + lane * kSlot + (((odd >> lane) & 1u) ? 8 : 0);
       const uint2 sc = ((vm >> lane) & 1u) ? *reinterpret_cast<const uint2*>(row + 256) : make_uint2(0x7f7f7f7fu, 0x7f7f7f7fu);
-      sf[(2 * static_cast<int64_t>(lane)) * n_tokens + t] = sc.x;
-      sf[(2 * static_cast<int64_t>(lane) + 1) * n_tokens + t] = sc.y;
+      s0[sf_word_index(t)] = sc.x;
+      s0[ld + sf_word_index(t)] = sc.y;
+      if (t == n_tokens - 1)  // the last position also fills the padding of its 128-block
+        for (int64_t p = n_tokens; p < ld; ++p) {
+          s0[sf_word_index(p)] = 0x7f7f7f7fu;
+          s0[ld + sf_word_index(p)] = 0x7f7f7f7fu;
+        }
     }
   }
 };
@@ -588,8 +598,8 @@ extern "C" int engram_gather_fp8(const uint8_t* table_d, int64_t total_rows, int
     return fail(ENGRAM_E_SHAPE, "table_bytes %lld < total_rows * 264", (long long)table_bytes);
   if (n_tokens == 0) return ENGRAM_OK;
   if (!table_d || !e8_d || !sf_d || !row_ids_d) return fail(ENGRAM_E_INVALID, "null device pointer");
-  if (!aligned(table_d, 16) || !aligned(e8_d, 16) || !aligned(sf_d, 4))
-    return fail(ENGRAM_E_ALIGN, "table and e8 must be 16-byte and sf 4-byte aligned");
+  if (!aligned(table_d, 16) || !aligned(e8_d, 16) || !aligned(sf_d, 16))
+    return fail(ENGRAM_E_ALIGN, "table, e8 and sf must be 16-byte aligned");
   int sms = 0;
   int rc = check_device(&sms);
   if (rc) return rc;
@@ -615,8 +625,8 @@ extern "C" int engram_hash_gather_fp8(const engram_layout* layout, int32_t layer
   if (n_tokens == 0 && hist_d == nullptr) return ENGRAM_OK;
   if (!cu_seqlens_d || !token_map_d || (n_tokens > 0 && (!raw_ids_d || !table_d || !e8_d || !sf_d || !mask_d)))
     return fail(ENGRAM_E_INVALID, "null device pointer");
-  if (n_tokens > 0 && (!aligned(table_d, 16) || !aligned(e8_d, 16) || !aligned(sf_d, 4)))
-    return fail(ENGRAM_E_ALIGN, "table and e8 must be 16-byte and sf 4-byte aligned");
+  if (n_tokens > 0 && (!aligned(table_d, 16) || !aligned(e8_d, 16) || !aligned(sf_d, 16)))
+    return fail(ENGRAM_E_ALIGN, "table, e8 and sf must be 16-byte aligned");
   int sms = 0;
   if ((rc = check_device(&sms))) return rc;
   cudaStream_t st = as_stream(stream);
@@ -677,8 +687,8 @@ extern "C" int engram_hash_gather_step_fp8(const engram_layout* layout, int32_t 
                                            const uint8_t* table_d, int64_t table_bytes, uint8_t* e8_d,
                                            uint32_t* sf_d, uint8_t* mask_d, int32_t* row_ids_d, int32_t* status_d,
                                            void* stream) {
-  if (batch > 0 && (sf_d == nullptr || !aligned(sf_d, 4)))
-    return fail(ENGRAM_E_INVALID, "sf must be a 4-byte aligned device pointer");
+  if (batch > 0 && (sf_d == nullptr || !aligned(sf_d, 16)))
+    return fail(ENGRAM_E_INVALID, "sf must be a 16-byte aligned device pointer");
   return hash_gather_step(layout, layer, raw_ids_d, slots_d, batch, token_map_d, vocab_raw, hist_d, n_slots, table_d,
                           table_bytes, e8_d, mask_d, row_ids_d, status_d, stream, Fp8Out{e8_d, sf_d, batch});
 }

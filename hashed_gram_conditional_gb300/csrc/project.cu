@@ -238,12 +238,6 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
       : "memory");
 }
 
-// Arrive on a barrier at a cluster address with the default (CTA-scope)
-// release: for signals whose data is ordered by other means (tcgen05 fences).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
@@ -880,38 +874,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // One CTA per 128 x 256 tile (one M = 128, N = 256 MMA per K = 32 step),
 // k-blocks of 128 bytes (four steps), 4 stages of 48 KB.  The scale factors
-// do not go through TMA: four "scale" warps (one per TMEM lane quarter) read
-// each k-block's scales from global memory and write them to a TMEM scale
-// slot with tcgen05.st in the layout the MMA reads -- lane L, column c, byte
-// k holds the scale of row (L mod 32) + 32 c for k-step k (c < 4 for the 128
-// rows of A, c < 8 for the 256 rows of B), replicated in every lane quarter
-// (established on GB300 by a standalone probe).  A slot is rewritten only
-// after the MMAs that read it have completed (its own sf_empty commit).
-// TMEM: the 256-column accumulator plus the scale slots, which leaves no
-// room for a second accumulator: the epilogue stalls the tensor pipe from
-// the last MMA of a tile to the accumulator's release, so the unfused form
-// keeps that window short (epilogue8_split).  The fused form reuses the bf16
-// kernels' epilogue.
+// travel with the operands: each stage also holds the k-block's scale words
+// of the tile's 128 rows of A and 256 rows of B (TMA, 1.5 KB), and the MMA
+// thread copies them into TMEM with tcgen05.cp ahead of the k-block's MMAs
+// (the tensor pipe runs a thread's copies and MMAs in issue order).  The
+// layout the MMA reads -- lane L, column c, byte k holds the scale of row
+// (L mod 32) + 32 c for k-step k (c < 4 for the 128 rows of A, c < 8 for the
+// 256 rows of B), the same in every lane quarter (established on GB300 by a
+// standalone probe) -- is what tcgen05.cp.32x128b.warpx4 makes of a 512-byte
+// image whose 16-byte row r holds the words of rows r, r + 32, r + 64 and
+// r + 96; the scale arrays are stored in that order (sf_word_index).  Each
+// stage has its own TMEM scale slot, rewritten only after the stage's MMAs
+// have completed.  TMEM: the 256-column accumulator plus the slots, which
+// leaves no room for a second accumulator: the epilogue stalls the tensor
+// pipe from the last MMA of a tile to the accumulator's release, so the
+// unfused form keeps that window short (epilogue8_split).  The fused form
+// reuses the bf16 kernels' epilogue.
 constexpr int BK8 = 128;  // bytes = elements per k-block
 constexpr int STAGES8 = 4;
 constexpr int A8_BYTES = BM * BK8;
 constexpr int B8_BYTES = BN * BK8;
+constexpr int SF_A_BYTES = BM * 4;  // a k-block's scale words of 128 rows of A
+constexpr int SF_BYTES = SF_A_BYTES + BN * 4;  // ... and of 256 rows of B
 constexpr int STAGE8_BYTES = A8_BYTES + B8_BYTES;
-constexpr int kThreads8 = 320;  // producer, MMA, 4 epilogue, 4 scale warps
+constexpr int kThreads8 = 192;  // producer, MMA, 4 epilogue warps
 constexpr int kSfCols = 12;     // per scale slot: A (4 columns), B (8 columns)
-constexpr int kSfBase = BN;     // scale slots after the accumulator
-// Scale slots, more than the operand stages: a slot is freed by its own
-// commit (sf_empty) once the k-block's MMAs are done, so the scale warps run
-// ahead of the operand loads and their writes are never what the MMAs wait
-// for.  TMEM: 256 + 8 x 12 (single CTA) and 256 + 12 x 12 (pair) columns.
-constexpr int kSfSlots8 = 8;
-constexpr int kSfSlots82 = 12;
+constexpr int kSfBase = BN;     // scale slots after the accumulator, one per stage
 constexpr int TMEM8_COLS = 512;
-
-struct __align__(8) Ctl8 {
-  uint64_t sf_full[kSfSlots8];
-  uint64_t sf_empty[kSfSlots8];
-};
 
 // kind::mxf8f6f4 instruction descriptor: A and B E4M3, K-major, N = 256,
 // M = 128, E8M0 scales, both scale-factor ids = the k-step (byte of the
@@ -932,18 +921,45 @@ __device__ __forceinline__ void tc_mma8(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
-__device__ __forceinline__ void tc_st4(uint32_t taddr, const uint32_t (&r)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
-               "r"(r[2]), "r"(r[3])
-               : "memory");
+// Shared-memory descriptor of a 32-row x 16-byte scale image for tcgen05.cp:
+// no swizzle, 8-row core matrices of 128 bytes stored one after another
+// (stride byte offset 128 B; the leading byte offset is unused with a single
+// core matrix along the row), descriptor version 1.
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
+// 32 rows x 128 bits from shared memory into 4 TMEM columns, the same rows in
+// each of the four lane quarters (warpx4).  The pair form copies in both CTAs
+// of the pair, each from its own shared memory into its own TMEM.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// 2-D TMA load into this CTA's shared memory, no swizzle handling needed by
+// the caller (the tensor map fixes the layout).
+__device__ __forceinline__ void tma_load_sf(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
 // Unfused FP8 projection (partial sums of the key tiles, bf16 v): 16 warps.
-// Warp 0 loads operands, warp 1 issues the MMAs, warps 4..7 write the scale
-// factors (warp w may only reach TMEM lane quarter w & 3), warps 8..15 are
-// the epilogue, two per lane quarter (warp w: quarter w & 3, tile columns
-// half * 128 .. +127 with half = (w >> 2) & 1).  Warps 2 and 3 idle.  The
-// fused form keeps the 10-warp layout of kThreads8.
+// Warp 0 loads operands and scales, warp 1 copies the scales to TMEM and
+// issues the MMAs, warps 8..15 are the epilogue, two per lane quarter (warp
+// w: quarter w & 3, tile columns half * 128 .. +127 with half = (w >> 2) &
+// 1; a warp may only reach TMEM lane quarter w & 3).  Warps 2..7 idle.  The
+// fused form has the 6-warp layout of kThreads8.
 constexpr int kThreads8u = 512;
 
 // The two halves of a key tile's partial sums meet in shared memory: the
@@ -1111,75 +1127,29 @@ __device__ __forceinline__ void epilogue8_split(const ProjArgs& a, SmemCtl* ctl,
   }
 }
 
-// Walks the (tile, k-block) sequence of one CTA (or CTA pair) for the scale
-// warps: pa points at the k-block's A-scale word of row m0 (the first row of
-// this CTA's 128), pb at its B-scale word of column n0 + lane.  The tile
-// coordinates are derived only when the walk enters a new tile.
-struct SfCursor {
-  int tile, stride, group, mtiles, rows_per_tile, row_off, kb;
-  int64_t m0;
-  const uint32_t* pa;
-  const uint32_t* pb;
-
-  __device__ __forceinline__ void enter(const ProjArgs& a, const uint32_t* sfa, const uint32_t* sfb,
-                                        uint32_t lane) {
-    kb = 0;
-    if (tile >= a.num_tiles) return;
-    int mb, nb;
-    tile_coords(tile, mtiles, a.nt, group, mb, nb);
-    m0 = static_cast<int64_t>(mb) * rows_per_tile + row_off;
-    pa = sfa + m0;
-    pb = sfb + static_cast<int64_t>(nb) * BN + lane;
-  }
-  __device__ __forceinline__ void start(const ProjArgs& a, int first, int step, int grp, int mt, int rows,
-                                        int off, const uint32_t* sfa, const uint32_t* sfb, uint32_t lane) {
-    tile = first;
-    stride = step;
-    group = grp;
-    mtiles = mt;
-    rows_per_tile = rows;
-    row_off = off;
-    enter(a, sfa, sfb, lane);
-  }
-  __device__ __forceinline__ void next(const ProjArgs& a, int nkb, const uint32_t* sfa, const uint32_t* sfb,
-                                       int64_t N, uint32_t lane) {
-    if (++kb < nkb) {
-      pa += a.M;
-      pb += N;
-      return;
-    }
-    tile += stride;
-    enter(a, sfa, sfb, lane);
-  }
-};
-
-// sfa: [K/128][M] words (four E8M0 bytes: the k-block's four 32-element
-// scales of a row); sfb: [K/128][N] words likewise for the rows of wkv^T.
+// tmSA: the A scale words [K/128][T128] (four E8M0 bytes: the k-block's four
+// 32-element scales of a row, rows in sf_word_index order within each 128);
+// tmSB: [K/128][N] words likewise for the rows of wkv^T.
 template <bool kFuse>
 __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
-    project8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ProjArgs a,
-                    const uint32_t* __restrict__ sfa, const uint32_t* __restrict__ sfb) {
+    project8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, ProjArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = smem;
   uint8_t* smB = smem + STAGES8 * A8_BYTES;
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + STAGES8 * STAGE8_BYTES);
-  Ctl8* ctl8 = reinterpret_cast<Ctl8*>(ctl + 1);
-  Comb8* comb = reinterpret_cast<Comb8*>((reinterpret_cast<uintptr_t>(ctl8 + 1) + 15) & ~uintptr_t(15));
+  uint8_t* smS = smem + STAGES8 * STAGE8_BYTES;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smS + STAGES8 * SF_BYTES);
+  Comb8* comb = reinterpret_cast<Comb8*>((reinterpret_cast<uintptr_t>(ctl + 1) + 15) & ~uintptr_t(15));
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const int nkb = a.K / BK8;
-  const int64_t N = static_cast<int64_t>(a.hc + 1) * a.H;
   volatile int* abort_flag = &ctl->abort;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES8; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
-    }
-    for (int j = 0; j < kSfSlots8; ++j) {
-      mbar_init(smem_u32(&ctl8->sf_full[j]), 4);
-      mbar_init(smem_u32(&ctl8->sf_empty[j]), 1);
     }
     mbar_init(smem_u32(&ctl->tfull[0]), 1);
     mbar_init(smem_u32(&ctl->tempty[0]), kFuse ? 4 : 8);
@@ -1190,6 +1160,8 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSA);
+    prefetch_tmap(&tmSB);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -1220,9 +1192,11 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
             break;
           }
           const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, STAGE8_BYTES);
+          mbar_arrive_expect_tx(fb, STAGE8_BYTES + SF_BYTES);
           tma_load_2d(smem_u32(smA + s * A8_BYTES), &tmA, kb * BK8, mb * BM, fb);
           tma_load_4d(smem_u32(smB + s * B8_BYTES), &tmB, kb, nb * (BN / 128), fb);
+          tma_load_sf(smem_u32(smS + s * SF_BYTES), &tmSA, mb * BM, kb, fb);
+          tma_load_sf(smem_u32(smS + s * SF_BYTES + SF_A_BYTES), &tmSB, nb * BN, kb, fb);
         }
       }
       for (int j = (it > STAGES8 ? it - STAGES8 : 0); j < it; ++j)
@@ -1243,9 +1217,7 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % STAGES8;
           const uint32_t ph = (it / STAGES8) & 1;
-          const int j = it % kSfSlots8;
-          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag) ||
-              !mbar_wait_bounded(smem_u32(&ctl8->sf_full[j]), (it / kSfSlots8) & 1, abort_flag)) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag)) {
             if (!*abort_flag) raise_abort(ctl, a);
             ok = false;
             break;
@@ -1253,13 +1225,17 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(smA + s * A8_BYTES);
           const uint32_t b0 = smem_u32(smB + s * B8_BYTES);
-          const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + j * kSfCols);
+          const uint32_t s0 = smem_u32(smS + s * SF_BYTES);
+          // the stage's scale slot: A (4 columns), B rows 0..127 and 128..255 (4 each)
+          const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + s * kSfCols);
+          tc_cp_sf(sf, sf_desc(s0));
+          tc_cp_sf(sf + 4u, sf_desc(s0 + SF_A_BYTES));
+          tc_cp_sf(sf + 8u, sf_desc(s0 + SF_A_BYTES + 512));
 #pragma unroll
           for (int k = 0; k < BK8 / 32; ++k)
             tc_mma8(tmem_base, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc8(static_cast<uint32_t>(k)), sf,
                     sf + 4u, (kb | k) != 0 ? 1u : 0u);
           tc_commit(smem_u32(&ctl->empty[s]));
-          tc_commit(smem_u32(&ctl8->sf_empty[j]));
         }
         if (ok) tc_commit(smem_u32(&ctl->tfull[0]));
       }
@@ -1291,65 +1267,6 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
         if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[0]));
       }
     }
-  } else if (kFuse || warp >= 4) {
-    // ---------------- scale warps (6..9): one per TMEM lane quarter.  The
-    // scales of the next kSfAhead k-blocks are in flight in registers while
-    // the current one is written, so the global-memory latency stays off the
-    // MMA's critical path.  A cursor walks (tile, k-block) so the tile
-    // coordinates are derived once per tile: the scale warp runs once per
-    // k-block and would otherwise pace the MMA with its integer divisions.
-    constexpr int kSfAhead = 4;
-    const uint32_t q = static_cast<uint32_t>(warp & 3);
-    const uint32_t lane_off = (q * 32u) << 16;
-    const int my_tiles = blockIdx.x < a.num_tiles ? (a.num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
-    const int total = my_tiles * nkb;
-    SfCursor cur;
-    cur.start(a, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), kGroupM, a.mt, BM, 0, sfa, sfb, lane);
-    // this k-block's scales, replicated layout: column c holds row lane + 32 c
-    auto load = [&](uint32_t (&r)[12]) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        r[c] = cur.m0 + lane + 32 * c < a.M ? __ldg(cur.pa + lane + 32 * c) : 0x7f7f7f7fu;
-        r[4 + c] = __ldg(cur.pb + 32 * c);
-        r[8 + c] = __ldg(cur.pb + 128 + 32 * c);
-      }
-      cur.next(a, nkb, sfa, sfb, N, lane);
-    };
-    uint32_t ring[kSfAhead][12];
-#pragma unroll
-    for (int u = 0; u < kSfAhead; ++u)
-      if (u < total) load(ring[u]);
-    bool ok = true;
-    for (int base = 0; ok && base < total; base += kSfAhead) {
-#pragma unroll
-      for (int u = 0; u < kSfAhead; ++u) {
-        const int it = base + u;
-        if (it >= total) break;
-        const int s = it % kSfSlots8;
-        const uint32_t ph = (it / kSfSlots8) & 1;
-        bool free_slot = true;
-        if (lane == 0) free_slot = mbar_wait_bounded(smem_u32(&ctl8->sf_empty[s]), ph ^ 1, abort_flag);
-        free_slot = __shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0) != 0;
-        if (!free_slot) {
-          if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sf = tmem_base + lane_off + static_cast<uint32_t>(kSfBase + s * kSfCols);
-        const uint32_t ra[4] = {ring[u][0], ring[u][1], ring[u][2], ring[u][3]};
-        const uint32_t rb0[4] = {ring[u][4], ring[u][5], ring[u][6], ring[u][7]};
-        const uint32_t rb1[4] = {ring[u][8], ring[u][9], ring[u][10], ring[u][11]};
-        tc_st4(sf, ra);
-        tc_st4(sf + 4u, rb0);
-        tc_st4(sf + 8u, rb1);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl8->sf_full[s]));
-        if (it + kSfAhead < total) load(ring[u]);
-      }
-    }
   }
 
   tc_fence_before();
@@ -1369,16 +1286,18 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
 // SM moves half the wkv bytes of project8_kernel through shared memory.  Each
 // CTA's TMEM holds the scales of its own 128 rows of A (4 columns) and of all
 // 256 rows of B (8 columns), in the layout of project8_kernel (established by
-// a standalone probe on GB300); the scale warps of both CTAs arrive on the
-// even CTA's sf_full barrier (count 8).  Accumulator single-buffered.
+// a standalone probe on GB300): each CTA loads those scale words into its
+// stage, and the even CTA's tcgen05.cp.cta_group::2 copies each CTA's image
+// into its own TMEM.  Accumulator single-buffered.
 constexpr int STAGES82 = 6;
 constexpr int B82_BYTES = (BN / 2) * BK8;
 constexpr int STAGE82_BYTES = A8_BYTES + B82_BYTES;
 
-struct __align__(8) Ctl82 {
-  uint64_t sf_full[kSfSlots82];
-  uint64_t sf_empty[kSfSlots82];
-};
+// 2-D TMA load into this CTA's shared memory counted on the leader CTA's
+// barrier (cluster address `bar`), no swizzle.
+__device__ __forceinline__ void tma_load_sf_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
+  tma_load_2d_pair(dst, tmap, x, y, bar);
+}
 
 __device__ __forceinline__ void tc_mma8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
@@ -1399,32 +1318,27 @@ __device__ __forceinline__ uint32_t idesc82(uint32_t sf_id) {
 
 template <bool kFuse>
 __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
-    project82_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ProjArgs a,
-                     const uint32_t* __restrict__ sfa, const uint32_t* __restrict__ sfb) {
+    project82_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, ProjArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = smem;
   uint8_t* smB = smem + STAGES82 * A8_BYTES;
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + STAGES82 * STAGE82_BYTES);
-  Ctl82* ctl8 = reinterpret_cast<Ctl82*>(ctl + 1);
-  Comb8* comb = reinterpret_cast<Comb8*>((reinterpret_cast<uintptr_t>(ctl8 + 1) + 15) & ~uintptr_t(15));
+  uint8_t* smS = smem + STAGES82 * STAGE82_BYTES;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smS + STAGES82 * SF_BYTES);
+  Comb8* comb = reinterpret_cast<Comb8*>((reinterpret_cast<uintptr_t>(ctl + 1) + 15) & ~uintptr_t(15));
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const uint32_t rank = cluster_rank();
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
   const int nkb = a.K / BK8;
-  const int64_t N = static_cast<int64_t>(a.hc + 1) * a.H;
   volatile int* abort_flag = &ctl->abort;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES82; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
-    }
-    for (int j = 0; j < kSfSlots82; ++j) {
-      mbar_init(smem_u32(&ctl8->sf_full[j]), 8);
-      mbar_init(smem_u32(&ctl8->sf_empty[j]), 1);
     }
     mbar_init(smem_u32(&ctl->tfull[0]), 1);
     mbar_init(smem_u32(&ctl->tempty[0]), kFuse ? 8 : 16);
@@ -1435,6 +1349,8 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSA);
+    prefetch_tmap(&tmSB);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -1466,12 +1382,15 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
             break;
           }
           const uint32_t fb = smem_u32(&ctl->full[s]);
-          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * STAGE82_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (STAGE82_BYTES + SF_BYTES));
           const uint32_t leader_fb = map_to_cta(fb, 0);
-          tma_load_2d_pair(smem_u32(smA + s * A8_BYTES), &tmA, kb * BK8, mb2 * (2 * BM) + static_cast<int>(rank) * BM,
-                           leader_fb);
+          const int m0 = mb2 * (2 * BM) + static_cast<int>(rank) * BM;
+          tma_load_2d_pair(smem_u32(smA + s * A8_BYTES), &tmA, kb * BK8, m0, leader_fb);
           tma_load_4d_pair(smem_u32(smB + s * B82_BYTES), &tmB, kb, nb * (BN / 128) + static_cast<int>(rank),
                            leader_fb);
+          // this CTA's 128 rows of A scales, all 256 rows of B scales
+          tma_load_sf_pair(smem_u32(smS + s * SF_BYTES), &tmSA, m0, kb, leader_fb);
+          tma_load_sf_pair(smem_u32(smS + s * SF_BYTES + SF_A_BYTES), &tmSB, nb * BN, kb, leader_fb);
         }
       }
       if (rank == 0) {
@@ -1494,9 +1413,7 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % STAGES82;
           const uint32_t ph = (it / STAGES82) & 1;
-          const int j = it % kSfSlots82;
-          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag) ||
-              !mbar_wait_bounded(smem_u32(&ctl8->sf_full[j]), (it / kSfSlots82) & 1, abort_flag)) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag)) {
             if (!*abort_flag) raise_abort(ctl, a);
             ok = false;
             break;
@@ -1504,13 +1421,16 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(smA + s * A8_BYTES);
           const uint32_t b0 = smem_u32(smB + s * B82_BYTES);
-          const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + j * kSfCols);
+          const uint32_t s0 = smem_u32(smS + s * SF_BYTES);
+          const uint32_t sf = tmem_base + static_cast<uint32_t>(kSfBase + s * kSfCols);
+          tc_cp_sf_pair(sf, sf_desc(s0));
+          tc_cp_sf_pair(sf + 4u, sf_desc(s0 + SF_A_BYTES));
+          tc_cp_sf_pair(sf + 8u, sf_desc(s0 + SF_A_BYTES + 512));
 #pragma unroll
           for (int k = 0; k < BK8 / 32; ++k)
             tc_mma8_pair(tmem_base, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc82(static_cast<uint32_t>(k)),
                          sf, sf + 4u, (kb | k) != 0 ? 1u : 0u);
           tc_commit_pair(smem_u32(&ctl->empty[s]));
-          tc_commit_pair(smem_u32(&ctl8->sf_empty[j]));
         }
         if (ok) tc_commit_pair(smem_u32(&ctl->tfull[0]));
       }
@@ -1544,63 +1464,6 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
         if (lane == 0) mbar_arrive_cluster(leader_tempty);
       }
     }
-  } else if (kFuse || warp >= 4) {
-    // ---------------- scale warps (6..9 of both CTAs): this CTA's 128 rows of
-    // A and all 256 rows of B, kSfAhead k-blocks in flight in registers; a
-    // cursor derives the tile coordinates once per tile (as project8_kernel)
-    constexpr int kSfAhead = 4;
-    const uint32_t q = static_cast<uint32_t>(warp & 3);
-    const uint32_t lane_off = (q * 32u) << 16;
-    const uint32_t leader_sf = map_to_cta(smem_u32(&ctl8->sf_full[0]), 0);
-    const int my_tiles = pair < a.num_tiles ? (a.num_tiles - 1 - pair) / npairs + 1 : 0;
-    const int total = my_tiles * nkb;
-    SfCursor cur;
-    cur.start(a, pair, npairs, kGroupM2, a.mt2, 2 * BM, static_cast<int>(rank) * BM, sfa, sfb, lane);
-    auto load = [&](uint32_t (&r)[12]) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        r[c] = cur.m0 + lane + 32 * c < a.M ? __ldg(cur.pa + lane + 32 * c) : 0x7f7f7f7fu;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) r[4 + c] = __ldg(cur.pb + 32 * c);
-      cur.next(a, nkb, sfa, sfb, N, lane);
-    };
-    uint32_t ring[kSfAhead][12];
-#pragma unroll
-    for (int u = 0; u < kSfAhead; ++u)
-      if (u < total) load(ring[u]);
-    bool ok = true;
-    for (int base = 0; ok && base < total; base += kSfAhead) {
-#pragma unroll
-      for (int u = 0; u < kSfAhead; ++u) {
-        const int it = base + u;
-        if (it >= total) break;
-        const int s = it % kSfSlots82;
-        const uint32_t ph = (it / kSfSlots82) & 1;
-        bool free_slot = true;
-        if (lane == 0) free_slot = mbar_wait_bounded(smem_u32(&ctl8->sf_empty[s]), ph ^ 1, abort_flag);
-        free_slot = __shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0) != 0;
-        if (!free_slot) {
-          if (lane == 0 && !*abort_flag) raise_abort(ctl, a);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sf = tmem_base + lane_off + static_cast<uint32_t>(kSfBase + s * kSfCols);
-        const uint32_t ra[4] = {ring[u][0], ring[u][1], ring[u][2], ring[u][3]};
-        const uint32_t rb0[4] = {ring[u][4], ring[u][5], ring[u][6], ring[u][7]};
-        const uint32_t rb1[4] = {ring[u][8], ring[u][9], ring[u][10], ring[u][11]};
-        tc_st4(sf, ra);
-        tc_st4(sf + 4u, rb0);
-        tc_st4(sf + 8u, rb1);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        __syncwarp();
-        // the TMEM writes are ordered by wait::st and the tcgen05 fence; the
-        // arrive needs no cluster-scope memory fence of its own
-        if (lane == 0) mbar_arrive_remote(leader_sf + static_cast<uint32_t>(s * 8));
-        if (it + kSfAhead < total) load(ring[u]);
-      }
-    }
   }
 
   // No CTA leaves while its partner may still signal its barriers or read its
@@ -1619,7 +1482,8 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
 // Block-FP8 wkv into the operand layouts of project8_kernel: codes [K][N]
 // (kv = e @ wkv) -> [N/128][K/128][128][128] bytes, so each 128 x 128-byte
 // tile of wkv^T is 16 KB contiguous; scales [K/32][N] -> [K/128][N] words,
-// byte j of word (kb, n) = scale of rows kb*128 + 32 j .. +31 of column n.
+// byte j of word (kb, n) = scale of rows kb*128 + 32 j .. +31 of column n,
+// the words of each 128 columns in tcgen05.cp image order (sf_word_index).
 __global__ void pack_wkv8_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ sf, int64_t K,
                                  int64_t N, uint8_t* __restrict__ wt, uint32_t* __restrict__ sft) {
   __shared__ uint8_t tile[32][33];
@@ -1640,7 +1504,7 @@ __global__ void pack_wkv8_kernel(const uint8_t* __restrict__ w, const uint8_t* _
     if (n < N && kb < K / 128) {
       uint32_t word = 0;
       for (int j = 0; j < 4; ++j) word |= static_cast<uint32_t>(sf[(kb * 4 + j) * N + n]) << (8 * j);
-      sft[kb * N + n] = word;
+      sft[kb * N + sf_word_index(n)] = word;
     }
   }
 }
@@ -1752,6 +1616,23 @@ int make_tmap_wkv8(CUtensorMap* tm, const void* base, uint64_t N, uint64_t K, ui
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ENGRAM_E_CUDA, "cuTensorMapEncodeTiled(wkv8) failed (%d)", static_cast<int>(r));
+  return ENGRAM_OK;
+}
+
+// Scale words as a 2-D uint32 tensor [rows][cols] (cols contiguous); a box is
+// box_cols consecutive words of one row, no swizzle.
+int make_tmap_sf(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols) {
+  EncodeTiledFn enc;
+  int rc = get_encode_fn(&enc);
+  if (rc) return rc;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 4};
+  const cuuint32_t box[2] = {box_cols, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ENGRAM_E_CUDA, "cuTensorMapEncodeTiled(scales) failed (%d)", static_cast<int>(r));
   return ENGRAM_OK;
 }
 
@@ -1883,10 +1764,10 @@ int launch(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB
 bool use_fp8_pair() { return kernel_options().fp8_pair != 0; }
 
 // Argument checks and set-up of the FP8 entry points.
+// tm[0..3]: e8, packed wkv8, A scales, B scales.
 int prepare8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K, const uint8_t* w8_d,
              const uint32_t* sfb_d, int32_t hidden, int32_t hc, const uint16_t* h_d, const float* q_w_d,
-             const float* k_w_d, float* partials_d, int32_t* status_d, bool pair, ProjArgs* a, CUtensorMap* tmA,
-             CUtensorMap* tmB) {
+             const float* k_w_d, float* partials_d, int32_t* status_d, bool pair, ProjArgs* a, CUtensorMap* tm) {
   if (n_tokens < 0) return fail(ENGRAM_E_INVALID, "n_tokens < 0");
   if (K < BK8 || K % BK8 != 0 || K > (int64_t(1) << 20))
     return fail(ENGRAM_E_SHAPE, "K %lld must be a positive multiple of 128", (long long)K);
@@ -1897,13 +1778,17 @@ int prepare8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64
   if (!e8_d || !sfa_d || !w8_d || !sfb_d || !h_d || !q_w_d || !k_w_d || !partials_d)
     return fail(ENGRAM_E_INVALID, "null device pointer");
   if (!aligned(e8_d, 16) || !aligned(w8_d, 16) || !aligned(h_d, 16) || !aligned(partials_d, 16) ||
-      !aligned(sfa_d, 4) || !aligned(sfb_d, 4))
-    return fail(ENGRAM_E_ALIGN, "e8, wkv8, h and partials must be 16-byte aligned, the scales 4-byte");
+      !aligned(sfa_d, 16) || !aligned(sfb_d, 16))
+    return fail(ENGRAM_E_ALIGN, "e8, wkv8, h, partials and the scales must be 16-byte aligned");
   int rc = check_device(nullptr);
   if (rc) return rc;
   const int64_t N = static_cast<int64_t>(hc + 1) * hidden;
-  if ((rc = make_tmap8(tmA, e8_d, static_cast<uint64_t>(n_tokens), static_cast<uint64_t>(K), BM))) return rc;
-  if ((rc = make_tmap_wkv8(tmB, w8_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), pair ? 1 : 2))) return rc;
+  const uint64_t t128 = static_cast<uint64_t>((n_tokens + 127) / 128 * 128);
+  if ((rc = make_tmap8(&tm[0], e8_d, static_cast<uint64_t>(n_tokens), static_cast<uint64_t>(K), BM))) return rc;
+  if ((rc = make_tmap_wkv8(&tm[1], w8_d, static_cast<uint64_t>(N), static_cast<uint64_t>(K), pair ? 1 : 2)))
+    return rc;
+  if ((rc = make_tmap_sf(&tm[2], sfa_d, static_cast<uint64_t>(K / BK8), t128, BM))) return rc;
+  if ((rc = make_tmap_sf(&tm[3], sfb_d, static_cast<uint64_t>(K / BK8), static_cast<uint64_t>(N), BN))) return rc;
   *a = ProjArgs{};
   a->M = n_tokens;
   a->K = static_cast<int32_t>(K);
@@ -1924,13 +1809,11 @@ int prepare8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64
 }
 
 size_t project8_smem_bytes(bool pair) {
-  return (pair ? 1024 + STAGES82 * STAGE82_BYTES + sizeof(SmemCtl) + sizeof(Ctl82)
-               : 1024 + STAGES8 * STAGE8_BYTES + sizeof(SmemCtl) + sizeof(Ctl8)) +
-         16 + sizeof(Comb8);
+  return (pair ? 1024 + STAGES82 * (STAGE82_BYTES + SF_BYTES) : 1024 + STAGES8 * (STAGE8_BYTES + SF_BYTES)) +
+         sizeof(SmemCtl) + 16 + sizeof(Comb8);
 }
 
-int launch8(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB, const ProjArgs& a,
-            const uint32_t* sfa, const uint32_t* sfb, cudaStream_t st) {
+int launch8(bool pair, bool fused, const CUtensorMap* tm, const ProjArgs& a, cudaStream_t st) {
   const void* fn = pair ? (fused ? reinterpret_cast<const void*>(&project82_kernel<true>)
                                  : reinterpret_cast<const void*>(&project82_kernel<false>))
                         : (fused ? reinterpret_cast<const void*>(&project8_kernel<true>)
@@ -1978,11 +1861,11 @@ int launch8(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tm
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
   if (pair)
-    err = fused ? cudaLaunchKernelEx(&cfg, project82_kernel<true>, tmA, tmB, a, sfa, sfb)
-                : cudaLaunchKernelEx(&cfg, project82_kernel<false>, tmA, tmB, a, sfa, sfb);
+    err = fused ? cudaLaunchKernelEx(&cfg, project82_kernel<true>, tm[0], tm[1], tm[2], tm[3], a)
+                : cudaLaunchKernelEx(&cfg, project82_kernel<false>, tm[0], tm[1], tm[2], tm[3], a);
   else
-    err = fused ? cudaLaunchKernelEx(&cfg, project8_kernel<true>, tmA, tmB, a, sfa, sfb)
-                : cudaLaunchKernelEx(&cfg, project8_kernel<false>, tmA, tmB, a, sfa, sfb);
+    err = fused ? cudaLaunchKernelEx(&cfg, project8_kernel<true>, tm[0], tm[1], tm[2], tm[3], a)
+                : cudaLaunchKernelEx(&cfg, project8_kernel<false>, tm[0], tm[1], tm[2], tm[3], a);
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "project8 kernel launch: %s", cudaGetErrorString(err));
   return check_launch("project8 kernel");
 }
@@ -2144,13 +2027,13 @@ extern "C" int engram_project_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, in
   if (!v_d && n_tokens > 0) return fail(ENGRAM_E_INVALID, "null device pointer");
   if (v_d && !aligned(v_d, 16)) return fail(ENGRAM_E_ALIGN, "v must be 16-byte aligned");
   ProjArgs a;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tm[4];
   const bool pair = use_fp8_pair();
   int rc = prepare8(e8_d, sfa_d, n_tokens, K, w8_packed_d, sfb_d, hidden, hc, h_d, q_w_d, k_w_d, partials_d,
-                    status_d, pair, &a, &tmA, &tmB);
+                    status_d, pair, &a, tm);
   if (rc || n_tokens == 0) return rc;
   a.v = v_d;
-  return launch8(pair, false, tmA, tmB, a, sfa_d, sfb_d, as_stream(stream));
+  return launch8(pair, false, tm, a, as_stream(stream));
 }
 
 extern "C" int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_d, int64_t n_tokens, int64_t K,
@@ -2175,10 +2058,10 @@ extern "C" int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_
                            stream);
   }
   ProjArgs a;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tm[4];
   const bool pair = use_fp8_pair();
   int rc = prepare8(e8_d, sfa_d, n_tokens, K, w8_packed_d, sfb_d, hidden, hc, h_d, q_w_d, k_w_d,
-                    static_cast<float*>(workspace_d), status_d, pair, &a, &tmA, &tmB);
+                    static_cast<float*>(workspace_d), status_d, pair, &a, tm);
   if (rc || n_tokens == 0) return rc;
   const int mt_ws = 2 * a.mt2;
   a.cnt = reinterpret_cast<int32_t*>(base + ws.counters_off);
@@ -2193,7 +2076,7 @@ extern "C" int engram_project_gate_fp8(const uint8_t* e8_d, const uint32_t* sfa_
   cudaStream_t st = as_stream(stream);
   cudaError_t err = cudaMemsetAsync(a.cnt, 0, ws.counter_words * sizeof(int32_t), st);
   if (err != cudaSuccess) return fail(ENGRAM_E_CUDA, "cudaMemsetAsync(counters): %s", cudaGetErrorString(err));
-  return launch8(pair, true, tmA, tmB, a, sfa_d, sfb_d, st);
+  return launch8(pair, true, tm, a, st);
 }
 
 extern "C" int engram_selftest_wait(int32_t which, int32_t* scratch_d, int32_t* status_d, void* stream) {

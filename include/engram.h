@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define ENGRAM_ABI_VERSION 2
+#define ENGRAM_ABI_VERSION 3
 
 #define ENGRAM_MAX_LAYERS 8
 #define ENGRAM_MAX_NGRAM 4   /* n-gram orders 2..max_ngram; history depth max_ngram-1 */
@@ -243,14 +243,20 @@ int engram_hash_gather(const engram_layout* layout, int32_t layer, const int32_t
 
 /* The gather for the block-scaled FP8 projection: the rows are copied as
  * stored instead of dequantised ([P-O1] §2.3: E4M3 payload with E8M0 scales
- * per 32 elements).  For position t and column j:
- *   e8_d[t][256 j + c]          = weight byte c of row row_ids_d[t][j]
- *   sf_d[(2 j + b / 4) * n_tokens + t], byte b % 4 = scale byte b of that row
+ * per 32 elements).  With T128 = n_tokens rounded up to a multiple of 128 and
+ * P(t) = (t & ~127) | ((t & 31) << 2) | ((t >> 5) & 3), for position t and
+ * column j:
+ *   e8_d[t][256 j + c]                  = weight byte c of row row_ids_d[t][j]
+ *   sf_d[(2 j + b / 4) * T128 + P(t)], byte b % 4 = scale byte b of that row
  * i.e. the scales are grouped per 128-element k-block, one 32-bit word of four
- * E8M0 scales per (k-block, position).  A row id outside [0, total_rows) sets
- * ENGRAM_ST_BAD_ROW and gives zero bytes with scales 127 (the value 0).
+ * E8M0 scales per (k-block, position), and within each 128 positions the word
+ * of position p0 + r + 32 c sits at p0 + 4 r + c: the 512-byte image the FP8
+ * projection copies into tensor memory as it is (tcgen05.cp).  Positions
+ * n_tokens .. T128-1 get scale words 0x7F7F7F7F.  A row id outside [0,
+ * total_rows) sets ENGRAM_ST_BAD_ROW and gives zero bytes with scales 127
+ * (the value 0).
  *   e8_d  uint8 [n_tokens][n_cols*256], 16-byte aligned
- *   sf_d  uint32 [n_cols*2][n_tokens], 4-byte aligned */
+ *   sf_d  uint32 [n_cols*2][T128], 16-byte aligned */
 int engram_gather_fp8(const uint8_t* table_d, int64_t total_rows, int64_t table_bytes, const int32_t* row_ids_d,
                       int64_t n_tokens, int32_t n_cols, uint8_t* e8_d, uint32_t* sf_d, int32_t* status_d,
                       void* stream);
@@ -280,8 +286,8 @@ int engram_hash_gather_step(const engram_layout* layout, int32_t layer, const in
                             uint16_t* e_d, uint8_t* mask_d, int32_t* row_ids_d, int32_t* status_d, void* stream);
 
 /* engram_hash_gather_step with the FP8 outputs of engram_gather_fp8
- * (e8_d uint8 [batch][n_cols*256] 16-byte aligned, sf_d uint32 [n_cols*2][batch]
- * 4-byte aligned). */
+ * (e8_d uint8 [batch][n_cols*256] 16-byte aligned, sf_d uint32
+ * [n_cols*2][batch rounded up to 128] 16-byte aligned, in that call's order). */
 int engram_hash_gather_step_fp8(const engram_layout* layout, int32_t layer, const int32_t* raw_ids_d,
                                 const int32_t* slots_d, int32_t batch, const int32_t* token_map_d,
                                 int64_t vocab_raw, int32_t* hist_d, int64_t n_slots, const uint8_t* table_d,
@@ -400,12 +406,16 @@ int engram_project(const uint16_t* e_d, int64_t n_tokens, int64_t K, const uint1
  * operand layouts of the FP8 projection: w8_packed_d uint8, K*N bytes, tiles
  * [N/128][K/128][128][128] (element (k, n) at ((n/128 * K/128 + k/128) * 128
  * + n%128) * 128 + k%128); sf_packed_d uint32 [K/128][N], byte j of word
- * (kb, n) = the scale of rows kb*128 + 32 j .. +31.  K and N multiples of 128. */
+ * (kb, P(n)) = the scale of rows kb*128 + 32 j .. +31 of column n, with P the
+ * order within each 128 columns of engram_gather_fp8's scales.  K and N
+ * multiples of 128; sf_packed_d 16-byte aligned for the projection. */
 int engram_pack_wkv_fp8(const uint8_t* w8_d, const uint8_t* sf_d, int64_t K, int64_t N, uint8_t* w8_packed_d,
                         uint32_t* sf_packed_d, void* stream);
 
 /* engram_project on FP8 operands: e in the engram_gather_fp8 form (e8_d uint8
- * [n_tokens][K], sfa_d uint32 [K/128][n_tokens]) and the packed FP8 wkv.  The
+ * [n_tokens][K], sfa_d uint32 [K/128][T128], 16-byte aligned) and the packed
+ * FP8 wkv.  The scale words travel with the operand tiles (TMA) and are
+ * copied into tensor memory by the MMA-issuing thread (tcgen05.cp); the
  * tensor cores take the E4M3 values with their E8M0 scales (tcgen05.mma
  * kind::mxf8f6f4, block size 32) and accumulate in fp32; the outputs
  * (partials_d, v_d) are those of engram_project.  K % 128 == 0; other

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_struct_sizes_match(lib):
     assert lib.engram_layout_size() == ctypes.sizeof(eg._Layout)
     assert lib.engram_layout_params_size() == ctypes.sizeof(eg._LayoutParams)
-    assert lib.engram_abi_version() == 2
+    assert lib.engram_abi_version() == 3
 
 
 @pytest.mark.parametrize("vocab,base,layers", [(1000, 4099, [1]), (99092, 2_000_000, [1]),

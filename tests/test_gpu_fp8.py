@@ -25,8 +25,14 @@ def _gpu():
 
 
 def _sf_bytes(sf_words: torch.Tensor) -> np.ndarray:
-    """int32 [2C][T] words -> uint8 [2C][T][4]."""
+    """int32 [2C][T128] words -> uint8 [2C][T128][4]."""
     return sf_words.cpu().numpy().view(np.uint8).reshape(sf_words.shape[0], sf_words.shape[1], 4)
+
+
+def _sf_perm(i: np.ndarray) -> np.ndarray:
+    """Documented word order of a block-FP8 scale row: within each 128 words,
+    word 4 r + c holds position (or column) r + 32 c."""
+    return (i // 128) * 128 + (i % 32) * 4 + (i % 128) // 32
 
 
 def test_gather_fp8_copies_rows_and_groups_scales():
@@ -49,9 +55,15 @@ def test_gather_fp8_copies_rows_and_groups_scales():
     ref_w[bad] = 0
     ref_s[bad] = 127
     assert (e8.cpu().numpy().reshape(T, 24, 256) == ref_w).all()
-    sb = _sf_bytes(sf)                                         # [48][T][4]
-    got_s = sb.reshape(24, 2, T, 4).transpose(2, 0, 1, 3).reshape(T, 24, 8)
+    T128 = (T + 127) // 128 * 128
+    assert tuple(sf.shape) == (48, T128)
+    sb = _sf_bytes(sf)                                         # [48][T128][4]
+    got_s = sb[:, _sf_perm(np.arange(T))].reshape(24, 2, T, 4).transpose(2, 0, 1, 3).reshape(T, 24, 8)
     assert (got_s == ref_s).all()
+    # positions T .. T128-1 of the last 128-block hold scale 127 (the value 1)
+    assert (sb[:, _sf_perm(np.arange(T, T128))] == 127).all()
+    # a permutation of each 128-block: every word is some position's
+    assert sorted(_sf_perm(np.arange(T128)).tolist()) == list(range(T128))
 
 
 def test_hash_gather_fp8_matches_hash_and_gather():
@@ -79,7 +91,7 @@ def test_pack_wkv_fp8_layout():
     idx = (((n // 128) * (K // 128) + k // 128) * 128 + n % 128) * 128 + k % 128
     assert (got[idx] == w8).all()
     words = sfp.cpu().numpy().view(np.uint8).reshape(K // 128, N, 4)
-    assert (words == sf.reshape(K // 128, 4, N).transpose(0, 2, 1)).all()
+    assert (words[:, _sf_perm(np.arange(N))] == sf.reshape(K // 128, 4, N).transpose(0, 2, 1)).all()
 
 
 def _fp8_layer_case(name, T_cut=None, seed=0, sample=None):
