@@ -100,6 +100,42 @@ def test_packed_prefill_matches_oracle(K, dil):
     assert (got[100] != bf16_bits_to_f64(h_bits[100])).any() == (K > 1)
 
 
+@pytest.mark.parametrize("hc,H,K,dil", [(1, 256, 4, 3), (3, 768, 2, 2), (6, 512, 4, 3), (8, 1280, 3, 1)])
+def test_stream_groups_and_widths_match_oracle(hc, H, K, dil):
+    """Stream counts that leave a block's group of four streams partly empty
+    or need two groups, and hidden sizes that leave warps of the last
+    512-channel block without channels: packed prefill against the oracle,
+    and one sequence in two chunks with the ring carried bit-identical to one
+    pass."""
+    T = 97 + 64
+    cu = np.array([0, 97, T])
+    mask, g, v_bits, h_bits, w, gamma = _inputs(T, hc, H, K, 11 + hc, dead=range(20, 26))
+    md = torch.from_numpy(mask.astype(np.uint8)).to(DEV)
+    wd, gd = f32(w), f32(gamma)
+    h = bf16(h_bits)
+    st = status()
+    eg.engram_short_conv_add(f32(g), bf16(v_bits), h, md, wd, gd, dil, 1e-6, cu_seqlens=i64(cu), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    exact, y, gated, n, _ = _oracle(cu, mask, g, v_bits, h_bits, w, gamma, dil, 1e-6)
+    got = bf16_bits_to_f64(bits(h))
+    err = _fp32_bound(bf16_bits_to_f64(h_bits), gated, y, n, w.astype(np.float64), dil, cu)
+    ok = _within(got, exact, err)
+    assert ok.all(), (np.argwhere(~ok)[:5], got[~ok][:5], exact[~ok][:5])
+    # the first sequence again, as chunks of 40 and 57 with the ring carried
+    R = (K - 1) * dil
+    ring = torch.zeros((1, max(R, 1), hc, H), dtype=torch.float32, device=DEV)
+    head = torch.zeros(1, dtype=torch.int32, device=DEV)
+    outs = []
+    for a, b in [(0, 40), (40, 97)]:
+        hk = bf16(h_bits[a:b])
+        eg.engram_short_conv_add(f32(g[a:b]), bf16(v_bits[a:b]), hk, md[a:b].contiguous(), wd, gd, dil, 1e-6,
+                                 cu_seqlens=i64([0, b - a]), state=ring, state_head=head)
+        outs.append(bits(hk))
+    torch.cuda.synchronize()
+    assert (np.concatenate(outs) == bits(h)[:97]).all()
+
+
 def test_chunked_prefill_with_state_equals_one_pass():
     """A 300-position sequence in chunks of 5, 1, 144, 150 with the ring carried:
     every chunk matches the oracle's whole-sequence result, the device chunks
