@@ -1155,8 +1155,11 @@ def generic_bench(args, w, flush, dev):
                                         status)
         if ev is not None:
             ev[1].record(stream)
-        eg.engram_project_gate(bufs["e"], layer.wkv_packed, h, layer.q_w, layer.k_w, bufs["mask"], layer.eps,
-                               layer.clamp, layer.score_scale, None, bufs["work"], status)
+        # the two kernels engram_project_gate runs at K < 3200, with an event between them
+        eg.engram_project(bufs["e"], layer.wkv_packed, h, layer.q_w, layer.k_w, bufs["partials"], bufs["v"], status)
+        if ev is not None:
+            ev[3].record(stream)
+        eg.engram_gate_add(bufs["partials"], bufs["v"], h, bufs["mask"], layer.eps, layer.clamp, layer.score_scale)
         if ev is not None:
             ev[2].record(stream)
 
@@ -1164,7 +1167,7 @@ def generic_bench(args, w, flush, dev):
         flush()
         run()
     n = args.generic_steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
     for k in range(n):
         flush()
         run(evs[k])
@@ -1172,6 +1175,8 @@ def generic_bench(args, w, flush, dev):
     step = statistics.mean(ev[0].elapsed_time(ev[2]) for ev in evs) / 1e3
     hg = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs) / 1e3
     proj = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs) / 1e3
+    proj_only = statistics.mean(ev[1].elapsed_time(ev[3]) for ev in evs) / 1e3
+    gate_only = statistics.mean(ev[3].elapsed_time(ev[2]) for ev in evs) / 1e3
     C = lay.n_cols
     hg_bytes = 4 + 2 * C * R * 2
     flops = 2.0 * C * R * (wg.hc + 1) * wg.hidden
@@ -1197,7 +1202,10 @@ def generic_bench(args, w, flush, dev):
                        "L2 flushed", "steps": n,
            "step_ms": step * 1e3, "tokens_per_s": T / step, "hash_gather_ms": hg * 1e3,
            "hash_gather_gbs": hg_bytes * T / hg / 1e9, "hash_gather_bytes_per_token": hg_bytes,
-           "project_gate_ms": proj * 1e3, "project_tflops": flops * T / proj / 1e12,
+           "project_gate_ms": proj * 1e3, "project_gate_tflops": flops * T / proj / 1e12,
+           "project_ms": proj_only * 1e3, "project_tflops": flops * T / proj_only / 1e12,
+           "gate_ms": gate_only * 1e3,
+           "gate_gbs": GATE_BYTES_PER_TOKEN(wg.hc, wg.hidden) * T / gate_only / 1e9,
            "device_status": int(status.item()), **base}
     del table
     return out
