@@ -1555,7 +1555,7 @@ int get_encode_fn(EncodeTiledFn* out) {
 // 2-D bf16 tensor [rows][cols] (cols contiguous), box = box_rows x 64 columns,
 // 128-byte swizzle, zero fill outside the tensor.
 int make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  EncodeTiledFn enc;
+  EncodeTiledFn enc = nullptr;
   int rc = get_encode_fn(&enc);
   if (rc) return rc;
   const cuuint64_t dims[2] = {cols, rows};
@@ -1572,7 +1572,7 @@ int make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, u
 // Packed wkv as a 4-D tensor {64, 128, K/64, N/128} (innermost first); a box
 // covers one k-block of `nblocks` consecutive 128-row blocks, 128-byte swizzle.
 int make_tmap_wkv(CUtensorMap* tm, const void* base, uint64_t N, uint64_t K, uint32_t nblocks) {
-  EncodeTiledFn enc;
+  EncodeTiledFn enc = nullptr;
   int rc = get_encode_fn(&enc);
   if (rc) return rc;
   const cuuint64_t dims[4] = {64, 128, K / 64, N / 128};
@@ -1588,7 +1588,7 @@ int make_tmap_wkv(CUtensorMap* tm, const void* base, uint64_t N, uint64_t K, uin
 
 // 2-D byte tensor [rows][cols] (E4M3 e), box = box_rows x 128 bytes, 128-byte swizzle.
 int make_tmap8(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  EncodeTiledFn enc;
+  EncodeTiledFn enc = nullptr;
   int rc = get_encode_fn(&enc);
   if (rc) return rc;
   const cuuint64_t dims[2] = {cols, rows};
@@ -1605,7 +1605,7 @@ int make_tmap8(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, 
 // Packed FP8 wkv as a 4-D byte tensor {128, 128, K/128, N/128}; a box covers
 // one k-block of `nblocks` consecutive 128-row blocks.
 int make_tmap_wkv8(CUtensorMap* tm, const void* base, uint64_t N, uint64_t K, uint32_t nblocks) {
-  EncodeTiledFn enc;
+  EncodeTiledFn enc = nullptr;
   int rc = get_encode_fn(&enc);
   if (rc) return rc;
   const cuuint64_t dims[4] = {128, 128, K / 128, N / 128};
@@ -1622,7 +1622,7 @@ int make_tmap_wkv8(CUtensorMap* tm, const void* base, uint64_t N, uint64_t K, ui
 // Scale words as a 2-D uint32 tensor [rows][cols] (cols contiguous); a box is
 // box_cols consecutive words of one row, no swizzle.
 int make_tmap_sf(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols) {
-  EncodeTiledFn enc;
+  EncodeTiledFn enc = nullptr;
   int rc = get_encode_fn(&enc);
   if (rc) return rc;
   const cuuint64_t dims[2] = {cols, rows};

@@ -55,23 +55,16 @@ __device__ __forceinline__ void unpack8(const uint4 x, float (&f)[8]) {
 }
 
 
-// x * sigmoid(x) = x / (1 + 2^(-x log2 e)) with the hardware base-2
-// exponential and reciprocal approximations (PTX ex2.approx.ftz.f32, rcp.approx.ftz.f32;
-// each about 2^-22 relative): a few ulp plus about 1.2 |x| ulp from rounding
-// the exponent's argument.  Inputs below -126/log2 e give 2^(..) = inf and
-// a result of -0, the limit of x sigmoid(x).
-__device__ __forceinline__ float silu(float x) {
-  float e, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-  return x * r;
-}
-
 __device__ __forceinline__ uint64_t f2_bf16(uint32_t w) {  // the two bf16 of a word, widened
   return f2(bf16_lo(w), bf16_hi(w));
 }
 
-// silu of both lanes, as silu() above
+// x * sigmoid(x) = x / (1 + 2^(-x log2 e)) of both lanes of a packed pair,
+// with the hardware base-2 exponential and reciprocal approximations (PTX
+// ex2.approx.ftz.f32, rcp.approx.ftz.f32; each about 2^-22 relative): a few
+// ulp plus about 1.2 |x| ulp from rounding the exponent's argument.  Inputs
+// below -126/log2 e give 2^(..) = inf and a result of -0, the limit of
+// x sigmoid(x).
 __device__ __forceinline__ uint64_t silu2(uint64_t x) {
   float m0, m1, e0, e1, d0, d1, r0, r1;
   f2_split(f2_mul(x, f2(-1.4426950408889634f, -1.4426950408889634f)), m0, m1);
