@@ -954,13 +954,15 @@ __device__ __forceinline__ void tma_load_sf(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
-// Unfused FP8 projection (partial sums of the key tiles, bf16 v): 16 warps.
+// Unfused FP8 projection (partial sums of the key tiles, bf16 v): 10 warps.
 // Warp 0 loads operands and scales, warp 1 copies the scales to TMEM and
-// issues the MMAs, warps 8..15 are the epilogue, two per lane quarter (warp
-// w: quarter w & 3, tile columns half * 128 .. +127 with half = (w >> 2) &
-// 1; a warp may only reach TMEM lane quarter w & 3).  Warps 2..7 idle.  The
-// fused form has the 6-warp layout of kThreads8.
-constexpr int kThreads8u = 512;
+// issues the MMAs, warps 2..9 are the epilogue, two per lane quarter (warp
+// w, numbered e = w + 8 inside the epilogue: quarter e & 3 = w & 3, since a
+// warp may only reach TMEM lane quarter w & 3; tile columns half * 128 ..
+// +127 with half = (e >> 2) & 1, so each quarter has one warp per half).  Ten warps leave each thread up to 200
+// registers, so the epilogue keeps a key tile's h in registers without
+// spilling.  The fused form has the 6-warp layout of kThreads8.
+constexpr int kThreads8u = 320;
 
 // The two halves of a key tile's partial sums meet in shared memory: the
 // second half writes its (dot, kk, hh) and arrives on its quarter's barrier
@@ -1242,9 +1244,9 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
       tc_commit(smem_u32(&ctl->drain));
       mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr);
     }
-  } else if (kFuse ? warp < 6 : warp >= 8) {
+  } else if (!kFuse || warp < 6) {
     if constexpr (!kFuse) {
-      epilogue8_split<false>(a, ctl, comb, warp, lane, tmem_base, static_cast<int>(blockIdx.x),
+      epilogue8_split<false>(a, ctl, comb, warp + 8, lane, tmem_base, static_cast<int>(blockIdx.x),
                              static_cast<int>(gridDim.x), 0, smem_u32(&ctl->tempty[0]), abort_flag);
     } else {
       // ---------------- epilogue (warps 2..5)
@@ -1437,9 +1439,9 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
       tc_commit_pair(smem_u32(&ctl->drain));
       mbar_wait_bounded(smem_u32(&ctl->drain), 0, nullptr);
     }
-  } else if (kFuse ? warp < 6 : warp >= 8) {
+  } else if (!kFuse || warp < 6) {
     if constexpr (!kFuse) {
-      epilogue8_split<true>(a, ctl, comb, warp, lane, tmem_base, pair, npairs, rank,
+      epilogue8_split<true>(a, ctl, comb, warp + 8, lane, tmem_base, pair, npairs, rank,
                             map_to_cta(smem_u32(&ctl->tempty[0]), 0), abort_flag);
     } else {
       // ---------------- epilogue (warps 2..5 of both CTAs; each its own 128 rows)
