@@ -944,24 +944,15 @@ __device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-// 2-D TMA load into this CTA's shared memory, no swizzle handling needed by
-// the caller (the tensor map fixes the layout).
-__device__ __forceinline__ void tma_load_sf(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
 // Unfused FP8 projection (partial sums of the key tiles, bf16 v): 10 warps.
 // Warp 0 loads operands and scales, warp 1 copies the scales to TMEM and
 // issues the MMAs, warps 2..9 are the epilogue, two per lane quarter (warp
 // w, numbered e = w + 8 inside the epilogue: quarter e & 3 = w & 3, since a
 // warp may only reach TMEM lane quarter w & 3; tile columns half * 128 ..
-// +127 with half = (e >> 2) & 1, so each quarter has one warp per half).  Ten warps leave each thread up to 200
-// registers, so the epilogue keeps a key tile's h in registers without
-// spilling.  The fused form has the 6-warp layout of kThreads8.
+// +127 with half = (e >> 2) & 1, so each quarter has one warp per half).
+// Ten warps leave each thread up to 200 registers, so the epilogue keeps a
+// key tile's h in registers without spilling.  The fused form has the
+// 6-warp layout of kThreads8.
 constexpr int kThreads8u = 320;
 
 // The two halves of a key tile's partial sums meet in shared memory: the
@@ -1197,8 +1188,8 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
           mbar_arrive_expect_tx(fb, STAGE8_BYTES + SF_BYTES);
           tma_load_2d(smem_u32(smA + s * A8_BYTES), &tmA, kb * BK8, mb * BM, fb);
           tma_load_4d(smem_u32(smB + s * B8_BYTES), &tmB, kb, nb * (BN / 128), fb);
-          tma_load_sf(smem_u32(smS + s * SF_BYTES), &tmSA, mb * BM, kb, fb);
-          tma_load_sf(smem_u32(smS + s * SF_BYTES + SF_A_BYTES), &tmSB, nb * BN, kb, fb);
+          tma_load_2d(smem_u32(smS + s * SF_BYTES), &tmSA, mb * BM, kb, fb);
+          tma_load_2d(smem_u32(smS + s * SF_BYTES + SF_A_BYTES), &tmSB, nb * BN, kb, fb);
         }
       }
       for (int j = (it > STAGES8 ? it - STAGES8 : 0); j < it; ++j)
@@ -1295,11 +1286,6 @@ constexpr int STAGES82 = 6;
 constexpr int B82_BYTES = (BN / 2) * BK8;
 constexpr int STAGE82_BYTES = A8_BYTES + B82_BYTES;
 
-// 2-D TMA load into this CTA's shared memory counted on the leader CTA's
-// barrier (cluster address `bar`), no swizzle.
-__device__ __forceinline__ void tma_load_sf_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
-  tma_load_2d_pair(dst, tmap, x, y, bar);
-}
 
 __device__ __forceinline__ void tc_mma8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
@@ -1391,8 +1377,8 @@ __global__ void __launch_bounds__(kFuse ? kThreads8 : kThreads8u, 1)
           tma_load_4d_pair(smem_u32(smB + s * B82_BYTES), &tmB, kb, nb * (BN / 128) + static_cast<int>(rank),
                            leader_fb);
           // this CTA's 128 rows of A scales, all 256 rows of B scales
-          tma_load_sf_pair(smem_u32(smS + s * SF_BYTES), &tmSA, m0, kb, leader_fb);
-          tma_load_sf_pair(smem_u32(smS + s * SF_BYTES + SF_A_BYTES), &tmSB, nb * BN, kb, leader_fb);
+          tma_load_2d_pair(smem_u32(smS + s * SF_BYTES), &tmSA, m0, kb, leader_fb);
+          tma_load_2d_pair(smem_u32(smS + s * SF_BYTES + SF_A_BYTES), &tmSB, nb * BN, kb, leader_fb);
         }
       }
       if (rank == 0) {
@@ -1759,10 +1745,11 @@ int launch(bool pair, bool fused, const CUtensorMap& tmA, const CUtensorMap& tmB
 
 // The single-CTA FP8 kernel is the default.  The CTA pair moves a third fewer
 // operand bytes per SM, but the per-SM MMA rate is the same (an M = 256 pair
-// MMA takes as many cycles as an M = 128 one), its two CTAs gate each other
-// at every k-block, and both keep a single accumulator: on 16,384 tokens the
-// two measure within 2 % of each other (1.94-1.98 ms).
-// engram_kernel_options.fp8_pair selects the pair.
+// MMA takes as many cycles as an M = 128 one), both issue the same three
+// scale copies per k-block per SM, and both keep a single accumulator: on
+// 16,384 tokens the two measure within 2 % of each other (1.80-1.82 ms), and
+// at 128 tokens the single CTA's 100 tiles fit one wave (43 vs 59 us for
+// projection + gate).  engram_kernel_options.fp8_pair selects the pair.
 bool use_fp8_pair() { return kernel_options().fp8_pair != 0; }
 
 // Argument checks and set-up of the FP8 entry points.
@@ -1934,7 +1921,7 @@ constexpr int64_t kFusedMinK = 3200;
 // The block-FP8 projection keeps a single accumulator buffer (TMEM also holds
 // the scale factors), so its fused epilogue cannot overlap the next tile's
 // main loop; the two kernels are faster at every size measured (16,384
-// tokens, hidden 5120: 2.53 ms per layer step vs 3.22 ms fused).
+// tokens, hidden 5120: projection + gate 2.03 ms vs 2.53 ms fused).
 // engram_kernel_options.fp8_fused selects the fused FP8 kernel above 1536
 // tokens (for comparisons).
 bool use_fp8_fused() { return kernel_options().fp8_fused != 0; }
