@@ -176,3 +176,14 @@ def test_kernel_options_round_trip_and_range_checks(lib):
     finally:
         eg.set_kernel_options(**prev)
     assert eg.kernel_options() == prev
+
+
+def test_fp8_scale_layout_helpers():
+    """sf_cols rounds a token count up to whole 128-position blocks, and
+    sf_word_index is the order the header states for block-FP8 scale words:
+    within each 128 words, word 4r + c holds position (or column) r + 32c, a
+    permutation of the block."""
+    assert [eg.sf_cols(n) for n in (0, 1, 127, 128, 129, 16384)] == [0, 128, 128, 128, 256, 16384]
+    for base in (0, 128, 4096):
+        idx = [eg.sf_word_index(base + r + 32 * c) for r in range(32) for c in range(4)]
+        assert idx == list(range(base, base + 128))
