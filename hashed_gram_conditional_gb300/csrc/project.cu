@@ -62,7 +62,7 @@ constexpr int kGroupM = 16;  // M-blocks per raster group: e group + wkv wave fi
 constexpr int STAGES2 = 6;
 constexpr int B2_BYTES = (BN / 2) * BK * 2;
 constexpr int STAGE2_BYTES = A_BYTES + B2_BYTES;
-constexpr int kGroupM2 = 8;  // pair M-blocks (256 rows) per raster group
+constexpr int kGroupM2 = 16;  // pair M-blocks (4096 rows) per raster group: the e group (50 MB) stays in L2
 constexpr int kMaxHc = 8;
 
 struct ProjArgs {
